@@ -30,7 +30,8 @@
  * kv_end counts the keys after this step's append; an empty key range gives
  * out = 0 and lse = -inf; a ring needs window > 0 and
  * window + q_len - 1 <= ring_rows; a segment that fails validation writes
- * nothing and its rows read 0.
+ * nothing and its rows read 0; an append is gated by the slots it writes, an
+ * attention by every key it reads.
  */
 #include <math.h>
 #include <stdint.h>
@@ -95,8 +96,12 @@ static void key_range(int64_t kend, int64_t qlen, int64_t i, int causal, int win
     if (window > 0 && last - window + 1 > 0) *lo = last - window + 1;
 }
 
+/* Segment validity.  The attention needs every key any row of the segment
+ * reads to map to a valid block; the append only needs the slots it writes
+ * (positions kv_end - q_len .. kv_end - 1), so `written_only` narrows the
+ * block check to those. */
 static int check_segment(const oracle_pool *P, const int32_t *seg, int total_rows,
-                         int causal, int window)
+                         int causal, int window, int written_only)
 {
     int64_t q0 = seg[0], ql = seg[1], col = seg[2], kend = seg[3];
     if (q0 < 0 || ql < 0 || q0 + ql > total_rows) return OR_BAD_SEGMENT;
@@ -115,6 +120,7 @@ static int check_segment(const oracle_pool *P, const int32_t *seg, int total_row
     key_range(kend, ql, 0, causal, window, &lo0, &hi0);
     key_range(kend, ql, ql - 1, causal, window, &lo_last, &hi_last);
     int64_t lo = lo0 < lo_last ? lo0 : lo_last;
+    if (written_only) lo = kend - ql;
     for (int64_t j = lo; j < kend; ++j) {
         int64_t b; int o;
         int st = locate(P, (int)col, j, &b, &o);
@@ -140,7 +146,7 @@ int oracle_append(uint8_t *k_pool, uint8_t *v_pool, int elem_size,
     int errs = 0;
     for (int s = 0; s < num_segments; ++s) {
         const int32_t *seg = seq_info + 4 * s;
-        int st = check_segment(&P, seg, total_rows, causal, window);
+        int st = check_segment(&P, seg, total_rows, causal, window, 1);
         if (st) { errs |= 1 << st; continue; }
         for (int64_t i = 0; i < seg[1]; ++i) {
             int64_t t = seg[0] + i;
@@ -181,7 +187,7 @@ int oracle_attend(const double *q, int q_heads, int total_rows,
 
     for (int s = 0; s < num_segments; ++s) {
         const int32_t *seg = seq_info + 4 * s;
-        int st = check_segment(&P, seg, total_rows, causal, window);
+        int st = check_segment(&P, seg, total_rows, causal, window, 0);
         if (st) { errs |= 1 << st; continue; }
         int64_t q0 = seg[0], ql = seg[1], col = seg[2], kend = seg[3];
         for (int64_t i = 0; i < ql; ++i) {

@@ -435,3 +435,19 @@ def test_invalid_segments_write_nothing(seg, ring, window, bit):
     k0 = kp.copy()
     err2 = O.append(kp, vp, bt, si, q[:, :1].copy(), q[:, :1].copy(), ring_rows=ring, window=window)
     assert err2 == 1 << bit and np.array_equal(kp, k0)
+
+
+def test_append_gated_only_by_written_slots():
+    # A bad page before the written slot blocks the attention (it would be
+    # read) but not the append (it is never written).
+    q = np.ones((1, 2, 4))
+    kp = np.zeros((8, PAGE, 1, 4))
+    vp = np.zeros_like(kp)
+    bt = np.arange(8, dtype=np.int32)[None].copy()
+    bt[0, 2] = -5
+    si = np.array([[0, 1, 0, 100]], np.int32)
+    _, _, err = O.attend(q, kp, vp, bt, si, 0.3)
+    assert err == 1 << 4
+    kn = np.full((1, 1, 4), 3.0)
+    assert O.append(kp, vp, bt, si, kn, kn) == 0
+    assert np.array_equal(kp.reshape(-1, 1, 4)[99], kn[0])
