@@ -1,0 +1,407 @@
+"""Benchmark: paged decode attention, SenseNova-style decode step on one GB300.
+
+A step is one replay of the captured decode graph: 42 layers, each one fused
+append + attention launch (32 q / 8 kv heads, head_dim 128, bf16, one
+sequence behind an identity block table) at a given KV length.  The headline
+is KV length 8192 in the 8192 bucket; a sweep over other lengths (each in its
+own bucket's graph) is reported beside it.  L2 is flushed (256 MiB write)
+before every timed step, outside the timed events.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS, HQ, HKV, D = 42, 32, 8, 128
+HEADLINE_LEN = 8192
+SWEEP = (256, 512, 1024, 2048, 4096, 6144, 8192)
+METRIC = "paged decode attention µs/step and achieved HBM GB/s (% of peak) vs KV length"
+WORKLOAD = ("SenseNova-style decode: 42 layers, 32 q / 8 kv heads, head_dim 128, bf16, one sequence, "
+            "identity block table, KV length 8192 in the 8192 bucket, one captured graph per bucket")
+KERNEL_SOURCES = ("paged_kv_decode_13_gb300/csrc/attend.cuh", "paged_kv_decode_13_gb300/csrc/common.cuh",
+                  "paged_kv_decode_13_gb300/csrc/attend_inst.cu")
+PROFILE = os.path.join(ROOT, "profiles", "attend_sensenova_8192_traffic.json")
+
+
+def algorithmic_bytes_per_layer(L: int) -> int:
+    """Bytes one layer's append + attention must move at KV length L.
+
+    K and V of every live key (L * kv_heads * head_dim * 2 tensors * 2 B),
+    the query (Hq * D * 2 B), the appended K/V row written once
+    (2 * Hkv * D * 2 B), the fp32 output (Hq * D * 4 B), the block-table
+    entries of the live pages (4 B each) and the segment entry (16 B)."""
+    kv = L * HKV * D * 2 * 2
+    q = HQ * D * 2
+    app = 2 * HKV * D * 2
+    out = HQ * D * 4
+    table = 4 * ((L + 15) // 16)
+    return kv + q + app + out + table + 16
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def make_runner(pkv, L: int, seed: int, device):
+    import torch
+
+    import workloads
+    from paged_kv_decode_13_gb300.graph import DecodeGraphRunner, DecodeStep
+    bucket = pkv.bucket_for(L)
+    w = workloads.sensenova(L, bucket, num_layers=LAYERS, seed=seed, device=device)
+    cache = pkv.PagedKVCache(w.k, w.v, w.block_table, bucket=bucket)
+    step = DecodeStep(cache, HQ)
+    for layer in range(LAYERS):
+        step.q[layer].copy_(w.q[layer])
+        step.k_new[layer].copy_(w.k_new[layer])
+        step.v_new[layer].copy_(w.v_new[layer])
+    step.seq_info.copy_(w.seq_info)
+    runner = DecodeGraphRunner(step)
+    runner.graph_for()
+    torch.cuda.synchronize()
+    return runner, w
+
+
+def time_steps(runner, steps: int, warmup: int, flush, stream):
+    import torch
+    graph = runner.graph_for()
+    for _ in range(warmup):
+        flush()
+        graph.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def time_e2e(runner, steps: int, warmup: int, flush, stream):
+    """Per step: pinned host -> device copy of the step's inputs, graph replay,
+    device -> host copy of the outputs, all inside the timed events."""
+    import torch
+    st = runner.step_bufs
+    host_in = [t.cpu().pin_memory() for t in st.q + st.k_new + st.v_new + [st.seq_info]]
+    dev_in = st.q + st.k_new + st.v_new + [st.seq_info]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in st.out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    graph = runner.graph_for()
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        for h, o in zip(host_out, st.out):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(warmup):
+        flush()
+        one()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs], h2d, d2h
+
+
+def oracle_layer_seconds(q, k, v, L: int, kv_heads: int = HKV) -> float:
+    """Seconds the fp64 C oracle takes for the first `kv_heads` kv heads (and
+    their query heads) of one layer at KV length L; input widening excluded."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    g = HQ // HKV
+    nb = (L + 15) // 16
+    qd = np.ascontiguousarray(q[:, :kv_heads * g].double().numpy())
+    kd = np.ascontiguousarray(k[:nb, :, :kv_heads].double().numpy())
+    vd = np.ascontiguousarray(v[:nb, :, :kv_heads].double().numpy())
+    si = np.array([[0, 1, 0, L]], np.int32)
+    bt = np.arange(nb, dtype=np.int32)[None]
+    t0 = time.perf_counter()
+    orc.attend(qd, kd, vd, bt, si, 1 / math.sqrt(D))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_sample(layers, L: int, seconds: float = 12.0):
+    """Whole layers of the step through the oracle on this host (one thread),
+    cycling over the given layers until `seconds` of oracle time; returns the
+    time scaled to the full 42-layer step in µs, and the layers run."""
+    spent, done = 0.0, 0
+    while True:
+        q, k, v = layers[done % len(layers)]
+        spent += oracle_layer_seconds(q, k, v, L)
+        done += 1
+        if spent >= seconds or done >= 4 * LAYERS:
+            break
+    return spent / done * LAYERS * 1e6, done
+
+
+def gpu_arm(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_decode_13_gb300 as pkv
+
+    stream = torch.cuda.current_stream()
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def flush():
+        scratch.fill_(1)
+
+    peak, peak_kind = load_peaks()
+
+    # Headline: KV length 8192.
+    runner, w = make_runner(pkv, HEADLINE_LEN, seed=rank, device=device)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(device.index or 0)
+    times = time_steps(runner, args.steps, args.warmup, flush, stream)
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = statistics.mean(times)
+    ms = reduce_max(ms, world, device)
+    err = int(runner.step_bufs.err.item())
+    if err:
+        raise RuntimeError(f"device error flags {err:#x}")
+    launches_per_step = runner.step_bufs.launch_count()
+    bytes_layer = algorithmic_bytes_per_layer(HEADLINE_LEN)
+    per_launch_ms = ms / launches_per_step
+    achieved = bytes_layer / (per_launch_ms * 1e-3) / 1e9
+    step_gbs = bytes_layer * LAYERS / (ms * 1e-3) / 1e9
+
+    e2e_times, h2d, d2h = time_e2e(runner, max(args.steps // 4, 10), args.warmup, flush, stream)
+    e2e_ms = reduce_max(statistics.mean(e2e_times), world, device)
+
+    # CPU oracle baseline on a bounded sample of the same step's layers.
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        layers = [(w.q[i].cpu(), w.k[i].cpu(), w.v[i].cpu()) for i in range(min(LAYERS, 6))]
+        cpu_us, done = cpu_baseline_sample(layers, HEADLINE_LEN, seconds=args.cpu_seconds)
+        cpu = {"value": round(cpu_us, 1), "unit": "µs/step", "cores": 1, "kind": "oracle",
+               "sample": f"{done} whole layers (cycling over 6 of the step's 42) at KV length {HEADLINE_LEN} "
+                         f"through the fp64 C oracle on one thread, mean per layer scaled to 42 layers"}
+    del runner, w
+    torch.cuda.empty_cache()
+
+    by_len = {}
+    if not args.no_sweep:
+        for L in SWEEP:
+            r, _ = make_runner(pkv, L, seed=rank, device=device)
+            t = time_steps(r, max(args.steps // 4, 20), args.warmup, flush, stream)
+            m = reduce_max(statistics.median(t), world, device)
+            gbs = algorithmic_bytes_per_layer(L) * LAYERS / (m * 1e-3) / 1e9
+            by_len[str(L)] = {"bucket": pkv.bucket_for(L), "us_per_step": round(m * 1e3, 2),
+                              "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+            del r
+            torch.cuda.empty_cache()
+
+    traffic = None
+    if os.path.exists(PROFILE):
+        with open(PROFILE) as f:
+            prof = json.load(f)
+        if prof.get("kernel_hash") == kernel_hash():
+            traffic = prof.get("dram_bytes_per_launch")
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(ms * 1e3, 2),
+            "unit": "µs/step",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 5),
+            "higher_is_better": False,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded torch normal draws; q ~ N(0,1), K/V ~ N(0,1)/sqrt(128))",
+            "config": {"workload": WORKLOAD, "kv_len": HEADLINE_LEN, "bucket": pkv.bucket_for(HEADLINE_LEN),
+                       "layers": LAYERS, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
+                       "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+                       "parallelism": f"replicas x{world} (one sequence per GPU)"},
+            "hbm_gbs": round(step_gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_kind": f"{peak_kind} (STREAM-style copy)",
+                         "kernel": "attend_kernel (fused append + split-K attention), one launch per layer",
+                         "algorithmic_bytes_per_launch": bytes_layer,
+                         "launch_ms": round(per_launch_ms, 6)},
+            "by_kv_len": by_len,
+            "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "µs/step", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    import workloads
+    from oracle import oracle as orc
+    orc.build()
+    bucket = 8192
+    w = workloads.sensenova(HEADLINE_LEN, bucket, num_layers=2, seed=0, device="cpu")
+    # Size each step's sample so the whole run stays within about two minutes.
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    m = 8 if budget >= 0.3 else 4 if budget >= 0.15 else 2 if budget >= 0.06 else 1
+    for i in range(args.warmup):
+        oracle_layer_seconds(w.q[i % 2], w.k[i % 2], w.v[i % 2], HEADLINE_LEN, m)
+    per = []
+    for i in range(args.steps):
+        t = oracle_layer_seconds(w.q[i % 2], w.k[i % 2], w.v[i % 2], HEADLINE_LEN, m)
+        per.append(t * (HKV / m) * LAYERS * 1e6)
+    us = statistics.mean(per)
+    sample = (f"each step: {m} of the 8 kv heads (with their query heads) of one layer at KV length "
+              f"{HEADLINE_LEN} through the fp64 C oracle (one thread), scaled to 8 kv heads x 42 layers")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "µs/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "kv_len": HEADLINE_LEN, "bucket": bucket},
+        "cpu_baseline": {"value": round(us, 1), "unit": "µs/step", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": "µs/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+"""Python binding of libpkv: the C entry points under the same names.
+
+Only argument marshalling happens here (tensor pointers, the current CUDA
+stream, status checks).  Every step of the computation runs in the library's
+CUDA kernels; torch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import lib
+
+_DTYPES = {torch.bfloat16: _lib.BF16, torch.float32: _lib.F32}
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _contig(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class PagedKVCache:
+    """Per-layer paged K/V pools plus one block table, and their descriptor.
+
+    Pools are (num_blocks, 16, kv_heads, head_dim) tensors of bf16 or fp32
+    (the layout of vLLM-Omni's SenseNova-U1 PagedDecodeCache); the block
+    table is int32 (max_seqs, max_blocks_per_seq).  The tensors are owned by
+    this object; the descriptor only points at them.
+    """
+
+    def __init__(self, k: Sequence[torch.Tensor], v: Sequence[torch.Tensor], block_table: torch.Tensor,
+                 ring_rows: int = 0, bucket: Optional[int] = None, generation: int = 0):
+        if len(k) != len(v) or not k:
+            raise ValueError("k and v need one tensor per layer")
+        shape, dtype = k[0].shape, k[0].dtype
+        if dtype not in _DTYPES:
+            raise ValueError(f"unsupported dtype {dtype}")
+        for t in list(k) + list(v):
+            if t.shape != shape or t.dtype != dtype or not t.is_contiguous():
+                raise ValueError("every pool must be contiguous with the same shape and dtype")
+        if len(shape) != 4 or shape[1] != _lib.BLOCK_SIZE:
+            raise ValueError("pools are (num_blocks, 16, kv_heads, head_dim)")
+        if block_table.dtype != torch.int32 or block_table.dim() != 2:
+            raise ValueError("block_table is int32 (max_seqs, max_blocks_per_seq)")
+        self.k: List[torch.Tensor] = list(k)
+        self.v: List[torch.Tensor] = list(v)
+        self.block_table = _contig(block_table, "block_table")
+        self.ring_rows = int(ring_rows)
+        self.generation = int(generation)
+        nb = shape[0]
+        self.bucket = int(bucket) if bucket is not None else int(block_table.shape[1]) * _lib.BLOCK_SIZE
+        self._kp = (ctypes.c_void_p * len(k))(*[t.data_ptr() for t in self.k])
+        self._vp = (ctypes.c_void_p * len(v))(*[t.data_ptr() for t in self.v])
+        self.desc = _lib.CacheDesc(
+            num_layers=len(k), kv_heads=shape[2], head_dim=shape[3], dtype=_DTYPES[dtype], num_blocks=nb,
+            max_seqs=block_table.shape[0], max_blocks_per_seq=block_table.shape[1], ring_rows=self.ring_rows,
+            reserved0=0, k=ctypes.cast(self._kp, ctypes.c_void_p), v=ctypes.cast(self._vp, ctypes.c_void_p),
+            block_table=block_table.data_ptr(), bucket=self.bucket, generation=self.generation)
+
+    @classmethod
+    def allocate(cls, num_layers: int, kv_heads: int, head_dim: int, bucket: int, dtype=torch.bfloat16,
+                 device="cuda", generation: int = 0) -> "PagedKVCache":
+        """Zeroed single-sequence cache behind an identity table (one bucket)."""
+        nb = (bucket + _lib.BLOCK_SIZE - 1) // _lib.BLOCK_SIZE
+        shape = (nb, _lib.BLOCK_SIZE, kv_heads, head_dim)
+        k = [torch.zeros(shape, dtype=dtype, device=device) for _ in range(num_layers)]
+        v = [torch.zeros(shape, dtype=dtype, device=device) for _ in range(num_layers)]
+        bt = torch.arange(nb, dtype=torch.int32, device=device).unsqueeze(0)
+        return cls(k, v, bt, bucket=bucket, generation=generation)
+
+    @property
+    def num_layers(self) -> int:
+        return len(self.k)
+
+    @property
+    def kv_heads(self) -> int:
+        return int(self.k[0].shape[2])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.k[0].shape[3])
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.k[0].dtype
+
+    def ref(self):
+        return ctypes.byref(self.desc)
+
+    def reusable_for(self, num_layers, kv_heads, head_dim, dtype, length) -> bool:
+        """Same shape and the length fits the current bucket (PagedDecodeCache.reusable_for)."""
+        return (self.num_layers == num_layers and self.kv_heads == kv_heads and self.head_dim == head_dim
+                and self.dtype == dtype and bucket_for(length) <= self.bucket)
+
+
+def bucket_for(length: int) -> int:
+    return int(lib.pkv_bucket_for(int(length)))
+
+
+def new_err_flags(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def append(cache: PagedKVCache, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, seq_info: torch.Tensor,
+           err: torch.Tensor, window: int = 0, stream=None) -> None:
+    rows = int(k_new.shape[0])
+    _lib.check("pkv_append", lib.pkv_append(
+        cache.ref(), layer, _ptr(_contig(k_new, "k_new")), _ptr(_contig(v_new, "v_new")), rows,
+        _ptr(_contig(seq_info, "seq_info")), int(seq_info.shape[0]), int(window), _ptr(err), _stream(stream)))
+
+
+def attend_workspace_bytes(cache: PagedKVCache, num_q_heads: int, num_segments: int, max_q_len: int,
+                           max_kv: int, num_splits: int = 0) -> int:
+    return int(lib.pkv_attend_workspace_bytes(cache.ref(), num_q_heads, num_segments, max_q_len, int(max_kv),
+                                              num_splits))
+
+
+def workspace_init(ws: torch.Tensor, stream=None) -> None:
+    nbytes = ws.numel() * ws.element_size()
+    _lib.check("pkv_workspace_init", lib.pkv_workspace_init(_ptr(ws), nbytes, _stream(stream)))
+
+
+def new_workspace(cache: PagedKVCache, num_q_heads: int, num_segments: int, max_q_len: int, max_kv: int,
+                  num_splits: int = 0, device="cuda") -> torch.Tensor:
+    n = max(attend_workspace_bytes(cache, num_q_heads, num_segments, max_q_len, max_kv, num_splits), 16)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _attend(fn_name, cache, layer, q, k_new, v_new, seq_info, out, lse, workspace, err, max_q_len, max_kv,
+            scale, causal, window, num_splits, flags, stream):
+    rows, hq = int(q.shape[0]), int(q.shape[1])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = [cache.ref(), layer, _ptr(_contig(q, "q"))]
+    if fn_name == "pkv_append_attend":
+        args += [_ptr(_contig(k_new, "k_new")), _ptr(_contig(v_new, "v_new"))]
+    args += [hq, rows, _ptr(_contig(seq_info, "seq_info")), int(seq_info.shape[0]), int(max_q_len), int(max_kv),
+             int(num_splits), float(scale), int(bool(causal)), int(window), _ptr(_contig(out, "out")),
+             _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err), int(flags), _stream(stream)]
+    _lib.check(fn_name, getattr(lib, fn_name)(*args))
+
+
+def attend_varlen(cache: PagedKVCache, layer: int, q: torch.Tensor, seq_info: torch.Tensor, out: torch.Tensor,
+                  err: torch.Tensor, workspace: Optional[torch.Tensor], max_q_len: int, max_kv: int,
+                  scale: float, causal: bool = False, window: int = 0, lse: Optional[torch.Tensor] = None,
+                  num_splits: int = 0, flags: int = 0, stream=None) -> None:
+    _attend("pkv_attend_varlen", cache, layer, q, None, None, seq_info, out, lse, workspace, err, max_q_len,
+            max_kv, scale, causal, window, num_splits, flags, stream)
+
+
+def append_attend(cache: PagedKVCache, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                  seq_info: torch.Tensor, out: torch.Tensor, err: torch.Tensor, workspace: Optional[torch.Tensor],
+                  max_q_len: int, max_kv: int, scale: float, causal: bool = False, window: int = 0,
+                  lse: Optional[torch.Tensor] = None, num_splits: int = 0, flags: int = 0, stream=None) -> None:
+    _attend("pkv_append_attend", cache, layer, q, k_new, v_new, seq_info, out, lse, workspace, err, max_q_len,
+            max_kv, scale, causal, window, num_splits, flags, stream)
+
+
+def seqinfo_from_seqused(cu_seqlens_q: torch.Tensor, seqused_k: torch.Tensor, out: torch.Tensor,
+                         stream=None) -> None:
+    n = int(seqused_k.shape[0])
+    _lib.check("pkv_seqinfo_from_seqused", lib.pkv_seqinfo_from_seqused(
+        _ptr(cu_seqlens_q), _ptr(seqused_k), n, _ptr(out), _stream(stream)))
+
+
+def advance(seq_info: torch.Tensor, stream=None) -> None:
+    _lib.check("pkv_advance", lib.pkv_advance(_ptr(seq_info), int(seq_info.shape[0]), _stream(stream)))
+
+
+def resize_bucket(old: PagedKVCache, new: PagedKVCache, old_len: int, stream=None) -> int:
+    """Copy the first old_len tokens of every layer; bumps new.generation on success."""
+    st = _lib.check("pkv_resize_bucket", lib.pkv_resize_bucket(old.ref(), new.ref(), int(old_len),
+                                                                 _stream(stream)), (_lib.OK, _lib.SAME_BUCKET))
+    new.generation = int(new.desc.generation)
+    return st
+
+
+def load_prefix(cache: PagedKVCache, keys: Sequence[torch.Tensor], values: Sequence[torch.Tensor],
+                stream=None) -> bool:
+    """keys/values: per layer [S, H, D] views (any strides with D contiguous).  False if empty."""
+    if not keys or keys[0] is None or keys[0].shape[0] == 0:
+        return False
+    n = int(keys[0].shape[0])
+    ss, sh, sd = keys[0].stride()
+    if sd != 1:
+        raise ValueError("head_dim must be contiguous")
+    for t in list(keys) + list(values):
+        if t.stride() != (ss, sh, 1) or t.shape != keys[0].shape or t.dtype != cache.dtype:
+            raise ValueError("all prefix tensors need the same shape, strides and dtype")
+    kp = (ctypes.c_void_p * len(keys))(*[t.data_ptr() for t in keys])
+    vp = (ctypes.c_void_p * len(values))(*[t.data_ptr() for t in values])
+    st = lib.pkv_load_prefix(cache.ref(), ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p), n,
+                             ss, sh, _stream(stream))
+    return _lib.check("pkv_load_prefix", st, (_lib.OK, _lib.EMPTY)) == _lib.OK
+
+
+def to_contiguous(cache: PagedKVCache, layer: int, n: int, keys_out: torch.Tensor, values_out: torch.Tensor,
+                  stream=None) -> None:
+    """keys_out / values_out: contiguous [kv_heads, n, head_dim]."""
+    _lib.check("pkv_to_contiguous", lib.pkv_to_contiguous(cache.ref(), layer, int(n), _ptr(keys_out),
+                                                          _ptr(values_out), _stream(stream)))

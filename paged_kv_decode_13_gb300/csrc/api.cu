@@ -1,0 +1,408 @@
+// C-ABI entry points of libpkv: argument checks, launch planning and launches.
+// Every entry point validates on the host first and returns a negative
+// pkv_status before launching anything; nothing here allocates memory,
+// synchronises the host or keeps state beyond per-process kernel attributes.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "launch.h"
+#include "misc_kernels.cuh"
+
+using namespace pkv;
+
+namespace {
+
+constexpr int kDefaultSms = 152;       // GB300, used when no device is visible
+constexpr int kSmemPerSm = 233472;     // shared memory per SM available to CTAs
+constexpr int kMinBlocksPerSplit = 2;  // pages per split-K piece, at least
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : dtype == PKV_F32 ? 4 : 0; }
+
+int check_cache(const pkv_cache *c) {
+    if (!c) return PKV_EINVAL;
+    if (c->dtype != PKV_BF16 && c->dtype != PKV_F32) return PKV_EUNSUPPORTED;
+    // vLLM-Omni paged_decode_supported: head_dim a multiple of 8, at most 256.
+    if (c->head_dim <= 0 || c->head_dim % 8 != 0 || c->head_dim > 256) return PKV_EUNSUPPORTED;
+    if (c->num_layers <= 0 || c->kv_heads <= 0 || c->num_blocks <= 0) return PKV_EINVAL;
+    if (c->max_seqs <= 0 || c->max_blocks_per_seq <= 0) return PKV_EINVAL;
+    if (!c->k || !c->v || !c->block_table) return PKV_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(c->block_table) & 3u) != 0) return PKV_EINVAL;
+    if (c->ring_rows < 0 || c->ring_rows % PKV_BLOCK_SIZE != 0) return PKV_EINVAL;
+    if ((long long)c->ring_rows > (long long)c->max_blocks_per_seq * PKV_BLOCK_SIZE) return PKV_EINVAL;
+    return PKV_OK;
+}
+
+int check_layer(const pkv_cache *c, int layer) {
+    if (layer < 0 || layer >= c->num_layers) return PKV_EINVAL;
+    if (!c->k[layer] || !c->v[layer] || !aligned16(c->k[layer]) || !aligned16(c->v[layer])) return PKV_EINVAL;
+    return PKV_OK;
+}
+
+int sm_count() {
+    static std::atomic<int> cached{0};
+    int v = cached.load();
+    if (v > 0) return v;
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = kDefaultSms;
+    }
+    cached.store(n);
+    return n;
+}
+
+// Launch plan of one attention call; identical for the workspace query and
+// the launch so both agree on the workspace layout.
+struct Plan {
+    AttnKernel k;
+    int G, rows_max, row_tiles, units, nsplits;
+    size_t off_lse, off_o, bytes;
+};
+
+AttnKernel pick(int variant, int dp, int rc) {
+    switch (variant * 1000 + dp) {
+        case 64: return pick_0_64(rc);
+        case 128: return pick_0_128(rc);
+        case 256: return pick_0_256(rc);
+        case 1064: return pick_1_64(rc);
+        case 1128: return pick_1_128(rc);
+        case 1256: return pick_1_256(rc);
+        case 2064: return pick_2_64(rc);
+        case 2128: return pick_2_128(rc);
+        case 2256: return pick_2_256(rc);
+    }
+    return AttnKernel{nullptr, 0, 0, 0, 0, false};
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv, int num_splits,
+              unsigned flags, Plan *pl) {
+    int st = check_cache(c);
+    if (st) return st;
+    if (Hq <= 0 || Hq % c->kv_heads != 0) return PKV_EINVAL;
+    if (S < 0 || max_q_len <= 0 || max_kv <= 0 || num_splits < 0) return PKV_EINVAL;
+    const int D = c->head_dim;
+    const int dp = D <= 64 ? 64 : D <= 128 ? 128 : 256;
+    const int variant = c->dtype == PKV_F32 ? kSimtF32 : (flags & PKV_FLAG_SIMT) ? kSimtBf16 : kMmaBf16;
+    pl->G = Hq / c->kv_heads;
+    const long long rows_max = (long long)pl->G * max_q_len;
+    if (rows_max > (1 << 20)) return PKV_EINVAL;
+    pl->rows_max = (int)rows_max;
+    const int rc = rows_max <= 16 ? 0 : rows_max <= 32 ? 1 : rows_max <= 64 ? 2 : 3;
+    pl->k = pick(variant, dp, rc);
+    if (!pl->k.fn) return PKV_EUNSUPPORTED;
+    pl->row_tiles = (int)((rows_max + pl->k.rows - 1) / pl->k.rows);
+    const long long units = (long long)S * c->kv_heads * pl->row_tiles;
+    if ((long long)c->kv_heads * pl->row_tiles > 65535 || S + 1 > 65535) return PKV_EINVAL;
+    pl->units = (int)units;
+    const long long max_pages = (max_kv + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE + 1;
+    const long long split_cap = (max_pages + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
+    long long ns = num_splits;
+    if (ns == 0) {
+        long long occ = std::min<long long>(2048 / pl->k.threads, kSmemPerSm / (long long)(pl->k.smem + 1024));
+        occ = std::max<long long>(occ, 1);
+        const long long target = (long long)sm_count() * occ;
+        ns = units > 0 ? (target + units - 1) / units : 1;
+        ns = std::max<long long>(1, std::min(ns, split_cap));
+    }
+    if (ns > 65535) return PKV_EINVAL;
+    pl->nsplits = (int)ns;
+    if (pl->nsplits == 1 || units == 0) {
+        pl->off_lse = pl->off_o = pl->bytes = 0;
+    } else {
+        const size_t tick = round256((size_t)units * 4);
+        const size_t lse = round256((size_t)units * ns * pl->k.rows * 4);
+        const size_t o = (size_t)units * ns * pl->k.rows * pl->k.dp * 4;
+        pl->off_lse = tick;
+        pl->off_o = tick + lse;
+        pl->bytes = tick + lse + o;
+    }
+    return PKV_OK;
+}
+
+// Opt a kernel into its dynamic shared memory size once per process.
+int prepare_kernel(const AttnKernel &k) {
+    static std::mutex mu;
+    static const void *done[64];
+    static int ndone = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ndone; ++i)
+        if (done[i] == k.fn) return PKV_OK;
+    if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ECUDA;
+    }
+    if (ndone < 64) done[ndone++] = k.fn;
+    return PKV_OK;
+}
+
+int launch_status(cudaError_t e) {
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
+int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_new, const void *v_new,
+                  int Hq, int total_rows, const int *seq_info, int S, int max_q_len, long long max_kv,
+                  int num_splits, float scale, int causal, int window, float *out, float *lse,
+                  void *ws, size_t ws_bytes, unsigned *err, unsigned flags, void *stream) {
+    Plan pl;
+    int st = make_plan(c, Hq, S, max_q_len, max_kv, num_splits, flags, &pl);
+    if (st) return st;
+    if ((st = check_layer(c, layer))) return st;
+    if (total_rows < 0 || window < 0 || (causal != 0 && causal != 1)) return PKV_EINVAL;
+    if (!err || !out || (total_rows > 0 && (!q || !aligned16(q)))) return PKV_EINVAL;
+    if (S > 0 && (!seq_info || !aligned16(seq_info))) return PKV_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return PKV_EINVAL;
+    if (k_new && (!v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
+    if (pl.bytes > 0 && (!ws || ws_bytes < pl.bytes || !aligned16(ws))) return PKV_EWORKSPACE;
+    if (S == 0 && total_rows == 0) return PKV_OK;
+    if ((st = prepare_kernel(pl.k))) return st;
+
+    AttendParams p;
+    p.q = q;
+    p.k_pool = c->k[layer];
+    p.v_pool = c->v[layer];
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_pool_w = c->k[layer];
+    p.v_pool_w = c->v[layer];
+    p.block_table = c->block_table;
+    p.seq_info = reinterpret_cast<const int4 *>(seq_info);
+    p.out = out;
+    p.lse = lse;
+    char *w = reinterpret_cast<char *>(ws);
+    p.ws_ticket = pl.bytes ? reinterpret_cast<unsigned *>(w) : nullptr;
+    p.ws_lse = pl.bytes ? reinterpret_cast<float *>(w + pl.off_lse) : nullptr;
+    p.ws_o = pl.bytes ? reinterpret_cast<float *>(w + pl.off_o) : nullptr;
+    p.err = err;
+    p.num_blocks = c->num_blocks;
+    p.Hq = Hq;
+    p.Hkv = c->kv_heads;
+    p.D = c->head_dim;
+    p.G = pl.G;
+    p.total_rows = total_rows;
+    p.S = S;
+    p.max_seqs = c->max_seqs;
+    p.mbps = c->max_blocks_per_seq;
+    p.ring_rows = c->ring_rows;
+    p.max_q_len = max_q_len;
+    p.rows_max = pl.rows_max;
+    p.row_tiles = pl.row_tiles;
+    p.nsplits = pl.nsplits;
+    p.min_blocks = kMinBlocksPerSplit;
+    p.causal = causal;
+    p.window = window;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.nsplits, (unsigned)(c->kv_heads * pl.row_tiles), (unsigned)(S + 1));
+    cfg.blockDim = dim3((unsigned)pl.k.threads);
+    cfg.dynamicSmemBytes = pl.k.smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (flags & PKV_FLAG_PDL) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void *args[] = {&p};
+    return launch_status(cudaLaunchKernelExC(&cfg, pl.k.fn, args));
+}
+
+int copy_rows(const void *s0, const void *s1, void *d0, void *d1, long long n, int H, int row_bytes,
+              long long ss, long long sh, long long ds, long long dh, void *stream) {
+    if (n <= 0) return PKV_OK;
+    CopyParams p{reinterpret_cast<const char *>(s0), reinterpret_cast<const char *>(s1),
+                 reinterpret_cast<char *>(d0), reinterpret_cast<char *>(d1), n, H, row_bytes / 16,
+                 ss, sh, ds, dh};
+    const long long total = 2 * n * H * (row_bytes / 16);
+    const long long blocks = std::min<long long>((total + 255) / 256, (long long)sm_count() * 8);
+    strided_copy_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    return launch_status(cudaSuccess);
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t pkv_bucket_for(int64_t length) {
+    // vLLM-Omni paged_decode.py: BUCKETS then TAIL_STEP-sized growth.
+    static const int64_t buckets[] = {512, 1024, 2048, 4096, 8192};
+    for (int64_t b : buckets)
+        if (length <= b) return b;
+    const int64_t tail = 2048;
+    return 8192 + ((length - 8192 + tail - 1) / tail) * tail;
+}
+
+const char *pkv_status_str(int s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_EMPTY: return "empty: nothing to copy";
+        case PKV_SAME_BUCKET: return "same bucket: no resize needed";
+        case PKV_EINVAL: return "invalid argument";
+        case PKV_EUNSUPPORTED: return "unsupported dtype or head_dim";
+        case PKV_ECUDA: return "CUDA launch or copy failed";
+        case PKV_ECAPACITY: return "capacity exceeded";
+        case PKV_ESTALE: return "caches describe different shapes";
+        case PKV_EWORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+int pkv_append(const pkv_cache *c, int32_t layer, const void *k_new, const void *v_new, int32_t total_rows,
+               const int32_t *seq_info, int32_t S, int32_t window, uint32_t *err, void *stream) {
+    int st = check_cache(c);
+    if (st) return st;
+    if ((st = check_layer(c, layer))) return st;
+    if (S < 0 || total_rows < 0 || window < 0 || !err) return PKV_EINVAL;
+    if (S == 0) return PKV_OK;
+    if (!seq_info || !aligned16(seq_info)) return PKV_EINVAL;
+    if (total_rows > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
+    AppendParams p;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_pool = c->k[layer];
+    p.v_pool = c->v[layer];
+    p.block_table = c->block_table;
+    p.seq_info = reinterpret_cast<const int4 *>(seq_info);
+    p.err = err;
+    p.num_blocks = c->num_blocks;
+    p.row_bytes = c->kv_heads * c->head_dim * elem_bytes(c->dtype);
+    p.total_rows = total_rows;
+    p.S = S;
+    p.max_seqs = c->max_seqs;
+    p.mbps = c->max_blocks_per_seq;
+    p.ring_rows = c->ring_rows;
+    p.window = window;
+    append_kernel<<<(unsigned)S, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    return launch_status(cudaSuccess);
+}
+
+size_t pkv_attend_workspace_bytes(const pkv_cache *c, int32_t Hq, int32_t S, int32_t max_q_len, int64_t max_kv,
+                                  int32_t num_splits) {
+    Plan pl;
+    if (make_plan(c, Hq, S, max_q_len, max_kv, num_splits, 0, &pl)) return 0;
+    // The CUDA-core bf16 kernel may use a different tile; report the larger.
+    Plan p2;
+    if (c->dtype == PKV_BF16 && !make_plan(c, Hq, S, max_q_len, max_kv, num_splits, PKV_FLAG_SIMT, &p2))
+        return std::max(pl.bytes, p2.bytes);
+    return pl.bytes;
+}
+
+int pkv_workspace_init(void *ws, size_t bytes, void *stream) {
+    if (bytes == 0) return PKV_OK;
+    if (!ws) return PKV_EINVAL;
+    return launch_status(cudaMemsetAsync(ws, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pkv_attend_varlen(const pkv_cache *c, int32_t layer, const void *q, int32_t Hq, int32_t total_rows,
+                      const int32_t *seq_info, int32_t S, int32_t max_q_len, int64_t max_kv, int32_t num_splits,
+                      float scale, int32_t causal, int32_t window, float *out, float *lse, void *ws,
+                      size_t ws_bytes, uint32_t *err, uint32_t flags, void *stream) {
+    return attend_common(c, layer, q, nullptr, nullptr, Hq, total_rows, seq_info, S, max_q_len, max_kv,
+                         num_splits, scale, causal, window, out, lse, ws, ws_bytes, err, flags, stream);
+}
+
+int pkv_append_attend(const pkv_cache *c, int32_t layer, const void *q, const void *k_new, const void *v_new,
+                      int32_t Hq, int32_t total_rows, const int32_t *seq_info, int32_t S, int32_t max_q_len,
+                      int64_t max_kv, int32_t num_splits, float scale, int32_t causal, int32_t window,
+                      float *out, float *lse, void *ws, size_t ws_bytes, uint32_t *err, uint32_t flags,
+                      void *stream) {
+    if (total_rows > 0 && (!k_new || !v_new)) return PKV_EINVAL;
+    return attend_common(c, layer, q, total_rows > 0 ? k_new : nullptr, total_rows > 0 ? v_new : nullptr, Hq,
+                         total_rows, seq_info, S, max_q_len, max_kv, num_splits, scale, causal, window, out, lse,
+                         ws, ws_bytes, err, flags, stream);
+}
+
+int pkv_seqinfo_from_seqused(const int32_t *cu, const int32_t *used, int32_t n, int32_t *out, void *stream) {
+    if (n < 0) return PKV_EINVAL;
+    if (n == 0) return PKV_OK;
+    if (!cu || !used || !out || !aligned16(out)) return PKV_EINVAL;
+    seqinfo_from_seqused_kernel<<<(unsigned)((n + 127) / 128), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        cu, used, n, reinterpret_cast<int4 *>(out));
+    return launch_status(cudaSuccess);
+}
+
+int pkv_advance(int32_t *seq_info, int32_t n, void *stream) {
+    if (n < 0) return PKV_EINVAL;
+    if (n == 0) return PKV_OK;
+    if (!seq_info || !aligned16(seq_info)) return PKV_EINVAL;
+    advance_kernel<<<(unsigned)((n + 127) / 128), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<int4 *>(seq_info), n);
+    return launch_status(cudaSuccess);
+}
+
+int pkv_resize_bucket(const pkv_cache *o, pkv_cache *n, int64_t old_len, void *stream) {
+    int st = check_cache(o);
+    if (st) return st;
+    if ((st = check_cache(n))) return st;
+    if (o->num_layers != n->num_layers || o->kv_heads != n->kv_heads || o->head_dim != n->head_dim ||
+        o->dtype != n->dtype)
+        return PKV_ESTALE;
+    if (o->ring_rows || n->ring_rows) return PKV_EINVAL;
+    if (old_len < 0) return PKV_EINVAL;
+    if (n->bucket == o->bucket) return PKV_SAME_BUCKET;
+    if (old_len > o->num_blocks * PKV_BLOCK_SIZE || old_len > n->num_blocks * PKV_BLOCK_SIZE) return PKV_ECAPACITY;
+    const int row = o->head_dim * elem_bytes(o->dtype);
+    const long long tok = (long long)o->kv_heads * row;
+    for (int l = 0; l < o->num_layers; ++l) {
+        if (check_layer(o, l) || check_layer(n, l)) return PKV_EINVAL;
+    }
+    for (int l = 0; l < o->num_layers; ++l) {
+        st = copy_rows(o->k[l], o->v[l], n->k[l], n->v[l], old_len, o->kv_heads, row, tok, row, tok, row, stream);
+        if (st) return st;
+    }
+    n->generation = o->generation + 1;
+    return PKV_OK;
+}
+
+int pkv_load_prefix(const pkv_cache *c, const void *const *keys, const void *const *values, int64_t n,
+                    int64_t stride_s, int64_t stride_h, void *stream) {
+    int st = check_cache(c);
+    if (st) return st;
+    if (n == 0 || !keys) return PKV_EMPTY;
+    if (n < 0 || !values) return PKV_EINVAL;
+    if (n > c->num_blocks * PKV_BLOCK_SIZE) return PKV_ECAPACITY;
+    const int eb = elem_bytes(c->dtype);
+    const int row = c->head_dim * eb;
+    if (stride_s < 0 || stride_h < 0 || (stride_s * eb) % 16 || (stride_h * eb) % 16) return PKV_EINVAL;
+    for (int l = 0; l < c->num_layers; ++l) {
+        if (check_layer(c, l) || !keys[l] || !values[l] || !aligned16(keys[l]) || !aligned16(values[l]))
+            return PKV_EINVAL;
+    }
+    const long long tok = (long long)c->kv_heads * row;
+    for (int l = 0; l < c->num_layers; ++l) {
+        st = copy_rows(keys[l], values[l], c->k[l], c->v[l], n, c->kv_heads, row, stride_s * eb, stride_h * eb,
+                       tok, row, stream);
+        if (st) return st;
+    }
+    return PKV_OK;
+}
+
+int pkv_to_contiguous(const pkv_cache *c, int32_t layer, int64_t n, void *keys_out, void *values_out,
+                      void *stream) {
+    int st = check_cache(c);
+    if (st) return st;
+    if ((st = check_layer(c, layer))) return st;
+    if (n < 0 || n > c->num_blocks * PKV_BLOCK_SIZE) return PKV_ECAPACITY;
+    if (n == 0) return PKV_OK;
+    if (!keys_out || !values_out || !aligned16(keys_out) || !aligned16(values_out)) return PKV_EINVAL;
+    const int row = c->head_dim * elem_bytes(c->dtype);
+    const long long tok = (long long)c->kv_heads * row;
+    return copy_rows(c->k[layer], c->v[layer], keys_out, values_out, n, c->kv_heads, row, tok, row, row,
+                     n * row, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,703 @@
+// Split-K decode attention over a paged KV cache.
+//
+// One CTA per (split, kv head x row tile, segment).  The CTA holds the query
+// rows of one kv head's GQA group (G heads x q_len rows, zero-padded to 16-row
+// tiles) and streams the K/V pages of its share of the segment's key range
+// through a cp.async ring in shared memory, 16 tokens (one page of one kv
+// head) per stage.  Warps are arranged as MT row tiles x KW key groups: the
+// KW groups take alternate pages and keep separate online-softmax states that
+// are merged in shared memory at the end.  Splits of one (segment, kv head)
+// write normalised partials and their log2-sum-exp; the last split to finish
+// (a ticket counter, no waiting) merges them.
+//
+// Semantics follow the segment-table attention of ExecuTorch PR #24072
+// (triton::sdpa_varlen) over the (num_blocks, 16, kv_heads, head_dim) paged
+// layout of vLLM-Omni's SenseNova-U1 PagedDecodeCache: causal rows are aligned
+// to kv_end (tiny-llm kv_cache.py, causal_kwargs), the window ends at the
+// row's own position, ring storage maps position p to slot p % ring_rows
+// (ExecuTorch #24074), rows no segment covers read zero.
+#pragma once
+
+#include <math_constants.h>
+
+#include "common.cuh"
+
+namespace pkv {
+
+template <typename T_, int DP_, int MT_, int KW_, int NST_, bool MMA_>
+struct AttnCfg {
+    using T = T_;
+    static constexpr int DP = DP_;      // head_dim rounded up to 64 / 128 / 256
+    static constexpr int MT = MT_;      // 16-row tiles per CTA
+    static constexpr int KW = KW_;      // key groups (pages interleaved across them)
+    static constexpr int NST = NST_;    // pipeline stages per key group
+    static constexpr bool MMA = MMA_;
+    static constexpr int kWarps = MT * KW;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kRows = MT * 16;
+    static constexpr int kElem = (int)sizeof(T);
+    static constexpr int kEpc = 16 / kElem;             // elements per 16-byte chunk
+    static constexpr int kLd = DP + kEpc;               // padded smem row (elements)
+    static constexpr int kChunks = DP / kEpc;           // 16-byte chunks per row
+    static constexpr int kTile = kPage * kLd;           // one K or V page, elements
+    static constexpr int kStage = 2 * kTile;
+    static constexpr int kQLdF = DP + 4;                // fp32 query row (CUDA-core path)
+    static constexpr size_t kQBytes =
+        MMA ? (size_t)kRows * kLd * kElem : (size_t)kRows * kQLdF * 4;
+    static constexpr size_t kPipeBytes = (size_t)KW * NST * kStage * kElem;
+    static constexpr size_t kMergeBytes = (size_t)KW * kRows * (DP + 2) * 4;
+    static constexpr size_t kBodyBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+    static constexpr size_t kBoundsBytes = (size_t)kRows * 2 * 4;
+    static constexpr size_t kSimtBytes = MMA ? 0 : (size_t)kWarps * (16 * 16 + 16) * 4;
+    static constexpr size_t kSmemBytes = kQBytes + kBodyBytes + kBoundsBytes + kSimtBytes;
+    static_assert(kQBytes % 16 == 0 && kBodyBytes % 16 == 0, "smem sections stay 16-byte aligned");
+    static_assert(!MMA || sizeof(T) == 2, "tensor-core path is bf16");
+};
+
+// ---------------------------------------------------------------- small vector loads
+
+template <typename T, int N>
+__device__ __forceinline__ void load_f32(float (&o)[N], const T *src);
+
+template <>
+__device__ __forceinline__ void load_f32<float, 2>(float (&o)[2], const float *s) {
+    float2 v = *reinterpret_cast<const float2 *>(s);
+    o[0] = v.x; o[1] = v.y;
+}
+template <>
+__device__ __forceinline__ void load_f32<float, 4>(float (&o)[4], const float *s) {
+    float4 v = *reinterpret_cast<const float4 *>(s);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load_f32<float, 8>(float (&o)[8], const float *s) {
+    float4 a = reinterpret_cast<const float4 *>(s)[0], b = reinterpret_cast<const float4 *>(s)[1];
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void bf2_to_f32(float *o, unsigned u) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    float2 f = __bfloat1622float2(v);
+    o[0] = f.x; o[1] = f.y;
+}
+template <>
+__device__ __forceinline__ void load_f32<__nv_bfloat16, 2>(float (&o)[2], const __nv_bfloat16 *s) {
+    bf2_to_f32(o, *reinterpret_cast<const unsigned *>(s));
+}
+template <>
+__device__ __forceinline__ void load_f32<__nv_bfloat16, 4>(float (&o)[4], const __nv_bfloat16 *s) {
+    uint2 v = *reinterpret_cast<const uint2 *>(s);
+    bf2_to_f32(o, v.x); bf2_to_f32(o + 2, v.y);
+}
+template <>
+__device__ __forceinline__ void load_f32<__nv_bfloat16, 8>(float (&o)[8], const __nv_bfloat16 *s) {
+    uint4 v = *reinterpret_cast<const uint4 *>(s);
+    bf2_to_f32(o, v.x); bf2_to_f32(o + 2, v.y); bf2_to_f32(o + 4, v.z); bf2_to_f32(o + 6, v.w);
+}
+
+// ---------------------------------------------------------------- per-warp compute states
+
+// Tensor-core state of one warp: a 16-row tile, fp32 accumulators in the
+// mma.m16n8k16 C layout (thread holds rows lane/4 and lane/4 + 8).
+template <class C>
+struct MmaWarp {
+    static constexpr int DP = C::DP, LD = C::kLd;
+    float m[2], l[2];
+    float acc[DP / 8][4];
+    unsigned qf[DP <= 128 ? DP / 16 : 1][4];
+
+    __device__ void init(const __nv_bfloat16 *sQ, int mt, int lane) {
+        m[0] = m[1] = -CUDART_INF_F;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int n = 0; n < DP / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        if constexpr (DP <= 128) {
+#pragma unroll
+            for (int kk = 0; kk < DP / 16; ++kk)
+                ldmatrix_x4(qf[kk], sQ + (mt * 16 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
+        }
+    }
+
+    __device__ void consume(const __nv_bfloat16 *sQ, const __nv_bfloat16 *sK, const __nv_bfloat16 *sV,
+                            long long pos0, const int *sLo, const int *sHi, int mt, int lane,
+                            float scale_log2) {
+        // S = Q K^T over the page's 16 keys.
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int krow = (lane & 7) + ((lane >> 4) << 3);
+        const int kcol = ((lane >> 3) & 1) << 3;
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk) {
+            unsigned a[4];
+            if constexpr (DP <= 128) {
+                a[0] = qf[kk][0]; a[1] = qf[kk][1]; a[2] = qf[kk][2]; a[3] = qf[kk][3];
+            } else {
+                ldmatrix_x4(a, sQ + (mt * 16 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
+            }
+            unsigned b[4];
+            ldmatrix_x4(b, sK + krow * LD + kk * 16 + kcol);
+            mma_bf16_16816(sc[0], a, b[0], b[1]);
+            mma_bf16_16816(sc[1], a, b[2], b[3]);
+        }
+        // Mask, online softmax (base 2).
+        const int t4 = lane & 3;
+        float mx[2], alpha[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = mt * 16 + (lane >> 2) + 8 * e;
+            const long long lo = sLo[r], hi = sHi[r];
+            float best = -CUDART_INF_F;
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const long long pos = pos0 + n * 8 + 2 * t4 + c;
+                    float v = sc[n][2 * e + c] * scale_log2;
+                    v = (pos >= lo && pos < hi) ? v : -CUDART_INF_F;
+                    sc[n][2 * e + c] = v;
+                    best = fmaxf(best, v);
+                }
+            best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
+            best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
+            const float mnew = fmaxf(m[e], best);
+            const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
+            alpha[e] = exp2f(m[e] - muse);
+            m[e] = mnew;
+            mx[e] = muse;
+        }
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float pr = exp2f(sc[n][c] - mx[c >> 1]);
+                sc[n][c] = pr;
+                rs[c >> 1] += pr;
+            }
+        l[0] = l[0] * alpha[0] + rs[0];
+        l[1] = l[1] * alpha[1] + rs[1];
+#pragma unroll
+        for (int n = 0; n < DP / 8; ++n) {
+            acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
+            acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
+        }
+        // P (bf16, A layout straight from the S accumulators) times V.
+        unsigned pa[4];
+        pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+        pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+        pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+        pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+        const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int vcol = (lane >> 4) << 3;
+#pragma unroll
+        for (int dn = 0; dn < DP / 16; ++dn) {
+            unsigned b[4];
+            ldmatrix_x4_trans(b, sV + vrow * LD + dn * 16 + vcol);
+            mma_bf16_16816(acc[2 * dn], pa, b[0], b[1]);
+            mma_bf16_16816(acc[2 * dn + 1], pa, b[2], b[3]);
+        }
+    }
+
+    __device__ void store(float *sMo, float *sMm, float *sMl, int kw, int mt, int lane) {
+        constexpr int R = C::kRows;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float ls = l[e];
+            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+            const int r = mt * 16 + (lane >> 2) + 8 * e;
+            if ((lane & 3) == 0) {
+                sMm[kw * R + r] = m[e];
+                sMl[kw * R + r] = ls;
+            }
+            float *row = sMo + ((size_t)kw * R + r) * DP;
+#pragma unroll
+            for (int n = 0; n < DP / 8; ++n) {
+                *reinterpret_cast<float2 *>(row + n * 8 + 2 * (lane & 3)) =
+                    make_float2(acc[n][2 * e], acc[n][2 * e + 1]);
+            }
+        }
+    }
+};
+
+// CUDA-core state of one warp: 16 rows; for QK^T lane = key (lane % 16) x
+// half of head_dim (lane / 16); for PV lane = head_dim / 32 columns.
+template <class C>
+struct SimtWarp {
+    using T = typename C::T;
+    static constexpr int DP = C::DP, LD = C::kLd, EPC = C::kEpc, DPL = DP / 32;
+    static constexpr int HCH = C::kChunks / 2;   // chunks per half row
+    float m[16], l[16];
+    float acc[16][DPL];
+
+    __device__ void init() {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            m[r] = -CUDART_INF_F;
+            l[r] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[r][e] = 0.f;
+        }
+    }
+
+    __device__ void consume(const float *sQf, const T *sK, const T *sV, long long pos0,
+                            const int *sLo, const int *sHi, int mt, int lane, int nrw,
+                            float scale_log2, float *sPw) {
+        const int kq = lane & 15, hf = lane >> 4;
+        float dot[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) dot[r] = 0.f;
+#pragma unroll
+        for (int c = 0; c < HCH; ++c) {
+            const int col = (hf * HCH + c) * EPC;
+            float kf[EPC];
+            load_f32<T, EPC>(kf, sK + kq * LD + col);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                if (r < nrw) {
+                    const float *qr = sQf + (mt * 16 + r) * C::kQLdF + col;
+#pragma unroll
+                    for (int e = 0; e < EPC; e += 4) {
+                        float4 qv = *reinterpret_cast<const float4 *>(qr + e);
+                        dot[r] = fmaf(qv.x, kf[e], dot[r]);
+                        dot[r] = fmaf(qv.y, kf[e + 1], dot[r]);
+                        dot[r] = fmaf(qv.z, kf[e + 2], dot[r]);
+                        dot[r] = fmaf(qv.w, kf[e + 3], dot[r]);
+                    }
+                }
+            }
+        }
+        const long long pos = pos0 + kq;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            if (r < nrw) {
+                float d = dot[r] + __shfl_xor_sync(0xffffffffu, dot[r], 16);
+                const int rr = mt * 16 + r;
+                float sv = (pos >= sLo[rr] && pos < sHi[rr]) ? d * scale_log2 : -CUDART_INF_F;
+                float best = sv;
+                best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
+                best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
+                best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 4));
+                best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 8));
+                const float mnew = fmaxf(m[r], best);
+                const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
+                const float alpha = exp2f(m[r] - muse);
+                const float pr = exp2f(sv - muse);
+                m[r] = mnew;
+                l[r] = l[r] * alpha + pr;
+                if (hf == 0) sPw[r * 16 + kq] = pr;
+                if (lane == 0) sPw[256 + r] = alpha;
+            }
+        }
+        __syncwarp();
+        const int d0 = lane * DPL;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            if (r < nrw) {
+                const float a = sPw[256 + r];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[r][e] *= a;
+            }
+        }
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+            float vf[DPL];
+            load_f32<T, DPL>(vf, sV + k * LD + d0);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                if (r < nrw) {
+                    const float pr = sPw[r * 16 + k];
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) acc[r][e] = fmaf(pr, vf[e], acc[r][e]);
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    __device__ void store(float *sMo, float *sMm, float *sMl, int kw, int mt, int lane, int nrw) {
+        constexpr int R = C::kRows;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float ls = l[r];
+            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+            const int rr = mt * 16 + r;
+            if (lane == 0) {
+                sMm[kw * R + rr] = r < nrw ? m[r] : -CUDART_INF_F;
+                sMl[kw * R + rr] = r < nrw ? ls : 0.f;
+            }
+            float *row = sMo + ((size_t)kw * R + rr) * DP + lane * DPL;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) row[e] = r < nrw ? acc[r][e] : 0.f;
+        }
+    }
+};
+
+// ---------------------------------------------------------------- rows no segment covers
+
+// One CTA zeroes every output row that no segment covers and flags rows that
+// two segments claim.  Segments with a negative q_start or non-positive q_len
+// cover nothing.
+static __device__ void zero_uncovered(const AttendParams &p, int *sFlags, int nthreads) {
+    const int tid = threadIdx.x;
+    for (int base = 0; base < p.total_rows; base += nthreads) {
+        const int t = base + tid;
+        int cnt = 0;
+        if (t < p.total_rows) {
+            for (int s = 0; s < p.S; ++s) {
+                const Segment g = load_segment(p.seq_info, s);
+                if (g.q0 >= 0 && g.ql > 0 && t >= g.q0 && (long long)t < (long long)g.q0 + g.ql) ++cnt;
+            }
+            if (cnt > 1) atomicOr(p.err, PKV_ERR_OVERLAP);
+        }
+        sFlags[tid] = (t < p.total_rows && cnt == 0);
+        __syncthreads();
+        const int n = min(nthreads, p.total_rows - base);
+        const int per_row = p.Hq * p.D;
+        for (int r = 0; r < n; ++r) {
+            if (!sFlags[r]) continue;
+            const long long t2 = base + r;
+            for (int e = tid; e < per_row; e += nthreads) p.out[t2 * per_row + e] = 0.f;
+            if (p.lse)
+                for (int e = tid; e < p.Hq; e += nthreads) p.lse[t2 * p.Hq + e] = -CUDART_INF_F;
+        }
+        __syncthreads();
+    }
+}
+
+// Zero the rows of kv head g's group for a segment that failed validation.
+static __device__ void zero_segment_rows(const AttendParams &p, const Segment &sg, int g, int nthreads) {
+    if (sg.ql <= 0) return;
+    const long long a = max(sg.q0, 0);
+    const long long b = min((long long)sg.q0 + sg.ql, (long long)p.total_rows);
+    const int per = p.G * p.D;
+    for (long long t = a; t < b; ++t) {
+        float *o = p.out + (t * p.Hq + (long long)g * p.G) * p.D;
+        for (int e = threadIdx.x; e < per; e += nthreads) o[e] = 0.f;
+        if (p.lse)
+            for (int e = threadIdx.x; e < p.G; e += nthreads) p.lse[t * p.Hq + g * p.G + e] = -CUDART_INF_F;
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_constant__ AttendParams p) {
+    using T = typename C::T;
+    constexpr int DP = C::DP, MT = C::MT, KW = C::KW, NST = C::NST, LD = C::kLd;
+    constexpr int EPC = C::kEpc, R = C::kRows, NT = C::kThreads;
+    constexpr int GT = MT * 32;  // threads per key group
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *body = smem + C::kQBytes;
+    T *sPipe = reinterpret_cast<T *>(body);
+    float *sMo = reinterpret_cast<float *>(body);
+    float *sMm = sMo + (size_t)KW * R * DP;
+    float *sMl = sMm + KW * R;
+    int *sLo = reinterpret_cast<int *>(body + C::kBodyBytes);
+    int *sHi = sLo + R;
+    float *sSimt = reinterpret_cast<float *>(sHi + R);
+    __shared__ int sLast;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int mt = warp % MT, kw = warp / MT;
+    const int gtid = tid - kw * GT;  // thread index inside the key group
+    const int split = blockIdx.x;
+    const int g = blockIdx.y / p.row_tiles, rt = blockIdx.y - g * p.row_tiles;
+    const int s = blockIdx.z;
+
+    if (s == p.S) {  // extra slice: rows no segment covers
+        pdl_wait();
+        pdl_trigger();
+        if (blockIdx.x == 0 && blockIdx.y == 0) zero_uncovered(p, sLo, NT);
+        return;
+    }
+
+    // ---- segment and its key range (reads allowed before the dependency wait)
+    const Segment sg = load_segment(p.seq_info, s);
+    unsigned fault = segment_fault(sg, p.total_rows, p.max_seqs, p.mbps, p.ring_rows, p.window);
+    if (!fault && sg.ql > p.max_q_len) fault = PKV_ERR_QLEN;
+    if (fault) {
+        pdl_wait();
+        pdl_trigger();
+        if (split == 0 && rt == 0) {
+            if (tid == 0) atomicOr(p.err, fault);
+            zero_segment_rows(p, sg, g, NT);
+        }
+        return;
+    }
+    const int rows_unit = sg.ql * p.G;
+    const int row0 = rt * R;
+    if (row0 >= rows_unit) {
+        pdl_wait();
+        pdl_trigger();
+        return;
+    }
+    const int rows_here = min(R, rows_unit - row0);
+    const long long kend = sg.kend;
+    const long long new_start = kend - sg.ql;  // first position appended this step
+    long long lo_u = 0;
+    if (p.window > 0) lo_u = max(0LL, (p.causal ? new_start : kend - 1) - p.window + 1);
+    const long long pb_begin = lo_u / kPage;
+    const long long pb_end = (kend + kPage - 1) / kPage;
+    const long long nblk = pb_end - pb_begin;
+    const long long bps = max((long long)p.min_blocks, (nblk + p.nsplits - 1) / p.nsplits);
+    const int active = (int)((nblk + bps - 1) / bps);
+    if (split >= active) {
+        pdl_wait();
+        pdl_trigger();
+        return;
+    }
+    const long long cb0 = pb_begin + (long long)split * bps;
+    const int nb = (int)(min(cb0 + bps, pb_end) - cb0);
+    const int n_mine = nb > kw ? (nb - kw + KW - 1) / KW : 0;
+    const int unit = (s * p.Hkv + g) * p.row_tiles + rt;
+
+    const T *kpool = reinterpret_cast<const T *>(p.k_pool);
+    const T *vpool = reinterpret_cast<const T *>(p.v_pool);
+    const T *knew = reinterpret_cast<const T *>(p.k_new);
+    const T *vnew = reinterpret_cast<const T *>(p.v_new);
+    const bool fused = knew != nullptr;
+    const int dchunks = p.D / EPC;  // real 16-byte chunks per row
+    const int* bt_row = p.block_table + (long long)sg.col * p.mbps;
+
+    // Page ids of this group's pages, 32 at a time: lane l holds the id of
+    // the group's page (window + l).
+    int id_reg = -1;
+    int id_window = -1;
+    auto load_ids = [&](int j) {
+        id_window = j & ~31;
+        const int li = kw + (id_window + lane) * KW;
+        id_reg = -1;
+        if (li < nb) id_reg = bt_row[table_page(cb0 + li, p.ring_rows)];
+    };
+    bool bad = false;
+
+    auto issue = [&](int j) {
+        if ((j & ~31) != id_window) load_ids(j);
+        const int bid = __shfl_sync(0xffffffffu, id_reg, j & 31);
+        const int li = kw + j * KW;
+        if (li >= nb) return;
+        const bool bid_ok = bid >= 0 && (long long)bid < p.num_blocks;
+        bad |= !bid_ok;
+        const long long pos_base = (cb0 + li) * kPage;
+        T *st = sPipe + ((size_t)kw * NST + (j % NST)) * C::kStage;
+        constexpr int kPer = 2 * kPage * C::kChunks;
+#pragma unroll 4
+        for (int c = gtid; c < kPer; c += GT) {
+            const int kv = c / (kPage * C::kChunks);
+            const int rem = c - kv * (kPage * C::kChunks);
+            const int o = rem / C::kChunks;
+            const int ch = rem - o * C::kChunks;
+            const long long pos = pos_base + o;
+            bool ok = bid_ok && pos >= lo_u && pos < kend && ch < dchunks;
+            const T *src = kpool;
+            if (ok) {
+                if (fused && pos >= new_start) {
+                    const T *base = kv ? vnew : knew;
+                    src = base + (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D + ch * EPC;
+                } else {
+                    const T *base = kv ? vpool : kpool;
+                    src = base + (((long long)bid * kPage + o) * p.Hkv + g) * p.D + ch * EPC;
+                }
+            }
+            cp_async16(st + kv * C::kTile + o * LD + ch * EPC, src, ok);
+        }
+    };
+    // Pages wholly below new_start hold keys written before this step, so they
+    // may be fetched before the dependency wait.
+    auto early_ok = [&](int j) { return (cb0 + kw + (long long)j * KW + 1) * kPage <= new_start; };
+
+    // ---- prologue: start the first stages before waiting on the previous kernel
+    int issued = 0;
+    load_ids(0);
+    for (; issued < NST - 1; ++issued) {
+        if (issued < n_mine && !early_ok(issued)) break;
+        issue(issued);
+        cp_async_commit();
+    }
+    pdl_wait();
+    pdl_trigger();
+
+    // Query rows of this tile and their key bounds.
+    if constexpr (C::MMA) {
+        T *sQ = reinterpret_cast<T *>(smem);
+        for (int c = tid; c < R * C::kChunks; c += NT) {
+            const int r = c / C::kChunks, ch = c - r * C::kChunks;
+            const int ur = row0 + r;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (ur < rows_unit && ch < dchunks) {
+                const int i = ur / p.G, jh = ur - i * p.G;
+                const T *src = reinterpret_cast<const T *>(p.q) +
+                               (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D + ch * EPC;
+                v = *reinterpret_cast<const uint4 *>(src);
+            }
+            *reinterpret_cast<uint4 *>(sQ + r * LD + ch * EPC) = v;
+        }
+    } else {
+        float *sQf = reinterpret_cast<float *>(smem);
+        for (int c = tid; c < R * C::kChunks; c += NT) {
+            const int r = c / C::kChunks, ch = c - r * C::kChunks;
+            const int ur = row0 + r;
+            float f[EPC];
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) f[e] = 0.f;
+            if (ur < rows_unit && ch < dchunks) {
+                const int i = ur / p.G, jh = ur - i * p.G;
+                const T *src = reinterpret_cast<const T *>(p.q) +
+                               (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D + ch * EPC;
+                load_f32<T, EPC>(f, src);
+            }
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) sQf[r * C::kQLdF + ch * EPC + e] = f[e];
+        }
+    }
+    for (int r = tid; r < R; r += NT) {
+        const int ur = row0 + r;
+        int lo = 0, hi = 0;
+        if (ur < rows_unit) {
+            const long long pos = new_start + ur / p.G;
+            const long long newest = p.causal ? pos : kend - 1;
+            hi = (int)(p.causal ? pos + 1 : kend);
+            lo = p.window > 0 ? (int)max(0LL, newest - p.window + 1) : 0;
+        }
+        sLo[r] = lo;
+        sHi[r] = hi;
+    }
+    for (; issued < NST - 1; ++issued) {
+        issue(issued);
+        cp_async_commit();
+    }
+    __syncthreads();
+
+    // ---- main loop over this group's pages
+    const int nrw = max(0, min(16, rows_here - mt * 16));
+    MmaWarp<C> mw;
+    SimtWarp<C> sw;
+    if constexpr (C::MMA) mw.init(reinterpret_cast<const T *>(smem), mt, lane);
+    else sw.init();
+    float *sPw = sSimt + warp * (16 * 16 + 16);
+
+    for (int j = 0; j < n_mine; ++j) {
+        cp_async_wait<NST - 2>();
+        if constexpr (MT == 1) __syncwarp(); else named_barrier(1 + kw, GT);
+        issue(j + NST - 1);
+        cp_async_commit();
+        const T *st = sPipe + ((size_t)kw * NST + (j % NST)) * C::kStage;
+        const long long pos0 = (cb0 + kw + (long long)j * KW) * kPage;
+        if (nrw > 0) {
+            if constexpr (C::MMA)
+                mw.consume(reinterpret_cast<const T *>(smem), st, st + C::kTile, pos0, sLo, sHi, mt, lane,
+                           p.scale_log2);
+            else
+                sw.consume(reinterpret_cast<const float *>(smem), st, st + C::kTile, pos0, sLo, sHi, mt,
+                           lane, nrw, p.scale_log2, sPw);
+        }
+    }
+    cp_async_wait<0>();
+    const bool any_bad = __syncthreads_or(bad);
+
+    // ---- fused append: the CTA whose pages hold this step's positions writes them
+    if (fused && rt == 0) {
+        const long long lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
+        if (new_start < hi_pos && kend > lo_pos) {
+            bool ok = true;
+            for (int i = tid; i < sg.ql; i += NT) {
+                const long long pos = new_start + i;
+                const long long rr = p.ring_rows ? pos % p.ring_rows : pos;
+                const int b = bt_row[rr / kPage];
+                ok &= b >= 0 && (long long)b < p.num_blocks;
+            }
+            if (__syncthreads_and(ok)) {
+                const long long a = max(new_start, lo_pos), e = min(kend, hi_pos);
+                const int per = (int)(e - a) * dchunks;
+                for (int c = tid; c < 2 * per; c += NT) {
+                    const int kv = c / per;
+                    const int rem = c - kv * per;
+                    const long long pos = a + rem / dchunks;
+                    const int ch = rem % dchunks;
+                    const long long rr = p.ring_rows ? pos % p.ring_rows : pos;
+                    const long long b = bt_row[rr / kPage];
+                    const T *src = (kv ? vnew : knew) +
+                                   (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D + ch * EPC;
+                    T *dst = reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
+                             ((b * kPage + rr % kPage) * p.Hkv + g) * p.D + ch * EPC;
+                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+                }
+            }
+        }
+    }
+
+    // ---- merge the key groups of each row tile
+    if (nrw > 0 || !C::MMA) {
+        if constexpr (C::MMA) mw.store(sMo, sMm, sMl, kw, mt, lane);
+        else sw.store(sMo, sMm, sMl, kw, mt, lane, nrw);
+    }
+    __syncthreads();
+    if (any_bad && tid == 0) atomicOr(p.err, PKV_ERR_BLOCK);
+
+    constexpr float kLn2 = 0.6931471805599453f;
+    const long long part = ((long long)unit * p.nsplits + split) * R;
+    for (int idx = tid; idx < rows_here * DP; idx += NT) {
+        const int r = idx / DP, d = idx - r * DP;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) M = fmaxf(M, sMm[k * R + r]);
+        float L = 0.f, o = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int k = 0; k < KW; ++k) {
+                const float w = exp2f(sMm[k * R + r] - M);
+                L = fmaf(w, sMl[k * R + r], L);
+                o = fmaf(w, sMo[((size_t)k * R + r) * DP + d], o);
+            }
+        }
+        o = L > 0.f ? o / L : 0.f;
+        const float lse2 = L > 0.f ? M + log2f(L) : -CUDART_INF_F;
+        if (active == 1) {
+            const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
+            const long long orow = ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
+            if (d < p.D) p.out[orow * p.D + d] = any_bad ? 0.f : o;
+            if (d == 0 && p.lse) p.lse[orow] = any_bad ? -CUDART_INF_F : lse2 * kLn2;
+        } else {
+            __stcg(p.ws_o + (part + r) * DP + d, o);
+            if (d == 0) __stcg(p.ws_lse + part + r, any_bad ? CUDART_INF_F : lse2);
+        }
+    }
+    if (active == 1) return;
+
+    // ---- ticket: the last split of this (segment, kv head, row tile) merges
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sLast = atomicAdd(p.ws_ticket + unit, 1u) == (unsigned)(active - 1);
+    __syncthreads();
+    if (!sLast) return;
+    __threadfence();
+    const long long part0 = (long long)unit * p.nsplits * R;
+    for (int idx = tid; idx < rows_here * DP; idx += NT) {
+        const int r = idx / DP, d = idx - r * DP;
+        float M = -CUDART_INF_F;
+        bool poison = false;
+        for (int k = 0; k < active; ++k) {
+            const float l2 = __ldcg(p.ws_lse + part0 + (long long)k * R + r);
+            poison |= l2 == CUDART_INF_F;
+            M = fmaxf(M, l2);
+        }
+        float W = 0.f, o = 0.f;
+        if (!poison && M != -CUDART_INF_F) {
+            for (int k = 0; k < active; ++k) {
+                const float w = exp2f(__ldcg(p.ws_lse + part0 + (long long)k * R + r) - M);
+                W += w;
+                o = fmaf(w, __ldcg(p.ws_o + (part0 + (long long)k * R + r) * DP + d), o);
+            }
+        }
+        const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
+        const long long orow = ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
+        if (d < p.D) p.out[orow * p.D + d] = W > 0.f ? o / W : 0.f;
+        if (d == 0 && p.lse) p.lse[orow] = W > 0.f ? (M + log2f(W)) * kLn2 : -CUDART_INF_F;
+    }
+    if (tid == 0) p.ws_ticket[unit] = 0u;
+}
+
+}  // namespace pkv

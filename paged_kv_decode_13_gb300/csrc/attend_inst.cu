@@ -1,0 +1,105 @@
+// Instantiates the attention kernel for one (variant, padded head_dim) pair.
+// Built once per pair with -DPKV_INST_VARIANT=<0|1|2> -DPKV_INST_DP=<64|128|256>
+// so the configurations compile in parallel.
+//
+// Per row class the tuple is (row tiles MT, key groups KW, stages NST): stage
+// counts keep a CTA near 100-135 KB of shared memory where the page size
+// allows (two CTAs per SM), and fp32 / wide heads drop to fewer key groups or
+// a 64-row cap to stay inside the 227 KB limit.
+#include "attend.cuh"
+#include "launch.h"
+
+#ifndef PKV_INST_VARIANT
+#error "PKV_INST_VARIANT not set"
+#endif
+#ifndef PKV_INST_DP
+#error "PKV_INST_DP not set"
+#endif
+
+namespace pkv {
+
+template <class C>
+static AttnKernel info() {
+    static_assert(C::kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
+    return AttnKernel{reinterpret_cast<const void *>(&attend_kernel<C>), C::kThreads, C::kSmemBytes,
+                      C::kRows, C::DP, C::MMA};
+}
+
+using B16 = __nv_bfloat16;
+#define CFG(T, MT, KW, NST, MMA) info<AttnCfg<T, PKV_INST_DP, MT, KW, NST, MMA>>()
+
+#define PICK_NAME2(V, DP) pick_##V##_##DP
+#define PICK_NAME(V, DP) PICK_NAME2(V, DP)
+
+AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
+#if PKV_INST_VARIANT == 0
+#if PKV_INST_DP == 64
+    {
+        if (rc == 0) return CFG(B16, 1, 4, 4, true);
+        if (rc == 1) return CFG(B16, 2, 2, 4, true);
+        if (rc == 2) return CFG(B16, 4, 1, 4, true);
+        return CFG(B16, 8, 1, 4, true);
+    }
+#elif PKV_INST_DP == 128
+    {
+        if (rc == 0) return CFG(B16, 1, 4, 3, true);
+        if (rc == 1) return CFG(B16, 2, 2, 4, true);
+        if (rc == 2) return CFG(B16, 4, 1, 4, true);
+        return CFG(B16, 8, 1, 4, true);
+    }
+#else
+    {
+        if (rc == 0) return CFG(B16, 1, 4, 2, true);
+        if (rc == 1) return CFG(B16, 2, 2, 3, true);
+        if (rc == 2) return CFG(B16, 4, 1, 4, true);
+        return CFG(B16, 8, 1, 4, true);
+    }
+#endif
+#elif PKV_INST_VARIANT == 1
+#if PKV_INST_DP == 64
+    {
+        if (rc == 0) return CFG(B16, 1, 4, 4, false);
+        if (rc == 1) return CFG(B16, 2, 2, 4, false);
+        if (rc == 2) return CFG(B16, 4, 1, 4, false);
+        return CFG(B16, 8, 1, 4, false);
+    }
+#elif PKV_INST_DP == 128
+    {
+        if (rc == 0) return CFG(B16, 1, 4, 3, false);
+        if (rc == 1) return CFG(B16, 2, 2, 4, false);
+        if (rc == 2) return CFG(B16, 4, 1, 4, false);
+        return CFG(B16, 8, 1, 4, false);
+    }
+#else
+    {
+        if (rc == 0) return CFG(B16, 1, 4, 2, false);
+        if (rc == 1) return CFG(B16, 2, 2, 3, false);
+        return CFG(B16, 4, 1, 4, false);
+    }
+#endif
+#else
+#if PKV_INST_DP == 64
+    {
+        if (rc == 0) return CFG(float, 1, 4, 3, false);
+        if (rc == 1) return CFG(float, 2, 2, 4, false);
+        if (rc == 2) return CFG(float, 4, 1, 4, false);
+        return CFG(float, 8, 1, 4, false);
+    }
+#elif PKV_INST_DP == 128
+    {
+        if (rc == 0) return CFG(float, 1, 4, 2, false);
+        if (rc == 1) return CFG(float, 2, 2, 3, false);
+        if (rc == 2) return CFG(float, 4, 1, 4, false);
+        return CFG(float, 8, 1, 4, false);
+    }
+#else
+    {
+        if (rc == 0) return CFG(float, 1, 2, 2, false);
+        if (rc == 1) return CFG(float, 2, 2, 2, false);
+        return CFG(float, 4, 1, 2, false);
+    }
+#endif
+#endif
+}
+
+}  // namespace pkv

@@ -1,0 +1,154 @@
+// Device helpers shared by the pkv kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kPage = PKV_BLOCK_SIZE;  // tokens per page
+
+// ---------------------------------------------------------------- element types
+
+template <typename T> struct Elem;
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+    __device__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+template <> struct Elem<float> {
+    static constexpr int kBytes = 4;
+    __device__ static float to_f32(float x) { return x; }
+};
+
+// ---------------------------------------------------------------- async copies
+
+// 16-byte global -> shared copy that bypasses L1.  When `pred` is false the
+// destination is zero-filled and nothing is read (src-size 0).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool pred) {
+    unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    int n = pred ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grid this launch depends on has completed and its writes are
+// visible (a no-op when the launch did not use programmatic serialisation).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Allow the next grid on the stream to begin launching.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------- tensor-core fragments
+
+__device__ __forceinline__ void ldmatrix_x4(unsigned (&r)[4], const void *smem) {
+    unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(s));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(unsigned (&r)[4], const void *smem) {
+    unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(s));
+}
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const unsigned (&a)[4], unsigned b0,
+                                               unsigned b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<unsigned *>(&v);
+}
+
+// Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- launch parameters
+
+struct Segment {
+    int q0, ql, col, kend;
+};
+
+// Everything one attention launch reads; passed by value as a grid constant.
+struct AttendParams {
+    const void *q;          // [rows][Hq][D]
+    const void *k_pool;     // [num_blocks][16][Hkv][D]
+    const void *v_pool;
+    const void *k_new;      // fused append: [rows][Hkv][D], else null
+    const void *v_new;
+    void *k_pool_w;         // fused append: writable aliases of the pools
+    void *v_pool_w;
+    const int *block_table; // [max_seqs][mbps]
+    const int4 *seq_info;   // [S]
+    float *out;             // [rows][Hq][D]
+    float *lse;             // [rows][Hq] or null
+    float *ws_o;            // [units][splits][Rmax][D] split partials (normalised)
+    float *ws_lse;          // [units][splits][Rmax] log2-sum-exp of each partial
+    unsigned *ws_ticket;    // [units]
+    unsigned *err;
+    long long num_blocks;
+    int Hq, Hkv, D, G;      // G = Hq / Hkv
+    int total_rows, S;
+    int max_seqs, mbps, ring_rows;
+    int max_q_len, rows_max; // rows_max = G * max_q_len
+    int row_tiles;          // CTAs along the rows of one (segment, kv head)
+    int nsplits, min_blocks;
+    int causal, window;
+    float scale_log2;       // softmax_scale * log2(e)
+};
+
+struct AppendParams {
+    const void *k_new, *v_new;  // [rows][Hkv][D]
+    void *k_pool, *v_pool;
+    const int *block_table;
+    const int4 *seq_info;
+    unsigned *err;
+    long long num_blocks;
+    int row_bytes;              // Hkv * D * elem
+    int total_rows, S, max_seqs, mbps, ring_rows, window;
+};
+
+// ---------------------------------------------------------------- segment rules
+
+// Field and capacity checks shared by append and attention; returns PKV_ERR_* or 0.
+__device__ __forceinline__ unsigned segment_fault(const Segment &s, int total_rows, int max_seqs,
+                                                  int mbps, int ring_rows, int window) {
+    if (s.q0 < 0 || s.ql < 0 || (long long)s.q0 + s.ql > total_rows) return PKV_ERR_SEGMENT;
+    if (s.col < 0 || s.col >= max_seqs) return PKV_ERR_SEGMENT;
+    if (s.kend < s.ql) return PKV_ERR_SEGMENT;
+    if (ring_rows) {
+        if (window <= 0 || (long long)window + s.ql - 1 > ring_rows) return PKV_ERR_RING;
+    } else if ((long long)s.kend > (long long)mbps * kPage) {
+        return PKV_ERR_CAPACITY;
+    }
+    return 0;
+}
+
+// Page index in the sequence's table row for logical position-block `pb`
+// (positions pb*16 .. pb*16+15).  Ring rows are a multiple of 16, so a page
+// of positions never straddles the wrap.
+__device__ __forceinline__ int table_page(long long pb, int ring_rows) {
+    return ring_rows ? (int)(pb % (ring_rows / kPage)) : (int)pb;
+}
+
+__device__ __forceinline__ Segment load_segment(const int4 *seq_info, int s) {
+    int4 v = seq_info[s];
+    return Segment{v.x, v.y, v.z, v.w};
+}
+
+}  // namespace pkv

@@ -1,0 +1,121 @@
+"""CUDA-graph decode step over the paged cache: one capture per bucket.
+
+Mirrors vLLM-Omni's SenseNova-U1 DecodeGraphRunner without a model: every
+input a step varies (the new rows' q/k/v and the segment table holding the
+live lengths) sits in static device tensors, so one captured graph of
+`num_layers` append+attend launches serves every length in the bucket.  A
+capture is keyed on (bucket, generation); a resize bumps the generation and
+the next step captures again.  Warm-up runs three times on a side stream
+before capture (it rewrites the same rows to the same slots, so it is
+idempotent), and every capture shares one graph memory pool: a private pool
+per runner grew device memory without bound in the page's measurement.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional, Tuple
+
+import torch
+
+from . import _lib
+from .api import PagedKVCache, append, append_attend, attend_varlen, new_err_flags, new_workspace
+
+_SHARED_POOL = None
+
+
+def shared_pool():
+    global _SHARED_POOL
+    if _SHARED_POOL is None:
+        _SHARED_POOL = torch.cuda.graph_pool_handle()
+    return _SHARED_POOL
+
+
+class DecodeStep:
+    """Static buffers and launches of one decode step over all layers."""
+
+    def __init__(self, cache: PagedKVCache, num_q_heads: int, rows: int = 1, num_segments: int = 1,
+                 max_q_len: int = 1, max_kv: Optional[int] = None, scale: Optional[float] = None,
+                 causal: bool = False, window: int = 0, fused: bool = True, pdl: bool = True,
+                 flags: int = 0, num_splits: int = 0, with_lse: bool = False):
+        dev = cache.k[0].device
+        L, Hkv, D = cache.num_layers, cache.kv_heads, cache.head_dim
+        self.cache = cache
+        self.num_q_heads = num_q_heads
+        self.max_q_len = max_q_len
+        self.max_kv = int(max_kv if max_kv is not None else cache.bucket)
+        self.scale = scale if scale is not None else 1.0 / math.sqrt(D)
+        self.causal, self.window = causal, window
+        self.fused, self.pdl, self.flags, self.num_splits = fused, pdl, flags, num_splits
+        self.q = [torch.zeros(rows, num_q_heads, D, dtype=cache.dtype, device=dev) for _ in range(L)]
+        self.k_new = [torch.zeros(rows, Hkv, D, dtype=cache.dtype, device=dev) for _ in range(L)]
+        self.v_new = [torch.zeros(rows, Hkv, D, dtype=cache.dtype, device=dev) for _ in range(L)]
+        self.out = [torch.zeros(rows, num_q_heads, D, dtype=torch.float32, device=dev) for _ in range(L)]
+        self.lse = [torch.zeros(rows, num_q_heads, dtype=torch.float32, device=dev) for _ in range(L)] \
+            if with_lse else [None] * L
+        self.seq_info = torch.zeros(num_segments, 4, dtype=torch.int32, device=dev)
+        self.err = new_err_flags(dev)
+        self.workspace = new_workspace(cache, num_q_heads, num_segments, max_q_len, self.max_kv, num_splits,
+                                       device=dev)
+
+    def launch_count(self) -> int:
+        return self.cache.num_layers * (1 if self.fused else 2)
+
+    def run(self, stream=None) -> None:
+        """Enqueue every layer's append + attention on the current stream."""
+        c = self.cache
+        for layer in range(c.num_layers):
+            flags = self.flags
+            if self.pdl and layer > 0 and self.fused:
+                flags |= _lib.FLAG_PDL
+            if self.fused:
+                append_attend(c, layer, self.q[layer], self.k_new[layer], self.v_new[layer], self.seq_info,
+                              self.out[layer], self.err, self.workspace, self.max_q_len, self.max_kv,
+                              self.scale, self.causal, self.window, lse=self.lse[layer],
+                              num_splits=self.num_splits, flags=flags, stream=stream)
+            else:
+                append(c, layer, self.k_new[layer], self.v_new[layer], self.seq_info, self.err,
+                       window=self.window, stream=stream)
+                attend_varlen(c, layer, self.q[layer], self.seq_info, self.out[layer], self.err, self.workspace,
+                              self.max_q_len, self.max_kv, self.scale, self.causal, self.window,
+                              lse=self.lse[layer], num_splits=self.num_splits, flags=flags, stream=stream)
+
+
+class DecodeGraphRunner:
+    """One captured DecodeStep per (bucket, generation), replayed for every length."""
+
+    def __init__(self, step: DecodeStep):
+        self.step_bufs = step
+        self._graphs: Dict[Tuple[int, int], torch.cuda.CUDAGraph] = {}
+        self.captures = 0
+
+    def _capture(self, key):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                self.step_bufs.run()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, pool=shared_pool()):
+            self.step_bufs.run()
+        self.captures += 1
+        self._graphs[key] = graph
+        return graph
+
+    def rebind(self, cache: PagedKVCache) -> None:
+        """Point the step at a resized cache; captures of older buffers are dropped."""
+        st = self.step_bufs
+        st.cache = cache
+        st.max_kv = cache.bucket
+        st.workspace = new_workspace(cache, st.num_q_heads, int(st.seq_info.shape[0]), st.max_q_len, st.max_kv,
+                                     st.num_splits, device=st.seq_info.device)
+        self._graphs = {k: g for k, g in self._graphs.items() if k == (cache.bucket, cache.generation)}
+
+    def graph_for(self) -> torch.cuda.CUDAGraph:
+        c = self.step_bufs.cache
+        key = (c.bucket, c.generation)
+        return self._graphs.get(key) or self._capture(key)
+
+    def step(self) -> None:
+        """Replay the step for whatever lengths the segment table holds now."""
+        self.graph_for().replay()

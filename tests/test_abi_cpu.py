@@ -1,0 +1,167 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point include/pkv.h declares, and rejects bad arguments on the host before
+launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "bucket_for.txt")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_decode_13_gb300 import _lib
+    return _lib
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_named_calls():
+    names = declared_symbols()
+    for n in ("pkv_append", "pkv_attend_varlen", "pkv_resize_bucket", "pkv_load_prefix"):
+        assert n in names
+    assert len(names) >= 10
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_symbols() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_struct_layout_matches_header(lib):
+    # int32 x4, int64, int32 x4, three pointers, int64 x2 on LP64.
+    assert ctypes.sizeof(lib.CacheDesc) == 4 * 4 + 8 + 4 * 4 + 3 * 8 + 2 * 8
+    assert lib.CacheDesc.k.offset == 40 and lib.CacheDesc.bucket.offset == 64
+
+
+def test_bucket_for_matches_golden(lib):
+    from oracle import oracle as O
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        length, bucket = (int(x) for x in line.split())
+        assert lib.lib.pkv_bucket_for(length) == bucket
+        assert O.bucket_for(length) == bucket
+    for length in range(0, 40000, 37):
+        assert lib.lib.pkv_bucket_for(length) == O.bucket_for(length)
+
+
+def test_status_strings(lib):
+    for s in (0, 1, 2, -1, -2, -3, -4, -5, -6):
+        assert lib.lib.pkv_status_str(s)
+    assert b"unknown" in lib.lib.pkv_status_str(99)
+
+
+def _desc(lib, **kw):
+    fake = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    d = lib.CacheDesc(num_layers=1, kv_heads=2, head_dim=64, dtype=lib.BF16, num_blocks=32, max_seqs=1,
+                      max_blocks_per_seq=32, ring_rows=0, reserved0=0, k=ctypes.cast(fake, ctypes.c_void_p),
+                      v=ctypes.cast(ctypes.byref(fake, 8), ctypes.c_void_p), block_table=0x3000, bucket=512,
+                      generation=0)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d, fake
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 72 + 4, -2),      # not a multiple of 8
+    ("head_dim", 264, -2),         # above 256
+    ("dtype", 7, -2),
+    ("kv_heads", 0, -1),
+    ("ring_rows", 24, -1),         # not a multiple of 16
+    ("ring_rows", 1024, -1),       # beyond the table's capacity
+    ("num_blocks", 0, -1),
+])
+def test_bad_cache_rejected_before_launch(lib, field, value, status):
+    d, keep = _desc(lib, **{field: value})
+    L = lib.lib
+    st = L.pkv_attend_varlen(ctypes.byref(d), 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 0.125, 0, 0,
+                             0x6000, None, None, 0, 0x7000, 0, None)
+    assert st == status
+    st = L.pkv_append(ctypes.byref(d), 0, 0x4000, 0x4000, 1, 0x5000, 1, 0, 0x7000, None)
+    assert st == status
+
+
+def test_bad_call_arguments_rejected(lib):
+    d, keep = _desc(lib)
+    L = lib.lib
+    ref = ctypes.byref(d)
+    # q heads not a multiple of kv heads
+    assert L.pkv_attend_varlen(ref, 0, 0x4000, 3, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
+                               0x7000, 0, None) == -1
+    # layer out of range
+    assert L.pkv_attend_varlen(ref, 1, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
+                               0x7000, 0, None) == -1
+    # misaligned q
+    assert L.pkv_attend_varlen(ref, 0, 0x4004, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
+                               0x7000, 0, None) == -1
+    # missing error word
+    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
+                               None, 0, None) == -1
+    # causal must be 0 or 1, window >= 0
+    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 2, 0, 0x6000, None, None, 0,
+                               0x7000, 0, None) == -1
+    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, -1, 0x6000, None, None, 0,
+                               0x7000, 0, None) == -1
+    # split-K without a workspace
+    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 4, 1.0, 0, 0, 0x6000, None, None, 0,
+                               0x7000, 0, None) == -6
+    # fused call without k_new / v_new
+    assert L.pkv_append_attend(ref, 0, 0x4000, None, None, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000,
+                               None, None, 0, 0x7000, 0, None) == -1
+
+
+def test_workspace_sizes(lib):
+    d, keep = _desc(lib)
+    L = lib.lib
+    ref = ctypes.byref(d)
+    assert L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 1) == 0          # one split: no workspace
+    w4 = L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 4)
+    w8 = L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 8)
+    assert 0 < w4 < w8
+    # 2 kv heads x 1 segment x 8 splits x 16 rows x (64 + 1) floats, plus tickets
+    assert w8 >= 2 * 8 * 16 * 65 * 4
+    assert L.pkv_attend_workspace_bytes(ref, 3, 1, 1, 512, 4) == 0          # invalid -> 0
+
+
+def test_resize_and_prefix_host_rules(lib):
+    L = lib.lib
+    a, ka = _desc(lib)
+    b, kb = _desc(lib, num_layers=1, head_dim=128)
+    assert L.pkv_resize_bucket(ctypes.byref(a), ctypes.byref(b), 10, None) == -5   # shapes differ
+    c, kc = _desc(lib)
+    assert L.pkv_resize_bucket(ctypes.byref(a), ctypes.byref(c), 10, None) == 2    # same bucket
+    c.bucket = 1024
+    assert L.pkv_resize_bucket(ctypes.byref(a), ctypes.byref(c), 10_000, None) == -4
+    assert c.generation == 0
+    assert L.pkv_load_prefix(ctypes.byref(a), None, None, 5, 128, 64, None) == 1   # empty
+    assert L.pkv_load_prefix(ctypes.byref(a), ctypes.cast(ka, ctypes.c_void_p), ctypes.cast(ka, ctypes.c_void_p),
+                             0, 128, 64, None) == 1
+    assert L.pkv_load_prefix(ctypes.byref(a), ctypes.cast(ka, ctypes.c_void_p), ctypes.cast(ka, ctypes.c_void_p),
+                             10_000, 128, 64, None) == -4
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import subprocess
+    import sys
+    # A copy of the binding package with no libpkv.so must refuse to import.
+    pkg = tmp_path / "paged_kv_decode_13_gb300"
+    pkg.mkdir()
+    src = os.path.join(ROOT, "paged_kv_decode_13_gb300")
+    for f in ("__init__.py", "_lib.py", "api.py", "graph.py"):
+        (pkg / f).write_text(open(os.path.join(src, f)).read())
+    r = subprocess.run([sys.executable, "-c", "import paged_kv_decode_13_gb300"], cwd=tmp_path,
+                       capture_output=True, text=True)
+    assert r.returncode != 0 and "libpkv.so not found" in r.stderr

@@ -1,0 +1,326 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI.
+
+Attention: max-abs error <= 2e-3 for bf16 inputs (fp32 out, fp32
+accumulation) and <= 1e-5 for fp32 inputs.  Append, resize and prefix copies:
+bit-exact.  Pools carry NaN in every slot no segment may read, and guard
+margins around pools and outputs catch out-of-range writes.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_decode_13_gb300 as m
+    return m
+
+
+def run(pkv, w, layer=0, fused=True, flags=0, num_splits=0, max_q_len=None, max_kv=None, canary=True):
+    """Append + attend layer `layer` of w on the GPU.  Returns (out, lse, err, cache)."""
+    cache = U.device_cache(pkv, w, canary=canary)
+    dev = torch.device("cuda")
+    q = w.q[layer].to(dev)
+    kn = w.k_new[layer].to(dev)
+    vn = w.v_new[layer].to(dev)
+    si = w.seq_info.to(dev)
+    mq = max_q_len or w.max_q_len
+    mk = max_kv or max(int(w.seq_info[:, 3].max()) if w.num_segments else 1, 1)
+    obuf, out = U.guarded_out(w.total_rows, w.q_heads, w.head_dim)
+    lse = torch.full((max(w.total_rows, 1), w.q_heads), 3.0, device=dev)[:w.total_rows]
+    err = pkv.new_err_flags()
+    ws = pkv.new_workspace(cache, w.q_heads, w.num_segments, mq, mk, num_splits)
+    if fused:
+        pkv.append_attend(cache, layer, q, kn, vn, si, out, err, ws, mq, mk, w.scale, w.causal, w.window, lse=lse,
+                          num_splits=num_splits, flags=flags)
+    else:
+        pkv.append(cache, layer, kn, vn, si, err, window=w.window)
+        pkv.attend_varlen(cache, layer, q, si, out, err, ws, mq, mk, w.scale, w.causal, w.window, lse=lse,
+                          num_splits=num_splits, flags=flags)
+    torch.cuda.synchronize()
+    U.check_guarded(obuf)
+    U.check_canaries(cache)
+    return out, lse, int(err.item()), cache
+
+
+def check_against_oracle(w, layer, out, lse, cache, segs=None, tol=None):
+    tol = tol or U.TOL[w.dtype]
+    ref, ref_lse = U.oracle_attend(w, layer, segs=segs)
+    rows = U.rows_of(w, segs) if segs is not None else list(range(w.total_rows))
+    got = U.f64(out)[rows]
+    exp = ref[rows]
+    assert np.isfinite(got).all()
+    diff = float(np.abs(got - exp).max()) if rows else 0.0
+    assert diff <= tol, f"max abs error {diff} > {tol}"
+    gl, el = U.f64(lse)[rows], ref_lse[rows]
+    same_inf = np.isinf(gl) == np.isinf(el)
+    assert same_inf.all()
+    fin = np.isfinite(el)
+    if fin.any():
+        assert float(np.abs(gl[fin] - el[fin]).max()) <= max(tol, 1e-5)
+    return diff
+
+
+def check_append(w, layer, cache):
+    kp, vp, err = U.oracle_append_pools(w, layer)
+    assert err == 0
+    assert U.pool_bytes(cache.k[layer]) == kp.tobytes(), "K pool differs from the oracle's append"
+    assert U.pool_bytes(cache.v[layer]) == vp.tobytes(), "V pool differs from the oracle's append"
+
+
+# ---------------------------------------------------------------- the five workloads, reduced
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_tiny_fp32(pkv, fused):
+    w = U.nan_tails(workloads.tiny(seed=0))
+    out, lse, err, cache = run(pkv, w, fused=fused)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+@pytest.mark.parametrize("seqused", [1, 15, 16, 17, 300, 1000, 1024])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_sensenova_shape(pkv, seqused, flags):
+    w = U.nan_tails(workloads.sensenova(seqused, 1024, num_layers=2, seed=seqused))
+    for layer in (0, 1):
+        out, lse, err, cache = run(pkv, w, layer=layer, flags=flags, max_kv=1024)
+        assert err == 0
+        check_append(w, layer, cache)
+        check_against_oracle(w, layer, out, lse, cache)
+
+
+@pytest.mark.parametrize("flags,fused", [(0, True), (0, False), (1, True)])
+def test_batched_varlen(pkv, flags, fused):
+    w = U.nan_tails(workloads.batched(S=8, max_len=3000, seed=3))
+    out, lse, err, cache = run(pkv, w, fused=fused, flags=flags, max_kv=3000)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+@pytest.mark.parametrize("q_heads", [8, 16, 32, 64])
+@pytest.mark.parametrize("causal", [True, False])
+def test_spec_verify(pkv, q_heads, causal):
+    w = U.nan_tails(workloads.spec_verify(S=6, max_q=16, len_lo=256, len_hi=2000, causal=causal, seed=q_heads,
+                                          q_heads=q_heads))
+    for flags in (0, 1):
+        out, lse, err, cache = run(pkv, w, flags=flags, max_kv=2000)
+        assert err == 0
+        check_append(w, 0, cache)
+        check_against_oracle(w, 0, out, lse, cache)
+
+
+@pytest.mark.parametrize("window,ring", [(0, 0), (1000, 0), (1024, 1024), (300, 320)])
+def test_long_context(pkv, window, ring):
+    w = U.nan_tails(workloads.long_context(S=2, kv_len=20000, window=window, ring_rows=ring, seed=5))
+    out, lse, err, cache = run(pkv, w, max_kv=20000)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+# ---------------------------------------------------------------- shapes, splits, modes
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("head_dim", [8, 40, 64, 72, 96, 136, 192, 256])
+def test_head_dims(pkv, dtype, head_dim):
+    w = U.nan_tails(workloads.batched(S=3, max_len=700, seed=head_dim, q_heads=8, kv_heads=2, head_dim=head_dim,
+                                      dtype=dtype))
+    out, lse, err, cache = run(pkv, w, max_kv=700)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 16, 0])
+def test_split_count_does_not_change_result(pkv, num_splits):
+    w = U.nan_tails(workloads.sensenova(2500, 4096, num_layers=1, seed=9))
+    out, lse, err, cache = run(pkv, w, num_splits=num_splits, max_kv=4096)
+    assert err == 0
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+def test_fused_equals_two_calls_bitwise(pkv):
+    w = U.nan_tails(workloads.spec_verify(S=5, max_q=8, len_lo=100, len_hi=900, seed=11, q_heads=16))
+    a, la, ea, ca = run(pkv, w, fused=True, max_kv=900)
+    b, lb, eb, cb = run(pkv, w, fused=False, max_kv=900)
+    assert ea == eb == 0
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    assert U.pool_bytes(ca.k[0]) == U.pool_bytes(cb.k[0])
+
+
+@pytest.mark.parametrize("window", [1, 7, 33, 500])
+def test_causal_window_flat(pkv, window):
+    w = U.nan_tails(workloads.spec_verify(S=4, max_q=12, len_lo=40, len_hi=800, seed=window, q_heads=16))
+    w.window = window
+    out, lse, err, cache = run(pkv, w, max_kv=800)
+    assert err == 0
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+def test_ring_wraps_many_times(pkv):
+    # kv_end far past the ring: the window keys sit at slots p % R after many wraps.
+    w = workloads.long_context(S=3, kv_len=50_001, window=64, ring_rows=80, seed=13, q_heads=8, kv_heads=2,
+                               head_dim=64)
+    w = U.nan_tails(w)
+    out, lse, err, cache = run(pkv, w, max_kv=50_001)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+# ---------------------------------------------------------------- edge cases
+
+def _single(kend, ql=1, D=64, dtype=torch.bfloat16, seed=0, nblocks=None, Hq=4, Hkv=2):
+    g = torch.Generator().manual_seed(seed)
+    nb = nblocks or max((kend + 15) // 16, 1) + 1
+    k = [torch.randn(nb, 16, Hkv, D, generator=g).to(dtype)]
+    v = [torch.randn(nb, 16, Hkv, D, generator=g).to(dtype)]
+    rows = max(ql, 1)
+    q = [torch.randn(rows, Hq, D, generator=g).to(dtype)]
+    kn = [torch.randn(rows, Hkv, D, generator=g).to(dtype)]
+    vn = [torch.randn(rows, Hkv, D, generator=g).to(dtype)]
+    bt = torch.arange(nb, dtype=torch.int32).unsqueeze(0)
+    si = torch.tensor([[0, ql, 0, kend]], dtype=torch.int32)
+    return workloads.Workload("edge", dtype, 1, Hq, Hkv, D, nb, bt, si, k, v, q, kn, vn, causal=True,
+                              bucket=nb * 16, max_q_len=max(ql, 1))
+
+
+def test_single_key_returns_new_value(pkv):
+    w = _single(1)
+    out, lse, err, cache = run(pkv, w, max_kv=16)
+    assert err == 0
+    for h in range(4):
+        assert torch.equal(out[0, h].cpu(), w.v_new[0][0, h // 2].float())
+
+
+def test_zero_length_segments_and_uncovered_rows(pkv):
+    w = U.nan_tails(workloads.spec_verify(S=4, max_q=4, len_lo=20, len_hi=200, seed=21, q_heads=8))
+    si = w.seq_info.clone()
+    si[1, 1] = 0                     # an empty segment
+    si[:, 0] += 2                    # two leading rows no segment covers
+    w.seq_info = si
+    extra = 5
+    for lst in (w.q, w.k_new, w.v_new):
+        lst[0] = torch.cat([lst[0], lst[0][:extra]], 0)
+    out, lse, err, cache = run(pkv, w, max_kv=200)
+    assert err == 0
+    covered = set(U.rows_of(w, range(4)))
+    for t in range(w.total_rows):
+        if t not in covered:
+            assert not out[t].abs().sum().item() and bool(torch.isinf(lse[t]).all())
+    check_against_oracle(w, 0, out, lse, cache, segs=[0, 2, 3])
+
+
+def test_no_segments_zeroes_every_row(pkv):
+    w = _single(10, ql=1)
+    w.seq_info = torch.zeros(0, 4, dtype=torch.int32)
+    w.q[0] = torch.cat([w.q[0]] * 3)
+    w.k_new[0] = torch.cat([w.k_new[0]] * 3)
+    w.v_new[0] = torch.cat([w.v_new[0]] * 3)
+    out, lse, err, cache = run(pkv, w, max_q_len=1, max_kv=16)
+    assert err == 0 and not out.abs().sum().item() and bool(torch.isinf(lse).all())
+
+
+@pytest.mark.parametrize("seg,window,ring,bit", [
+    ([0, 2, 0, 1], 0, 0, 1),        # kv_end < q_len
+    ([0, 1, 3, 10], 0, 0, 1),       # col past max_seqs
+    ([0, 3, 0, 10], 0, 0, 1),       # rows past total_rows
+    ([0, 1, 0, 100000], 0, 0, 2),   # past the table's capacity
+    ([0, 1, 0, 40], 0, 32, 4),      # ring without a window
+    ([0, 2, 0, 40], 32, 32, 4),     # window + q_len - 1 > ring rows
+])
+def test_invalid_segment_sets_error_and_zeroes(pkv, seg, window, ring, bit):
+    w = _single(40, ql=2, nblocks=6)
+    w.seq_info = torch.tensor([seg], dtype=torch.int32)
+    w.window, w.ring_rows, w.causal = window, ring, True
+    before = U.pool_bytes(w.k[0])
+    out, lse, err, cache = run(pkv, w, max_q_len=2, max_kv=64)
+    assert err & bit, f"expected bit {bit}, got {err:#x}"
+    assert not out.abs().sum().item()
+    assert U.pool_bytes(cache.k[0]) == before          # nothing appended
+
+
+def test_bad_block_id_in_range(pkv):
+    w = _single(100, ql=1, nblocks=8)
+    bt = w.block_table.clone()
+    bt[0, 2] = 1 << 20
+    w.block_table = bt
+    out, lse, err, cache = run(pkv, w, max_kv=128, num_splits=3)
+    assert err & 8 and not out.abs().sum().item()
+    assert bool(torch.isinf(lse).all())
+
+
+def test_q_len_above_launch_bound(pkv):
+    w = _single(50, ql=4)
+    out, lse, err, cache = run(pkv, w, max_q_len=2, max_kv=64)
+    assert err & 16 and not out.abs().sum().item()
+
+
+def test_overlapping_segments_flagged(pkv):
+    w = U.nan_tails(workloads.spec_verify(S=2, max_q=4, len_lo=50, len_hi=60, seed=3, q_heads=8))
+    si = w.seq_info.clone()
+    si[1, 0] = si[0, 0]
+    w.seq_info = si
+    _, _, err, _ = run(pkv, w, max_kv=64)
+    assert err & 32
+
+
+# ---------------------------------------------------------------- table helpers, resize, prefix
+
+def test_seqinfo_from_seqused_and_advance(pkv):
+    cu = torch.tensor([0, 1, 4, 4, 9], dtype=torch.int32, device="cuda")
+    used = torch.tensor([7, 30, 2, 500], dtype=torch.int32, device="cuda")
+    si = torch.zeros(4, 4, dtype=torch.int32, device="cuda")
+    pkv.seqinfo_from_seqused(cu, used, si)
+    pkv.advance(si)
+    torch.cuda.synchronize()
+    expect = [[0, 1, 0, 8], [1, 3, 1, 33], [4, 0, 2, 2], [4, 5, 3, 505]]
+    assert si.cpu().tolist() == expect
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_resize_keeps_prefix_and_bumps_generation(pkv, dtype):
+    old = pkv.PagedKVCache.allocate(3, 4, 64, 512, dtype=dtype)
+    for t in old.k + old.v:
+        t.copy_(torch.randn(t.shape, device="cuda").to(dtype))
+    n = pkv.bucket_for(700)
+    new = pkv.PagedKVCache.allocate(3, 4, 64, n, dtype=dtype)
+    assert pkv.resize_bucket(old, new, 333) == 0
+    torch.cuda.synchronize()
+    assert new.generation == old.generation + 1
+    for a, b in zip(old.k + old.v, new.k + new.v):
+        fa, fb = a.view(-1, 4, 64), b.view(-1, 4, 64)
+        assert torch.equal(fa[:333], fb[:333])
+        assert not fb[333:].abs().sum().item()
+    same = pkv.PagedKVCache.allocate(3, 4, 64, 512, dtype=dtype)
+    assert pkv.resize_bucket(old, same, 10) == 2 and same.generation == 0
+
+
+def test_load_prefix_and_write_back(pkv):
+    L, H, S, D = 2, 4, 77, 64
+    cache = pkv.PagedKVCache.allocate(L, H, D, 512)
+    keys = [torch.randn(1, H, S, D, device="cuda").to(torch.bfloat16) for _ in range(L)]
+    vals = [torch.randn(1, H, S, D, device="cuda").to(torch.bfloat16) for _ in range(L)]
+    # [B, H, S, D] -> [S, H, D] views, as PagedDecodeCache.load_prefix does
+    assert pkv.load_prefix(cache, [k[0].transpose(0, 1) for k in keys], [v[0].transpose(0, 1) for v in vals])
+    assert not pkv.load_prefix(cache, [keys[0][0, :, :0].transpose(0, 1)] * L,
+                               [vals[0][0, :, :0].transpose(0, 1)] * L)
+    for layer in range(L):
+        ko = torch.empty(H, S, D, dtype=torch.bfloat16, device="cuda")
+        vo = torch.empty_like(ko)
+        pkv.to_contiguous(cache, layer, S, ko, vo)
+        torch.cuda.synchronize()
+        assert torch.equal(ko, keys[layer][0]) and torch.equal(vo, vals[layer][0])
+        flat = cache.k[layer].view(-1, H, D)
+        assert torch.equal(flat[:S], keys[layer][0].transpose(0, 1))
