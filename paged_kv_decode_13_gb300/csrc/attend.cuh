@@ -52,6 +52,7 @@ struct AttnCfg {
     static constexpr size_t kSmemBytes = kQBytes + kBodyBytes + kBoundsBytes + kSimtBytes;
     static_assert(kQBytes % 16 == 0 && kBodyBytes % 16 == 0, "smem sections stay 16-byte aligned");
     static_assert(!MMA || sizeof(T) == 2, "tensor-core path is bf16");
+    static_assert(kBodyBytes >= (size_t)kThreads * 4, "coverage pass keeps one int per thread in the body");
 };
 
 // ---------------------------------------------------------------- small vector loads
@@ -410,7 +411,8 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     if (s == p.S) {  // extra slice: rows no segment covers
         pdl_wait();
         pdl_trigger();
-        if (blockIdx.x == 0 && blockIdx.y == 0) zero_uncovered(p, sLo, NT);
+        // The pipeline region is idle in this CTA; it holds one flag per thread.
+        if (blockIdx.x == 0 && blockIdx.y == 0) zero_uncovered(p, reinterpret_cast<int *>(body), NT);
         return;
     }
 
