@@ -10,12 +10,12 @@
  * run, so one capture serves every length the grid was sized for.
  *
  * Errors come back two ways.  Problems visible on the host (bad sizes, null
- * or misaligned pointers, an unsupported head_dim or dtype, a workspace that
- * is too small) return a negative pkv_status before anything is launched.
- * Problems only the device sees (a segment whose fields are out of range, a
- * block id outside the pool, ...) set PKV_ERR_* bits in the caller's
- * `err_flags` word with an atomic OR and zero that segment's output; no
- * kernel traps, asserts or waits on another block.
+ * or misaligned pointers, an unsupported head_dim or dtype) return a negative
+ * pkv_status before anything is launched.  Problems only the device sees (a
+ * segment whose fields are out of range, a block id outside the pool, ...)
+ * set PKV_ERR_* bits in the caller's `err_flags` word with an atomic OR and
+ * zero that segment's output; no kernel traps or asserts, and every wait
+ * inside a kernel is bounded.
  *
  * Sources, by page and section:
  *   [vllm-omni paged_decode.py]  "Paged KV cache for SenseNova-U1
@@ -51,8 +51,7 @@ typedef enum pkv_status {
     PKV_EUNSUPPORTED = -2,  /* dtype or head_dim the kernels do not cover */
     PKV_ECUDA = -3,         /* a CUDA launch or copy failed to enqueue */
     PKV_ECAPACITY = -4,     /* the destination cannot hold the requested tokens */
-    PKV_ESTALE = -5,        /* descriptors that do not describe the same cache shape */
-    PKV_EWORKSPACE = -6     /* workspace null or smaller than pkv_attend_workspace_bytes */
+    PKV_ESTALE = -5         /* descriptors that do not describe the same cache shape */
 } pkv_status;
 
 typedef enum pkv_dtype { PKV_BF16 = 0, PKV_F32 = 1 } pkv_dtype;
@@ -64,6 +63,7 @@ typedef enum pkv_dtype { PKV_BF16 = 0, PKV_F32 = 1 } pkv_dtype;
 #define PKV_ERR_BLOCK    (1u << 3)  /* a block-table entry the segment needs is outside [0, num_blocks) */
 #define PKV_ERR_QLEN     (1u << 4)  /* q_len above the max_q_len the launch was sized for */
 #define PKV_ERR_OVERLAP  (1u << 5)  /* an output row lies in two segments (its value is then unspecified) */
+#define PKV_ERR_TIMEOUT  (1u << 6)  /* a bounded wait for a K/V copy inside the kernel gave up; output zeroed */
 
 /* Flags for the attention calls. */
 #define PKV_FLAG_SIMT  (1u << 0)  /* bf16: use the CUDA-core kernel instead of the tensor-core one */
@@ -146,21 +146,6 @@ int pkv_append(const pkv_cache *cache, int32_t layer,
                uint32_t *err_flags, void *stream);
 
 /*
- * Bytes of device workspace pkv_attend_varlen / pkv_append_attend need for a
- * launch of this shape (split-K partials and per-(segment, kv head) tickets).
- * The workspace must be zero-filled before its first use (pkv_workspace_init
- * does that); every call leaves its tickets at zero again, so it can be
- * reused by later calls and graph replays on the same stream.  num_splits = 0
- * asks for the automatic split count.  Returns 0 for invalid arguments.
- */
-size_t pkv_attend_workspace_bytes(const pkv_cache *cache, int32_t num_q_heads,
-                                  int32_t num_segments, int32_t max_q_len,
-                                  int64_t max_kv, int32_t num_splits);
-
-/* Zero `bytes` of workspace on `stream` (a cudaMemsetAsync). */
-int pkv_workspace_init(void *workspace, size_t bytes, void *stream);
-
-/*
  * Decode attention over the paged cache ([ExecuTorch #24072]
  * triton::sdpa_varlen semantics over the paged layout of
  * [vllm-omni paged_decode.py]).
@@ -180,21 +165,24 @@ int pkv_workspace_init(void *workspace, size_t bytes, void *stream);
  * hold anything (NaN included).
  *
  * max_q_len bounds every segment's q_len and max_kv bounds every segment's
- * kv_end (used only to size the grid: a graph captured once serves every
- * length up to it).  num_splits = 0 picks the split-K count automatically;
- * otherwise the key range of each (segment, kv head) is cut into that many
- * pieces whose partial results are merged by log-sum-exp in the same launch.
+ * kv_end; both only size the launch, so a graph captured once serves every
+ * length up to them.  num_splits (0..16) is the number of CTAs that share one
+ * (segment, kv head) key range as a thread-block cluster; their partial
+ * softmax results are merged by log-sum-exp through distributed shared
+ * memory in the same launch, so no workspace is needed.  0 picks the count
+ * from the launch shape (and a smaller one if the device cannot co-schedule
+ * the cluster); a larger count than the segment has 16-token pages leaves
+ * CTAs idle.
  *
  * flags: PKV_FLAG_SIMT selects the CUDA-core kernel for bf16 (fp32 always
  * uses it).  PKV_FLAG_PDL launches with programmatic dependent launch: the
  * kernel may start reading cache slots of positions below kv_end - q_len,
  * the block table and seq_info while the previous kernel on the stream is
  * still running, so set it only when that previous kernel writes none of
- * those; q, k_new, v_new, out, lse, the workspace and err_flags are touched
- * only after it has finished.
+ * those; q, k_new, v_new, out, lse and err_flags are touched only after it
+ * has finished.
  *
- * Device pointers must be 16-byte aligned.  workspace: device, at least
- * pkv_attend_workspace_bytes(...) bytes, zero-filled before first use.
+ * Device pointers must be 16-byte aligned (out and lse: 4-byte).
  */
 int pkv_attend_varlen(const pkv_cache *cache, int32_t layer,
                       const void *q, int32_t num_q_heads, int32_t total_rows,
@@ -202,7 +190,6 @@ int pkv_attend_varlen(const pkv_cache *cache, int32_t layer,
                       int32_t max_q_len, int64_t max_kv, int32_t num_splits,
                       float softmax_scale, int32_t causal, int32_t window,
                       float *out, float *lse,
-                      void *workspace, size_t workspace_bytes,
                       uint32_t *err_flags, uint32_t flags, void *stream);
 
 /*
@@ -219,7 +206,6 @@ int pkv_append_attend(const pkv_cache *cache, int32_t layer,
                       int32_t max_q_len, int64_t max_kv, int32_t num_splits,
                       float softmax_scale, int32_t causal, int32_t window,
                       float *out, float *lse,
-                      void *workspace, size_t workspace_bytes,
                       uint32_t *err_flags, uint32_t flags, void *stream);
 
 /*

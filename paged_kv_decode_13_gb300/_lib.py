@@ -13,11 +13,11 @@ LIB_PATH = os.path.join(HERE, "libpkv.so")
 
 # pkv_status
 OK, EMPTY, SAME_BUCKET = 0, 1, 2
-EINVAL, EUNSUPPORTED, ECUDA, ECAPACITY, ESTALE, EWORKSPACE = -1, -2, -3, -4, -5, -6
+EINVAL, EUNSUPPORTED, ECUDA, ECAPACITY, ESTALE = -1, -2, -3, -4, -5
 # pkv_dtype
 BF16, F32 = 0, 1
 # device error bits
-ERR_SEGMENT, ERR_CAPACITY, ERR_RING, ERR_BLOCK, ERR_QLEN, ERR_OVERLAP = 1, 2, 4, 8, 16, 32
+ERR_SEGMENT, ERR_CAPACITY, ERR_RING, ERR_BLOCK, ERR_QLEN, ERR_OVERLAP, ERR_TIMEOUT = 1, 2, 4, 8, 16, 32, 64
 # attention flags
 FLAG_SIMT, FLAG_PDL = 1, 2
 BLOCK_SIZE = 16
@@ -46,18 +46,16 @@ class CacheDesc(ctypes.Structure):
 
 def _declare(lib):
     i32, i64, u32, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_float
-    p, sz = ctypes.c_void_p, ctypes.c_size_t
+    p = ctypes.c_void_p
     cp = ctypes.POINTER(CacheDesc)
     sigs = {
         "pkv_bucket_for": (i64, [i64]),
         "pkv_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "pkv_append": (ctypes.c_int, [cp, i32, p, p, i32, p, i32, i32, p, p]),
-        "pkv_attend_workspace_bytes": (sz, [cp, i32, i32, i32, i64, i32]),
-        "pkv_workspace_init": (ctypes.c_int, [p, sz, p]),
         "pkv_attend_varlen": (ctypes.c_int, [cp, i32, p, i32, i32, p, i32, i32, i64, i32, f32, i32, i32,
-                                             p, p, p, sz, p, u32, p]),
+                                             p, p, p, u32, p]),
         "pkv_append_attend": (ctypes.c_int, [cp, i32, p, p, p, i32, i32, p, i32, i32, i64, i32, f32, i32,
-                                             i32, p, p, p, sz, p, u32, p]),
+                                             i32, p, p, p, u32, p]),
         "pkv_seqinfo_from_seqused": (ctypes.c_int, [p, p, i32, p, p]),
         "pkv_advance": (ctypes.c_int, [p, i32, p]),
         "pkv_resize_bucket": (ctypes.c_int, [cp, cp, i64, p]),

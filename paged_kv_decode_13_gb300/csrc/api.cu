@@ -4,7 +4,9 @@
 // synchronises the host or keeps state beyond per-process kernel attributes.
 #include <cuda_runtime.h>
 
-#include <atomic>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
 #include <mutex>
 
 #include "launch.h"
@@ -15,8 +17,8 @@ using namespace pkv;
 namespace {
 
 constexpr int kDefaultSms = 152;       // GB300, used when no device is visible
-constexpr int kSmemPerSm = 233472;     // shared memory per SM available to CTAs
-constexpr int kMinBlocksPerSplit = 2;  // pages per split-K piece, at least
+constexpr int kTargetCtas = 4 * 152;   // aim for a few CTAs per SM when choosing the split count
+constexpr int kMaxCluster = 16;        // largest thread-block cluster (non-portable size)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -28,6 +30,7 @@ int check_cache(const pkv_cache *c) {
     // vLLM-Omni paged_decode_supported: head_dim a multiple of 8, at most 256.
     if (c->head_dim <= 0 || c->head_dim % 8 != 0 || c->head_dim > 256) return PKV_EUNSUPPORTED;
     if (c->num_layers <= 0 || c->kv_heads <= 0 || c->num_blocks <= 0) return PKV_EINVAL;
+    if (c->num_blocks > INT32_MAX || c->kv_heads > 65535) return PKV_EINVAL;
     if (c->max_seqs <= 0 || c->max_blocks_per_seq <= 0) return PKV_EINVAL;
     if (!c->k || !c->v || !c->block_table) return PKV_EINVAL;
     if ((reinterpret_cast<uintptr_t>(c->block_table) & 3u) != 0) return PKV_EINVAL;
@@ -42,26 +45,10 @@ int check_layer(const pkv_cache *c, int layer) {
     return PKV_OK;
 }
 
-int sm_count() {
-    static std::atomic<int> cached{0};
-    int v = cached.load();
-    if (v > 0) return v;
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        n = kDefaultSms;
-    }
-    cached.store(n);
-    return n;
-}
-
-// Launch plan of one attention call; identical for the workspace query and
-// the launch so both agree on the workspace layout.
+// Launch plan of one attention call.
 struct Plan {
     AttnKernel k;
-    int G, rows_max, row_tiles, units, nsplits;
-    size_t off_lse, off_o, bytes;
+    int G, rows_max, row_tiles, units, ncta;
 };
 
 AttnKernel pick(int variant, int dp, int rc) {
@@ -79,14 +66,56 @@ AttnKernel pick(int variant, int dp, int rc) {
     return AttnKernel{nullptr, 0, 0, 0, 0, false};
 }
 
-size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+// Largest cluster size <= want that the device can schedule for this kernel
+// (1 when no device answers the query).
+int schedulable_cluster(const AttnKernel &k, int want) {
+    static std::mutex mu;
+    static const void *fns[64];
+    static int best[64][kMaxCluster + 1];
+    static int n = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
+    for (int i = 0; i < n; ++i)
+        if (fns[i] == k.fn) slot = i;
+    if (slot < 0 && n < 64) {
+        slot = n++;
+        fns[slot] = k.fn;
+        for (int c = 0; c <= kMaxCluster; ++c) best[slot][c] = -1;
+    }
+    for (int c = want; c > 1; --c) {
+        if (slot >= 0 && best[slot][c] >= 0) {
+            if (best[slot][c] > 0) return c;
+            continue;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)c, 1, 1);
+        cfg.blockDim = dim3((unsigned)k.threads);
+        cfg.dynamicSmemBytes = k.smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)c;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, k.fn, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            clusters = 0;
+        }
+        if (slot >= 0) best[slot][c] = clusters > 0 ? 1 : 0;
+        if (clusters > 0) return c;
+    }
+    return 1;
+}
 
 int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv, int num_splits,
               unsigned flags, Plan *pl) {
     int st = check_cache(c);
     if (st) return st;
     if (Hq <= 0 || Hq % c->kv_heads != 0) return PKV_EINVAL;
-    if (S < 0 || max_q_len <= 0 || max_kv <= 0 || num_splits < 0) return PKV_EINVAL;
+    if (S < 0 || S > 65535 || max_q_len <= 0 || max_kv <= 0 || num_splits < 0 || num_splits > kMaxCluster)
+        return PKV_EINVAL;
     const int D = c->head_dim;
     const int dp = D <= 64 ? 64 : D <= 128 ? 128 : 256;
     const int variant = c->dtype == PKV_F32 ? kSimtF32 : (flags & PKV_FLAG_SIMT) ? kSimtBf16 : kMmaBf16;
@@ -98,35 +127,22 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
     pl->k = pick(variant, dp, rc);
     if (!pl->k.fn) return PKV_EUNSUPPORTED;
     pl->row_tiles = (int)((rows_max + pl->k.rows - 1) / pl->k.rows);
-    const long long units = (long long)S * c->kv_heads * pl->row_tiles;
-    if ((long long)c->kv_heads * pl->row_tiles > 65535 || S + 1 > 65535) return PKV_EINVAL;
+    if ((long long)c->kv_heads * pl->row_tiles > 65535) return PKV_EINVAL;
+    const long long units = (long long)std::max(S, 1) * c->kv_heads * pl->row_tiles;
     pl->units = (int)units;
     const long long max_pages = (max_kv + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE + 1;
-    const long long split_cap = (max_pages + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
-    long long ns = num_splits;
-    if (ns == 0) {
-        long long occ = std::min<long long>(2048 / pl->k.threads, kSmemPerSm / (long long)(pl->k.smem + 1024));
-        occ = std::max<long long>(occ, 1);
-        const long long target = (long long)sm_count() * occ;
-        ns = units > 0 ? (target + units - 1) / units : 1;
-        ns = std::max<long long>(1, std::min(ns, split_cap));
+    long long n = num_splits;
+    if (n == 0) {
+        const long long want = (kTargetCtas + units - 1) / units;
+        n = 1;
+        while (n < want && n < kMaxCluster) n *= 2;
     }
-    if (ns > 65535) return PKV_EINVAL;
-    pl->nsplits = (int)ns;
-    if (pl->nsplits == 1 || units == 0) {
-        pl->off_lse = pl->off_o = pl->bytes = 0;
-    } else {
-        const size_t tick = round256((size_t)units * 4);
-        const size_t lse = round256((size_t)units * ns * pl->k.rows * 4);
-        const size_t o = (size_t)units * ns * pl->k.rows * pl->k.dp * 4;
-        pl->off_lse = tick;
-        pl->off_o = tick + lse;
-        pl->bytes = tick + lse + o;
-    }
+    n = std::max<long long>(1, std::min<long long>(n, max_pages));
+    pl->ncta = (int)n;
     return PKV_OK;
 }
 
-// Opt a kernel into its dynamic shared memory size once per process.
+// Opt a kernel into its dynamic shared memory size and cluster sizes once per process.
 int prepare_kernel(const AttnKernel &k) {
     static std::mutex mu;
     static const void *done[64];
@@ -134,7 +150,8 @@ int prepare_kernel(const AttnKernel &k) {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < ndone; ++i)
         if (done[i] == k.fn) return PKV_OK;
-    if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem) != cudaSuccess ||
+        cudaFuncSetAttribute(k.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ECUDA;
     }
@@ -151,10 +168,46 @@ int launch_status(cudaError_t e) {
     return PKV_OK;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 4-D view (head_dim, kv_heads, 16, num_blocks) of one pool; a box is 128
+// bytes of one row of one kv head across the 16 tokens of a page, loaded with
+// 128-byte swizzling.
+int encode_pool(CUtensorMap *map, const void *pool, const pkv_cache *c) {
+    auto fn = encode_fn();
+    if (!fn) return PKV_ECUDA;
+    const int eb = elem_bytes(c->dtype);
+    const cuuint64_t D = (cuuint64_t)c->head_dim, H = (cuuint64_t)c->kv_heads;
+    cuuint64_t dims[4] = {D, H, (cuuint64_t)PKV_BLOCK_SIZE, (cuuint64_t)c->num_blocks};
+    cuuint64_t strides[3] = {D * eb, H * D * eb, (cuuint64_t)PKV_BLOCK_SIZE * H * D * eb};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / eb), 1, (cuuint32_t)PKV_BLOCK_SIZE, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    4, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ECUDA;
+}
+
 int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_new, const void *v_new,
                   int Hq, int total_rows, const int *seq_info, int S, int max_q_len, long long max_kv,
                   int num_splits, float scale, int causal, int window, float *out, float *lse,
-                  void *ws, size_t ws_bytes, unsigned *err, unsigned flags, void *stream) {
+                  unsigned *err, unsigned flags, void *stream) {
     Plan pl;
     int st = make_plan(c, Hq, S, max_q_len, max_kv, num_splits, flags, &pl);
     if (st) return st;
@@ -165,14 +218,13 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     if ((reinterpret_cast<uintptr_t>(out) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return PKV_EINVAL;
     if (k_new && (!v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
-    if (pl.bytes > 0 && (!ws || ws_bytes < pl.bytes || !aligned16(ws))) return PKV_EWORKSPACE;
     if (S == 0 && total_rows == 0) return PKV_OK;
     if ((st = prepare_kernel(pl.k))) return st;
+    const int ncta = S == 0 ? 1 : schedulable_cluster(pl.k, pl.ncta);
 
     AttendParams p;
+    if ((st = encode_pool(&p.tmap_k, c->k[layer], c)) || (st = encode_pool(&p.tmap_v, c->v[layer], c))) return st;
     p.q = q;
-    p.k_pool = c->k[layer];
-    p.v_pool = c->v[layer];
     p.k_new = k_new;
     p.v_new = v_new;
     p.k_pool_w = c->k[layer];
@@ -181,10 +233,6 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     p.seq_info = reinterpret_cast<const int4 *>(seq_info);
     p.out = out;
     p.lse = lse;
-    char *w = reinterpret_cast<char *>(ws);
-    p.ws_ticket = pl.bytes ? reinterpret_cast<unsigned *>(w) : nullptr;
-    p.ws_lse = pl.bytes ? reinterpret_cast<float *>(w + pl.off_lse) : nullptr;
-    p.ws_o = pl.bytes ? reinterpret_cast<float *>(w + pl.off_o) : nullptr;
     p.err = err;
     p.num_blocks = c->num_blocks;
     p.Hq = Hq;
@@ -197,26 +245,35 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     p.mbps = c->max_blocks_per_seq;
     p.ring_rows = c->ring_rows;
     p.max_q_len = max_q_len;
-    p.rows_max = pl.rows_max;
     p.row_tiles = pl.row_tiles;
-    p.nsplits = pl.nsplits;
-    p.min_blocks = kMinBlocksPerSplit;
     p.causal = causal;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pl.nsplits, (unsigned)(c->kv_heads * pl.row_tiles), (unsigned)(S + 1));
+    if (S == 0)
+        cfg.gridDim = dim3(1, 1, 1);
+    else
+        cfg.gridDim = dim3((unsigned)ncta, (unsigned)(c->kv_heads * pl.row_tiles), (unsigned)S);
     cfg.blockDim = dim3((unsigned)pl.k.threads);
     cfg.dynamicSmemBytes = pl.k.smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    if (flags & PKV_FLAG_PDL) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (ncta > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)ncta;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    if (flags & PKV_FLAG_PDL) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = (unsigned)na;
     void *args[] = {&p};
     return launch_status(cudaLaunchKernelExC(&cfg, pl.k.fn, args));
 }
@@ -228,7 +285,7 @@ int copy_rows(const void *s0, const void *s1, void *d0, void *d1, long long n, i
                  reinterpret_cast<char *>(d0), reinterpret_cast<char *>(d1), n, H, row_bytes / 16,
                  ss, sh, ds, dh};
     const long long total = 2 * n * H * (row_bytes / 16);
-    const long long blocks = std::min<long long>((total + 255) / 256, (long long)sm_count() * 8);
+    const long long blocks = std::min<long long>((total + 255) / 256, (long long)kDefaultSms * 8);
     strided_copy_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     return launch_status(cudaSuccess);
 }
@@ -256,7 +313,6 @@ const char *pkv_status_str(int s) {
         case PKV_ECUDA: return "CUDA launch or copy failed";
         case PKV_ECAPACITY: return "capacity exceeded";
         case PKV_ESTALE: return "caches describe different shapes";
-        case PKV_EWORKSPACE: return "workspace missing or too small";
     }
     return "unknown status";
 }
@@ -290,40 +346,22 @@ int pkv_append(const pkv_cache *c, int32_t layer, const void *k_new, const void 
     return launch_status(cudaSuccess);
 }
 
-size_t pkv_attend_workspace_bytes(const pkv_cache *c, int32_t Hq, int32_t S, int32_t max_q_len, int64_t max_kv,
-                                  int32_t num_splits) {
-    Plan pl;
-    if (make_plan(c, Hq, S, max_q_len, max_kv, num_splits, 0, &pl)) return 0;
-    // The CUDA-core bf16 kernel may use a different tile; report the larger.
-    Plan p2;
-    if (c->dtype == PKV_BF16 && !make_plan(c, Hq, S, max_q_len, max_kv, num_splits, PKV_FLAG_SIMT, &p2))
-        return std::max(pl.bytes, p2.bytes);
-    return pl.bytes;
-}
-
-int pkv_workspace_init(void *ws, size_t bytes, void *stream) {
-    if (bytes == 0) return PKV_OK;
-    if (!ws) return PKV_EINVAL;
-    return launch_status(cudaMemsetAsync(ws, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
-}
-
 int pkv_attend_varlen(const pkv_cache *c, int32_t layer, const void *q, int32_t Hq, int32_t total_rows,
                       const int32_t *seq_info, int32_t S, int32_t max_q_len, int64_t max_kv, int32_t num_splits,
-                      float scale, int32_t causal, int32_t window, float *out, float *lse, void *ws,
-                      size_t ws_bytes, uint32_t *err, uint32_t flags, void *stream) {
+                      float scale, int32_t causal, int32_t window, float *out, float *lse, uint32_t *err,
+                      uint32_t flags, void *stream) {
     return attend_common(c, layer, q, nullptr, nullptr, Hq, total_rows, seq_info, S, max_q_len, max_kv,
-                         num_splits, scale, causal, window, out, lse, ws, ws_bytes, err, flags, stream);
+                         num_splits, scale, causal, window, out, lse, err, flags, stream);
 }
 
 int pkv_append_attend(const pkv_cache *c, int32_t layer, const void *q, const void *k_new, const void *v_new,
                       int32_t Hq, int32_t total_rows, const int32_t *seq_info, int32_t S, int32_t max_q_len,
                       int64_t max_kv, int32_t num_splits, float scale, int32_t causal, int32_t window,
-                      float *out, float *lse, void *ws, size_t ws_bytes, uint32_t *err, uint32_t flags,
-                      void *stream) {
+                      float *out, float *lse, uint32_t *err, uint32_t flags, void *stream) {
     if (total_rows > 0 && (!k_new || !v_new)) return PKV_EINVAL;
     return attend_common(c, layer, q, total_rows > 0 ? k_new : nullptr, total_rows > 0 ? v_new : nullptr, Hq,
                          total_rows, seq_info, S, max_q_len, max_kv, num_splits, scale, causal, window, out, lse,
-                         ws, ws_bytes, err, flags, stream);
+                         err, flags, stream);
 }
 
 int pkv_seqinfo_from_seqused(const int32_t *cu, const int32_t *used, int32_t n, int32_t *out, void *stream) {

@@ -1,14 +1,16 @@
-// Split-K decode attention over a paged KV cache.
+// Split-K decode attention over a paged KV cache (sm_103a).
 //
-// One CTA per (split, kv head x row tile, segment).  The CTA holds the query
-// rows of one kv head's GQA group (G heads x q_len rows, zero-padded to 16-row
-// tiles) and streams the K/V pages of its share of the segment's key range
-// through a cp.async ring in shared memory, 16 tokens (one page of one kv
-// head) per stage.  Warps are arranged as MT row tiles x KW key groups: the
-// KW groups take alternate pages and keep separate online-softmax states that
-// are merged in shared memory at the end.  Splits of one (segment, kv head)
-// write normalised partials and their log2-sum-exp; the last split to finish
-// (a ticket counter, no waiting) merges them.
+// Grid (C, kv_heads x row tiles, segments); the C CTAs along x form one
+// thread-block cluster and split one (segment, kv head) key range between
+// them.  A CTA holds the query rows of one kv head's GQA group (G heads x
+// q_len rows, zero-padded to 16-row tiles) and streams its K/V pages through
+// shared memory: TMA (cp.async.bulk.tensor, 128-byte swizzle) brings one page
+// of one kv head (16 tokens) per stage into a ring of stages tracked by
+// mbarriers, one elected thread per ring issuing the copies.  Warps are MT row
+// tiles x KW key groups; each key group owns a ring and takes every KW-th
+// page, keeping its own online-softmax state.  At the end the key groups merge
+// in shared memory and the C partial results merge across the cluster through
+// distributed shared memory, each CTA producing a slice of the output.
 //
 // Semantics follow the segment-table attention of ExecuTorch PR #24072
 // (triton::sdpa_varlen) over the (num_blocks, 16, kv_heads, head_dim) paged
@@ -18,11 +20,16 @@
 // (ExecuTorch #24074), rows no segment covers read zero.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <math_constants.h>
 
 #include "common.cuh"
 
 namespace pkv {
+
+// Bound on the probes of one barrier phase; past it the kernel records
+// PKV_ERR_TIMEOUT, zeroes the affected output and carries on.
+constexpr int kWaitProbes = 1 << 20;
 
 template <typename T_, int DP_, int MT_, int KW_, int NST_, bool MMA_>
 struct AttnCfg {
@@ -36,23 +43,27 @@ struct AttnCfg {
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kRows = MT * 16;
     static constexpr int kElem = (int)sizeof(T);
-    static constexpr int kEpc = 16 / kElem;             // elements per 16-byte chunk
-    static constexpr int kLd = DP + kEpc;               // padded smem row (elements)
-    static constexpr int kChunks = DP / kEpc;           // 16-byte chunks per row
-    static constexpr int kTile = kPage * kLd;           // one K or V page, elements
-    static constexpr int kStage = 2 * kTile;
-    static constexpr int kQLdF = DP + 4;                // fp32 query row (CUDA-core path)
-    static constexpr size_t kQBytes =
-        MMA ? (size_t)kRows * kLd * kElem : (size_t)kRows * kQLdF * 4;
-    static constexpr size_t kPipeBytes = (size_t)KW * NST * kStage * kElem;
-    static constexpr size_t kMergeBytes = (size_t)KW * kRows * (DP + 2) * 4;
-    static constexpr size_t kBodyBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
-    static constexpr size_t kBoundsBytes = (size_t)kRows * 2 * 4;
+    static constexpr int kEpc = 16 / kElem;               // elements per 16-byte chunk
+    static constexpr int kChunks = DP / kEpc;             // 16-byte chunks per row
+    static constexpr int kBoxEl = 128 / kElem;            // elements per 128-byte swizzle box row
+    static constexpr int kBoxes = DP / kBoxEl;            // boxes per page tile
+    static constexpr unsigned kTileBytes = kPage * DP * kElem;  // one K or V page of one kv head
+    static constexpr unsigned kStageBytes = 2 * kTileBytes;
+    static constexpr int kQLd = MMA ? DP + 8 : DP + 4;    // padded query row (elements of T / fp32)
+    static constexpr size_t kPipeBytes = (size_t)KW * NST * kStageBytes;
+    static constexpr size_t kMergeBytes = (size_t)KW * kRows * DP * 4 + (size_t)2 * KW * kRows * 4;
+    static constexpr size_t kBodyBytes =
+        ((kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes) + 1023) & ~size_t(1023);
+    static constexpr size_t kQBytes = MMA ? (size_t)kRows * kQLd * 2 : (size_t)kRows * kQLd * 4;
+    static constexpr size_t kRowBytes = (size_t)kRows * (2 + 2 + 16 + 1) * 4;  // pm, pl, lo, hi, weights, lse
+    static constexpr size_t kBarBytes = (size_t)KW * NST * 8;
     static constexpr size_t kSimtBytes = MMA ? 0 : (size_t)kWarps * (16 * 16 + 16) * 4;
-    static constexpr size_t kSmemBytes = kQBytes + kBodyBytes + kBoundsBytes + kSimtBytes;
-    static_assert(kQBytes % 16 == 0 && kBodyBytes % 16 == 0, "smem sections stay 16-byte aligned");
+    static constexpr size_t kSmemBytes = 1024 + kBodyBytes + kQBytes + kRowBytes + kBarBytes + kSimtBytes + 16;
+    static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
+    static_assert(kQBytes % 16 == 0, "smem sections stay 16-byte aligned");
     static_assert(!MMA || sizeof(T) == 2, "tensor-core path is bf16");
     static_assert(kBodyBytes >= (size_t)kThreads * 4, "coverage pass keeps one int per thread in the body");
+    static_assert(kRows <= kThreads, "one thread per row in the cluster merge");
 };
 
 // ---------------------------------------------------------------- small vector loads
@@ -69,11 +80,6 @@ template <>
 __device__ __forceinline__ void load_f32<float, 4>(float (&o)[4], const float *s) {
     float4 v = *reinterpret_cast<const float4 *>(s);
     o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-}
-template <>
-__device__ __forceinline__ void load_f32<float, 8>(float (&o)[8], const float *s) {
-    float4 a = reinterpret_cast<const float4 *>(s)[0], b = reinterpret_cast<const float4 *>(s)[1];
-    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 __device__ __forceinline__ void bf2_to_f32(float *o, unsigned u) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
@@ -95,13 +101,22 @@ __device__ __forceinline__ void load_f32<__nv_bfloat16, 8>(float (&o)[8], const 
     bf2_to_f32(o, v.x); bf2_to_f32(o + 2, v.y); bf2_to_f32(o + 4, v.z); bf2_to_f32(o + 6, v.w);
 }
 
+// N consecutive elements starting at element `col` of row `row` in a
+// swizzled page tile, widened to fp32 (N * sizeof(T) <= 16 and aligned).
+template <typename T, int N>
+__device__ __forceinline__ void tile_load(float (&o)[N], const unsigned char *tile, int row, int col) {
+    constexpr int kEpc = 16 / (int)sizeof(T);
+    const int chunk = col / kEpc, within = col - chunk * kEpc;
+    load_f32<T, N>(o, reinterpret_cast<const T *>(tile + swz(row, chunk)) + within);
+}
+
 // ---------------------------------------------------------------- per-warp compute states
 
 // Tensor-core state of one warp: a 16-row tile, fp32 accumulators in the
 // mma.m16n8k16 C layout (thread holds rows lane/4 and lane/4 + 8).
 template <class C>
 struct MmaWarp {
-    static constexpr int DP = C::DP, LD = C::kLd;
+    static constexpr int DP = C::DP, LD = C::kQLd;
     float m[2], l[2];
     float acc[DP / 8][4];
     unsigned qf[DP <= 128 ? DP / 16 : 1][4];
@@ -118,13 +133,13 @@ struct MmaWarp {
         }
     }
 
-    __device__ void consume(const __nv_bfloat16 *sQ, const __nv_bfloat16 *sK, const __nv_bfloat16 *sV,
+    __device__ void consume(const __nv_bfloat16 *sQ, const unsigned char *sK, const unsigned char *sV,
                             long long pos0, const int *sLo, const int *sHi, int mt, int lane,
                             float scale_log2) {
         // S = Q K^T over the page's 16 keys.
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int krow = (lane & 7) + ((lane >> 4) << 3);
-        const int kcol = ((lane >> 3) & 1) << 3;
+        const int kchk = (lane >> 3) & 1;
 #pragma unroll
         for (int kk = 0; kk < DP / 16; ++kk) {
             unsigned a[4];
@@ -134,7 +149,7 @@ struct MmaWarp {
                 ldmatrix_x4(a, sQ + (mt * 16 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
             }
             unsigned b[4];
-            ldmatrix_x4(b, sK + krow * LD + kk * 16 + kcol);
+            ldmatrix_x4(b, sK + swz(krow, 2 * kk + kchk));
             mma_bf16_16816(sc[0], a, b[0], b[1]);
             mma_bf16_16816(sc[1], a, b[2], b[3]);
         }
@@ -175,10 +190,12 @@ struct MmaWarp {
             }
         l[0] = l[0] * alpha[0] + rs[0];
         l[1] = l[1] * alpha[1] + rs[1];
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-        for (int n = 0; n < DP / 8; ++n) {
-            acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
-            acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
+            for (int n = 0; n < DP / 8; ++n) {
+                acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
+                acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
+            }
         }
         // P (bf16, A layout straight from the S accumulators) times V.
         unsigned pa[4];
@@ -187,11 +204,11 @@ struct MmaWarp {
         pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
         pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
         const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int vcol = (lane >> 4) << 3;
+        const int vchk = lane >> 4;
 #pragma unroll
         for (int dn = 0; dn < DP / 16; ++dn) {
             unsigned b[4];
-            ldmatrix_x4_trans(b, sV + vrow * LD + dn * 16 + vcol);
+            ldmatrix_x4_trans(b, sV + swz(vrow, 2 * dn + vchk));
             mma_bf16_16816(acc[2 * dn], pa, b[0], b[1]);
             mma_bf16_16816(acc[2 * dn + 1], pa, b[2], b[3]);
         }
@@ -224,8 +241,9 @@ struct MmaWarp {
 template <class C>
 struct SimtWarp {
     using T = typename C::T;
-    static constexpr int DP = C::DP, LD = C::kLd, EPC = C::kEpc, DPL = DP / 32;
+    static constexpr int DP = C::DP, EPC = C::kEpc, DPL = DP / 32;
     static constexpr int HCH = C::kChunks / 2;   // chunks per half row
+    static constexpr int VL = DPL * C::kElem > 16 ? 16 / C::kElem : DPL;  // elements per V load
     float m[16], l[16];
     float acc[16][DPL];
 
@@ -239,9 +257,9 @@ struct SimtWarp {
         }
     }
 
-    __device__ void consume(const float *sQf, const T *sK, const T *sV, long long pos0,
-                            const int *sLo, const int *sHi, int mt, int lane, int nrw,
-                            float scale_log2, float *sPw) {
+    __device__ void consume(const float *sQf, const unsigned char *sK, const unsigned char *sV, long long pos0,
+                            const int *sLo, const int *sHi, int mt, int lane, int nrw, float scale_log2,
+                            float *sPw) {
         const int kq = lane & 15, hf = lane >> 4;
         float dot[16];
 #pragma unroll
@@ -250,11 +268,11 @@ struct SimtWarp {
         for (int c = 0; c < HCH; ++c) {
             const int col = (hf * HCH + c) * EPC;
             float kf[EPC];
-            load_f32<T, EPC>(kf, sK + kq * LD + col);
+            tile_load<T, EPC>(kf, sK, kq, col);
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 if (r < nrw) {
-                    const float *qr = sQf + (mt * 16 + r) * C::kQLdF + col;
+                    const float *qr = sQf + (mt * 16 + r) * C::kQLd + col;
 #pragma unroll
                     for (int e = 0; e < EPC; e += 4) {
                         float4 qv = *reinterpret_cast<const float4 *>(qr + e);
@@ -301,7 +319,13 @@ struct SimtWarp {
 #pragma unroll 4
         for (int k = 0; k < 16; ++k) {
             float vf[DPL];
-            load_f32<T, DPL>(vf, sV + k * LD + d0);
+#pragma unroll
+            for (int part = 0; part < DPL / VL; ++part) {
+                float tmp[VL];
+                tile_load<T, VL>(tmp, sV, k, d0 + part * VL);
+#pragma unroll
+                for (int e = 0; e < VL; ++e) vf[part * VL + e] = tmp[e];
+            }
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 if (r < nrw) {
@@ -386,33 +410,40 @@ static __device__ void zero_segment_rows(const AttendParams &p, const Segment &s
 template <class C>
 __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_constant__ AttendParams p) {
     using T = typename C::T;
-    constexpr int DP = C::DP, MT = C::MT, KW = C::KW, NST = C::NST, LD = C::kLd;
+    namespace cg = cooperative_groups;
+    constexpr int DP = C::DP, MT = C::MT, KW = C::KW, NST = C::NST;
     constexpr int EPC = C::kEpc, R = C::kRows, NT = C::kThreads;
     constexpr int GT = MT * 32;  // threads per key group
 
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *body = smem + C::kQBytes;
-    T *sPipe = reinterpret_cast<T *>(body);
-    float *sMo = reinterpret_cast<float *>(body);
-    float *sMm = sMo + (size_t)KW * R * DP;
-    float *sMl = sMm + KW * R;
-    int *sLo = reinterpret_cast<int *>(body + C::kBodyBytes);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *body = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *sMo = reinterpret_cast<float *>(body);          // [KW][R][DP], aliases the stages
+    float *sMm = sMo + (size_t)KW * R * DP;                 // [KW][R]
+    float *sMl = sMm + KW * R;                              // [KW][R]
+    unsigned char *qarea = body + C::kBodyBytes;
+    float *sPm = reinterpret_cast<float *>(qarea + C::kQBytes);  // [R] this CTA's merged max
+    float *sPl = sPm + R;                                   // [R] and sum
+    int *sLo = reinterpret_cast<int *>(sPl + R);            // [R] key bounds per row
     int *sHi = sLo + R;
-    float *sSimt = reinterpret_cast<float *>(sHi + R);
-    __shared__ int sLast;
+    float *sWt = reinterpret_cast<float *>(sHi + R);        // [R][16] cluster merge weights
+    float *sLse = sWt + R * 16;                             // [R]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sLse + R);  // [KW][NST]
+    float *sSimt = reinterpret_cast<float *>(bars + KW * NST);
+    int *sFlag = reinterpret_cast<int *>(sSimt + (C::kSimtBytes / 4));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = warp % MT, kw = warp / MT;
     const int gtid = tid - kw * GT;  // thread index inside the key group
-    const int split = blockIdx.x;
+    const int rank = blockIdx.x, ncta = gridDim.x;
     const int g = blockIdx.y / p.row_tiles, rt = blockIdx.y - g * p.row_tiles;
     const int s = blockIdx.z;
+    const bool first_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
-    if (s == p.S) {  // extra slice: rows no segment covers
+    if (p.S == 0) {  // nothing but rows no segment covers
         pdl_wait();
         pdl_trigger();
-        // The pipeline region is idle in this CTA; it holds one flag per thread.
-        if (blockIdx.x == 0 && blockIdx.y == 0) zero_uncovered(p, reinterpret_cast<int *>(body), NT);
+        if (first_cta) zero_uncovered(p, reinterpret_cast<int *>(body), NT);
         return;
     }
 
@@ -420,20 +451,19 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     const Segment sg = load_segment(p.seq_info, s);
     unsigned fault = segment_fault(sg, p.total_rows, p.max_seqs, p.mbps, p.ring_rows, p.window);
     if (!fault && sg.ql > p.max_q_len) fault = PKV_ERR_QLEN;
-    if (fault) {
+    const int rows_unit = fault ? 0 : sg.ql * p.G;
+    const int row0 = rt * R;
+    if (fault || row0 >= rows_unit) {  // uniform across the cluster: same segment and row tile
         pdl_wait();
         pdl_trigger();
-        if (split == 0 && rt == 0) {
+        if (fault && rank == 0 && rt == 0) {
             if (tid == 0) atomicOr(p.err, fault);
             zero_segment_rows(p, sg, g, NT);
         }
-        return;
-    }
-    const int rows_unit = sg.ql * p.G;
-    const int row0 = rt * R;
-    if (row0 >= rows_unit) {
-        pdl_wait();
-        pdl_trigger();
+        if (first_cta) {
+            __syncthreads();
+            zero_uncovered(p, reinterpret_cast<int *>(body), NT);
+        }
         return;
     }
     const int rows_here = min(R, rows_unit - row0);
@@ -444,87 +474,87 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     const long long pb_begin = lo_u / kPage;
     const long long pb_end = (kend + kPage - 1) / kPage;
     const long long nblk = pb_end - pb_begin;
-    const long long bps = max((long long)p.min_blocks, (nblk + p.nsplits - 1) / p.nsplits);
+    const long long bps = (nblk + ncta - 1) / ncta;
     const int active = (int)((nblk + bps - 1) / bps);
-    if (split >= active) {
-        pdl_wait();
-        pdl_trigger();
-        return;
-    }
-    const long long cb0 = pb_begin + (long long)split * bps;
-    const int nb = (int)(min(cb0 + bps, pb_end) - cb0);
+    const long long cb0 = pb_begin + (long long)rank * bps;
+    const int nb = rank < active ? (int)(min(cb0 + bps, pb_end) - cb0) : 0;
     const int n_mine = nb > kw ? (nb - kw + KW - 1) / KW : 0;
-    const int unit = (s * p.Hkv + g) * p.row_tiles + rt;
 
-    const T *kpool = reinterpret_cast<const T *>(p.k_pool);
-    const T *vpool = reinterpret_cast<const T *>(p.v_pool);
     const T *knew = reinterpret_cast<const T *>(p.k_new);
     const T *vnew = reinterpret_cast<const T *>(p.v_new);
     const bool fused = knew != nullptr;
     const int dchunks = p.D / EPC;  // real 16-byte chunks per row
-    const int* bt_row = p.block_table + (long long)sg.col * p.mbps;
+    const int *bt_row = p.block_table + (long long)sg.col * p.mbps;
+    uint64_t *gbars = bars + kw * NST;
+    unsigned char *gstage = body + (size_t)kw * NST * C::kStageBytes;
 
-    // Page ids of this group's pages, 32 at a time: lane l holds the id of
-    // the group's page (window + l).
-    int id_reg = -1;
-    int id_window = -1;
+    if (gtid == 0) {
+        for (int i = 0; i < NST; ++i) mbar_init(gbars + i, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // Page ids of this group's pages, 32 at a time, held by the group's first
+    // warp: lane l holds the id of the group's page (window + l).
+    int id_reg = -1, id_window = -1;
+    bool bad = false, timed_out = false;
     auto load_ids = [&](int j) {
         id_window = j & ~31;
         const int li = kw + (id_window + lane) * KW;
         id_reg = -1;
         if (li < nb) id_reg = bt_row[table_page(cb0 + li, p.ring_rows)];
     };
-    bool bad = false;
-
+    // Issue the TMA copies of the group's j-th page (called by the group's first warp).
     auto issue = [&](int j) {
         if ((j & ~31) != id_window) load_ids(j);
         const int bid = __shfl_sync(0xffffffffu, id_reg, j & 31);
-        const int li = kw + j * KW;
-        if (li >= nb) return;
-        const bool bid_ok = bid >= 0 && (long long)bid < p.num_blocks;
-        bad |= !bid_ok;
-        const long long pos_base = (cb0 + li) * kPage;
-        T *st = sPipe + ((size_t)kw * NST + (j % NST)) * C::kStage;
-        constexpr int kPer = 2 * kPage * C::kChunks;
-#pragma unroll 4
-        for (int c = gtid; c < kPer; c += GT) {
-            const int kv = c / (kPage * C::kChunks);
-            const int rem = c - kv * (kPage * C::kChunks);
-            const int o = rem / C::kChunks;
-            const int ch = rem - o * C::kChunks;
-            const long long pos = pos_base + o;
-            bool ok = bid_ok && pos >= lo_u && pos < kend && ch < dchunks;
-            const T *src = kpool;
+        const bool ok = bid >= 0 && (long long)bid < p.num_blocks;
+        bad |= !ok;
+        if (lane == 0) {
+            uint64_t *bar = gbars + (j % NST);
+            unsigned char *st = gstage + (size_t)(j % NST) * C::kStageBytes;
             if (ok) {
-                if (fused && pos >= new_start) {
-                    const T *base = kv ? vnew : knew;
-                    src = base + (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D + ch * EPC;
-                } else {
-                    const T *base = kv ? vpool : kpool;
-                    src = base + (((long long)bid * kPage + o) * p.Hkv + g) * p.D + ch * EPC;
+                fence_proxy_async();
+                mbar_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+                for (int b = 0; b < C::kBoxes; ++b) {
+                    tma_load_4d(st + b * 2048, &p.tmap_k, bar, b * C::kBoxEl, g, 0, bid);
+                    tma_load_4d(st + C::kTileBytes + b * 2048, &p.tmap_v, bar, b * C::kBoxEl, g, 0, bid);
                 }
+            } else {
+                mbar_arrive(bar);  // nothing to fetch: complete the phase, the result is discarded
             }
-            cp_async16(st + kv * C::kTile + o * LD + ch * EPC, src, ok);
         }
     };
     // Pages wholly below new_start hold keys written before this step, so they
     // may be fetched before the dependency wait.
     auto early_ok = [&](int j) { return (cb0 + kw + (long long)j * KW + 1) * kPage <= new_start; };
+    // Bounded wait for the j-th page of the group; warp-uniform result.
+    auto wait_page = [&](int j) {
+        if (timed_out) return;
+        bool done = false;
+        if (lane == 0) {
+            for (int it = 0; it < kWaitProbes && !done; ++it) done = mbar_try_wait(gbars + (j % NST), (j / NST) & 1);
+        }
+        done = __shfl_sync(0xffffffffu, done, 0);
+        if (!done) timed_out = true;
+    };
 
     // ---- prologue: start the first stages before waiting on the previous kernel
     int issued = 0;
-    load_ids(0);
-    for (; issued < NST - 1; ++issued) {
-        if (issued < n_mine && !early_ok(issued)) break;
-        issue(issued);
-        cp_async_commit();
+    if (mt == 0) {
+        load_ids(0);
+        for (; issued < NST && issued < n_mine; ++issued) {
+            if (!early_ok(issued)) break;
+            issue(issued);
+        }
     }
     pdl_wait();
     pdl_trigger();
 
     // Query rows of this tile and their key bounds.
     if constexpr (C::MMA) {
-        T *sQ = reinterpret_cast<T *>(smem);
+        T *sQ = reinterpret_cast<T *>(qarea);
         for (int c = tid; c < R * C::kChunks; c += NT) {
             const int r = c / C::kChunks, ch = c - r * C::kChunks;
             const int ur = row0 + r;
@@ -535,10 +565,10 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
                                (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D + ch * EPC;
                 v = *reinterpret_cast<const uint4 *>(src);
             }
-            *reinterpret_cast<uint4 *>(sQ + r * LD + ch * EPC) = v;
+            *reinterpret_cast<uint4 *>(sQ + r * C::kQLd + ch * EPC) = v;
         }
     } else {
-        float *sQf = reinterpret_cast<float *>(smem);
+        float *sQf = reinterpret_cast<float *>(qarea);
         for (int c = tid; c < R * C::kChunks; c += NT) {
             const int r = c / C::kChunks, ch = c - r * C::kChunks;
             const int ur = row0 + r;
@@ -552,7 +582,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
                 load_f32<T, EPC>(f, src);
             }
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) sQf[r * C::kQLdF + ch * EPC + e] = f[e];
+            for (int e = 0; e < EPC; ++e) sQf[r * C::kQLd + ch * EPC + e] = f[e];
         }
     }
     for (int r = tid; r < R; r += NT) {
@@ -567,9 +597,8 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         sLo[r] = lo;
         sHi[r] = hi;
     }
-    for (; issued < NST - 1; ++issued) {
-        issue(issued);
-        cp_async_commit();
+    if (mt == 0) {
+        for (; issued < NST && issued < n_mine; ++issued) issue(issued);
     }
     __syncthreads();
 
@@ -577,31 +606,63 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     const int nrw = max(0, min(16, rows_here - mt * 16));
     MmaWarp<C> mw;
     SimtWarp<C> sw;
-    if constexpr (C::MMA) mw.init(reinterpret_cast<const T *>(smem), mt, lane);
+    if constexpr (C::MMA) mw.init(reinterpret_cast<const T *>(qarea), mt, lane);
     else sw.init();
     float *sPw = sSimt + warp * (16 * 16 + 16);
+    auto group_sync = [&]() {
+        if constexpr (MT == 1) __syncwarp(); else named_barrier(1 + kw, GT);
+    };
 
     for (int j = 0; j < n_mine; ++j) {
-        cp_async_wait<NST - 2>();
-        if constexpr (MT == 1) __syncwarp(); else named_barrier(1 + kw, GT);
-        issue(j + NST - 1);
-        cp_async_commit();
-        const T *st = sPipe + ((size_t)kw * NST + (j % NST)) * C::kStage;
+        wait_page(j);
+        unsigned char *st = gstage + (size_t)(j % NST) * C::kStageBytes;
         const long long pos0 = (cb0 + kw + (long long)j * KW) * kPage;
+        // Rows outside [lo_u, kend) may hold anything (NaN included): zero them.
+        // This step's own rows come from k_new / v_new in the fused call.
+        if (pos0 < lo_u || pos0 + kPage > kend || (fused && pos0 + kPage > new_start)) {
+            for (int c = gtid; c < 2 * kPage * C::kChunks; c += GT) {
+                const int kv = c / (kPage * C::kChunks);
+                const int rem = c - kv * (kPage * C::kChunks);
+                const int o = rem / C::kChunks, ch = rem - o * C::kChunks;
+                const long long pos = pos0 + o;
+                uint4 *dst = reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch));
+                if (pos < lo_u || pos >= kend) {
+                    *dst = make_uint4(0u, 0u, 0u, 0u);
+                } else if (fused && pos >= new_start) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (ch < dchunks)
+                        v = *reinterpret_cast<const uint4 *>(
+                            (kv ? vnew : knew) + (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D +
+                            ch * EPC);
+                    *dst = v;
+                }
+            }
+            fence_proxy_async();
+            group_sync();
+        }
         if (nrw > 0) {
             if constexpr (C::MMA)
-                mw.consume(reinterpret_cast<const T *>(smem), st, st + C::kTile, pos0, sLo, sHi, mt, lane,
+                mw.consume(reinterpret_cast<const T *>(qarea), st, st + C::kTileBytes, pos0, sLo, sHi, mt, lane,
                            p.scale_log2);
             else
-                sw.consume(reinterpret_cast<const float *>(smem), st, st + C::kTile, pos0, sLo, sHi, mt,
+                sw.consume(reinterpret_cast<const float *>(qarea), st, st + C::kTileBytes, pos0, sLo, sHi, mt,
                            lane, nrw, p.scale_log2, sPw);
         }
+        group_sync();  // every warp of the group is done with this stage
+        if (mt == 0 && j + NST < n_mine) issue(j + NST);
     }
-    cp_async_wait<0>();
+    if (timed_out && lane == 0 && mt == 0) {
+        // Give the copies still in flight a bounded chance to land before the
+        // stage memory is reused.
+        for (int j = max(0, n_mine - NST); j < n_mine; ++j)
+            for (int it = 0; it < kWaitProbes && !mbar_try_wait(gbars + (j % NST), (j / NST) & 1); ++it) {
+            }
+    }
     const bool any_bad = __syncthreads_or(bad);
+    const bool any_timeout = __syncthreads_or(timed_out);
 
     // ---- fused append: the CTA whose pages hold this step's positions writes them
-    if (fused && rt == 0) {
+    if (fused && rt == 0 && nb > 0) {
         const long long lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
         if (new_start < hi_pos && kend > lo_pos) {
             bool ok = true;
@@ -631,16 +692,18 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         }
     }
 
-    // ---- merge the key groups of each row tile
+    // ---- merge the key groups of this CTA (stage memory is free again)
     if (nrw > 0 || !C::MMA) {
         if constexpr (C::MMA) mw.store(sMo, sMm, sMl, kw, mt, lane);
         else sw.store(sMo, sMm, sMl, kw, mt, lane, nrw);
     }
+    const bool poisoned = any_bad || any_timeout;
+    if (tid == 0) {
+        sFlag[0] = poisoned;
+        if (any_bad) atomicOr(p.err, PKV_ERR_BLOCK);
+        if (any_timeout) atomicOr(p.err, PKV_ERR_TIMEOUT);
+    }
     __syncthreads();
-    if (any_bad && tid == 0) atomicOr(p.err, PKV_ERR_BLOCK);
-
-    constexpr float kLn2 = 0.6931471805599453f;
-    const long long part = ((long long)unit * p.nsplits + split) * R;
     for (int idx = tid; idx < rows_here * DP; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
         float M = -CUDART_INF_F;
@@ -655,51 +718,71 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
                 o = fmaf(w, sMo[((size_t)k * R + r) * DP + d], o);
             }
         }
-        o = L > 0.f ? o / L : 0.f;
-        const float lse2 = L > 0.f ? M + log2f(L) : -CUDART_INF_F;
-        if (active == 1) {
-            const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
-            const long long orow = ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
-            if (d < p.D) p.out[orow * p.D + d] = any_bad ? 0.f : o;
-            if (d == 0 && p.lse) p.lse[orow] = any_bad ? -CUDART_INF_F : lse2 * kLn2;
-        } else {
-            __stcg(p.ws_o + (part + r) * DP + d, o);
-            if (d == 0) __stcg(p.ws_lse + part + r, any_bad ? CUDART_INF_F : lse2);
+        sMo[(size_t)r * DP + d] = o;  // element owned by this thread alone: merged in place
+        if (d == 0) {
+            sPm[r] = M;
+            sPl[r] = L;
         }
     }
-    if (active == 1) return;
+    __syncthreads();
 
-    // ---- ticket: the last split of this (segment, kv head, row tile) merges
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) sLast = atomicAdd(p.ws_ticket + unit, 1u) == (unsigned)(active - 1);
-    __syncthreads();
-    if (!sLast) return;
-    __threadfence();
-    const long long part0 = (long long)unit * p.nsplits * R;
-    for (int idx = tid; idx < rows_here * DP; idx += NT) {
-        const int r = idx / DP, d = idx - r * DP;
-        float M = -CUDART_INF_F;
-        bool poison = false;
-        for (int k = 0; k < active; ++k) {
-            const float l2 = __ldcg(p.ws_lse + part0 + (long long)k * R + r);
-            poison |= l2 == CUDART_INF_F;
-            M = fmaxf(M, l2);
-        }
-        float W = 0.f, o = 0.f;
-        if (!poison && M != -CUDART_INF_F) {
-            for (int k = 0; k < active; ++k) {
-                const float w = exp2f(__ldcg(p.ws_lse + part0 + (long long)k * R + r) - M);
-                W += w;
-                o = fmaf(w, __ldcg(p.ws_o + (part0 + (long long)k * R + r) * DP + d), o);
-            }
-        }
+    constexpr float kLn2 = 0.6931471805599453f;
+    auto out_row = [&](int r) {
         const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
-        const long long orow = ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
-        if (d < p.D) p.out[orow * p.D + d] = W > 0.f ? o / W : 0.f;
-        if (d == 0 && p.lse) p.lse[orow] = W > 0.f ? (M + log2f(W)) * kLn2 : -CUDART_INF_F;
+        return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
+    };
+    if (ncta == 1) {
+        for (int idx = tid; idx < rows_here * DP; idx += NT) {
+            const int r = idx / DP, d = idx - r * DP;
+            const float L = sPl[r];
+            const bool zero = poisoned || L <= 0.f;
+            const long long orow = out_row(r);
+            if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : sMo[(size_t)r * DP + d] / L;
+            if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (sPm[r] + log2f(L)) * kLn2;
+        }
+    } else {
+        // ---- merge the cluster's partials through distributed shared memory
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (tid < rows_here) {
+            const int r = tid;
+            float M = -CUDART_INF_F;
+            bool poison = false;
+            for (int c = 0; c < ncta; ++c) {
+                M = fmaxf(M, *cluster.map_shared_rank(sPm + r, c));
+                poison |= *cluster.map_shared_rank(sFlag, c) != 0;
+            }
+            float W = 0.f;
+            for (int c = 0; c < ncta; ++c) {
+                const float w = (M == -CUDART_INF_F) ? 0.f : exp2f(*cluster.map_shared_rank(sPm + r, c) - M);
+                sWt[r * 16 + c] = w;
+                W = fmaf(w, *cluster.map_shared_rank(sPl + r, c), W);
+            }
+            const bool zero = poison || W <= 0.f;
+            for (int c = 0; c < ncta; ++c) sWt[r * 16 + c] = zero ? 0.f : sWt[r * 16 + c] / W;
+            sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+        }
+        __syncthreads();
+        const int E = rows_here * DP;
+        const int per = (E + ncta - 1) / ncta;
+        const int e0 = rank * per, e1 = min(E, e0 + per);
+        for (int idx = e0 + tid; idx < e1; idx += NT) {
+            const int r = idx / DP, d = idx - r * DP;
+            float o = 0.f;
+            for (int c = 0; c < ncta; ++c) {
+                const float w = sWt[r * 16 + c];
+                if (w != 0.f) o = fmaf(w, *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c), o);
+            }
+            const long long orow = out_row(r);
+            if (d < p.D) p.out[orow * p.D + d] = o;
+            if (d == 0 && p.lse) p.lse[orow] = sLse[r];
+        }
+        cluster.sync();  // partials stay readable until every CTA has merged its slice
     }
-    if (tid == 0) p.ws_ticket[unit] = 0u;
+    if (first_cta) {
+        __syncthreads();
+        zero_uncovered(p, reinterpret_cast<int *>(body), NT);
+    }
 }
 
 }  // namespace pkv

@@ -1,6 +1,7 @@
 // Device helpers shared by the pkv kernels (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -23,19 +24,58 @@ template <> struct Elem<float> {
     __device__ static float to_f32(float x) { return x; }
 };
 
-// ---------------------------------------------------------------- async copies
+// ---------------------------------------------------------------- shared memory, mbarriers, TMA
 
-// 16-byte global -> shared copy that bypasses L1.  When `pred` is false the
-// destination is zero-filled and nothing is read (src-size 0).
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool pred) {
-    unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    int n = pred ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
+__device__ __forceinline__ unsigned smem_u32(const void *p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Make barrier initialisation visible to the async proxy (TMA completion).
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// One bounded-time probe of a barrier phase (the hardware may suspend the
+// thread for a short while before returning false).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+// 4-D tiled TMA load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1, int c2,
+                                            int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` inside a page tile
+// loaded with 128-byte swizzling: the tile is a run of 2 KB boxes (16 rows x
+// 128 B), and inside each 1 KB half the chunk index is XOR-ed with row % 8.
+__device__ __forceinline__ unsigned swz(int row, int chunk) {
+    return (unsigned)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
 
 // ---------------------------------------------------------------- programmatic dependent launch
 
@@ -86,28 +126,24 @@ struct Segment {
 
 // Everything one attention launch reads; passed by value as a grid constant.
 struct AttendParams {
+    CUtensorMap tmap_k;     // 4-D view (D, Hkv, 16, num_blocks) of this layer's K pool
+    CUtensorMap tmap_v;
     const void *q;          // [rows][Hq][D]
-    const void *k_pool;     // [num_blocks][16][Hkv][D]
-    const void *v_pool;
     const void *k_new;      // fused append: [rows][Hkv][D], else null
     const void *v_new;
-    void *k_pool_w;         // fused append: writable aliases of the pools
+    void *k_pool_w;         // fused append: the pools, written at this step's slots
     void *v_pool_w;
     const int *block_table; // [max_seqs][mbps]
     const int4 *seq_info;   // [S]
     float *out;             // [rows][Hq][D]
     float *lse;             // [rows][Hq] or null
-    float *ws_o;            // [units][splits][Rmax][D] split partials (normalised)
-    float *ws_lse;          // [units][splits][Rmax] log2-sum-exp of each partial
-    unsigned *ws_ticket;    // [units]
     unsigned *err;
     long long num_blocks;
     int Hq, Hkv, D, G;      // G = Hq / Hkv
     int total_rows, S;
     int max_seqs, mbps, ring_rows;
-    int max_q_len, rows_max; // rows_max = G * max_q_len
+    int max_q_len;
     int row_tiles;          // CTAs along the rows of one (segment, kv head)
-    int nsplits, min_blocks;
     int causal, window;
     float scale_log2;       // softmax_scale * log2(e)
 };

@@ -18,7 +18,7 @@ from typing import Dict, Optional, Tuple
 import torch
 
 from . import _lib
-from .api import PagedKVCache, append, append_attend, attend_varlen, new_err_flags, new_workspace
+from .api import PagedKVCache, append, append_attend, attend_varlen, new_err_flags
 
 _SHARED_POOL = None
 
@@ -54,8 +54,6 @@ class DecodeStep:
             if with_lse else [None] * L
         self.seq_info = torch.zeros(num_segments, 4, dtype=torch.int32, device=dev)
         self.err = new_err_flags(dev)
-        self.workspace = new_workspace(cache, num_q_heads, num_segments, max_q_len, self.max_kv, num_splits,
-                                       device=dev)
 
     def launch_count(self) -> int:
         return self.cache.num_layers * (1 if self.fused else 2)
@@ -69,15 +67,15 @@ class DecodeStep:
                 flags |= _lib.FLAG_PDL
             if self.fused:
                 append_attend(c, layer, self.q[layer], self.k_new[layer], self.v_new[layer], self.seq_info,
-                              self.out[layer], self.err, self.workspace, self.max_q_len, self.max_kv,
-                              self.scale, self.causal, self.window, lse=self.lse[layer],
-                              num_splits=self.num_splits, flags=flags, stream=stream)
+                              self.out[layer], self.err, self.max_q_len, self.max_kv, self.scale, self.causal,
+                              self.window, lse=self.lse[layer], num_splits=self.num_splits, flags=flags,
+                              stream=stream)
             else:
                 append(c, layer, self.k_new[layer], self.v_new[layer], self.seq_info, self.err,
                        window=self.window, stream=stream)
-                attend_varlen(c, layer, self.q[layer], self.seq_info, self.out[layer], self.err, self.workspace,
-                              self.max_q_len, self.max_kv, self.scale, self.causal, self.window,
-                              lse=self.lse[layer], num_splits=self.num_splits, flags=flags, stream=stream)
+                attend_varlen(c, layer, self.q[layer], self.seq_info, self.out[layer], self.err, self.max_q_len,
+                              self.max_kv, self.scale, self.causal, self.window, lse=self.lse[layer],
+                              num_splits=self.num_splits, flags=flags, stream=stream)
 
 
 class DecodeGraphRunner:
@@ -107,8 +105,6 @@ class DecodeGraphRunner:
         st = self.step_bufs
         st.cache = cache
         st.max_kv = cache.bucket
-        st.workspace = new_workspace(cache, st.num_q_heads, int(st.seq_info.shape[0]), st.max_q_len, st.max_kv,
-                                     st.num_splits, device=st.seq_info.device)
         self._graphs = {k: g for k, g in self._graphs.items() if k == (cache.bucket, cache.generation)}
 
     def graph_for(self) -> torch.cuda.CUDAGraph:

@@ -59,7 +59,7 @@ def test_bucket_for_matches_golden(lib):
 
 
 def test_status_strings(lib):
-    for s in (0, 1, 2, -1, -2, -3, -4, -5, -6):
+    for s in (0, 1, 2, -1, -2, -3, -4, -5):
         assert lib.lib.pkv_status_str(s)
     assert b"unknown" in lib.lib.pkv_status_str(99)
 
@@ -88,7 +88,7 @@ def test_bad_cache_rejected_before_launch(lib, field, value, status):
     d, keep = _desc(lib, **{field: value})
     L = lib.lib
     st = L.pkv_attend_varlen(ctypes.byref(d), 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 0.125, 0, 0,
-                             0x6000, None, None, 0, 0x7000, 0, None)
+                             0x6000, None, 0x7000, 0, None)
     assert st == status
     st = L.pkv_append(ctypes.byref(d), 0, 0x4000, 0x4000, 1, 0x5000, 1, 0, 0x7000, None)
     assert st == status
@@ -98,42 +98,32 @@ def test_bad_call_arguments_rejected(lib):
     d, keep = _desc(lib)
     L = lib.lib
     ref = ctypes.byref(d)
-    # q heads not a multiple of kv heads
-    assert L.pkv_attend_varlen(ref, 0, 0x4000, 3, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
-                               0x7000, 0, None) == -1
-    # layer out of range
-    assert L.pkv_attend_varlen(ref, 1, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
-                               0x7000, 0, None) == -1
-    # misaligned q
-    assert L.pkv_attend_varlen(ref, 0, 0x4004, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
-                               0x7000, 0, None) == -1
-    # missing error word
-    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000, None, None, 0,
-                               None, 0, None) == -1
-    # causal must be 0 or 1, window >= 0
-    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 2, 0, 0x6000, None, None, 0,
-                               0x7000, 0, None) == -1
-    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, -1, 0x6000, None, None, 0,
-                               0x7000, 0, None) == -1
-    # split-K without a workspace
-    assert L.pkv_attend_varlen(ref, 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 4, 1.0, 0, 0, 0x6000, None, None, 0,
-                               0x7000, 0, None) == -6
+
+    def attend(**kw):
+        a = dict(layer=0, q=0x4000, hq=8, rows=1, si=0x5000, S=1, mq=1, mk=512, ns=0, scale=1.0, causal=0,
+                 window=0, out=0x6000, lse=None, err=0x7000, flags=0)
+        a.update(kw)
+        return L.pkv_attend_varlen(ref, a["layer"], a["q"], a["hq"], a["rows"], a["si"], a["S"], a["mq"], a["mk"],
+                                   a["ns"], a["scale"], a["causal"], a["window"], a["out"], a["lse"], a["err"],
+                                   a["flags"], None)
+
+    assert attend(hq=3) == -1              # q heads not a multiple of kv heads
+    assert attend(layer=1) == -1           # layer out of range
+    assert attend(q=0x4004) == -1          # misaligned q
+    assert attend(si=0x5004) == -1         # misaligned segment table
+    assert attend(err=None) == -1          # missing error word
+    assert attend(causal=2) == -1
+    assert attend(window=-1) == -1
+    assert attend(ns=17) == -1             # more splits than a cluster can hold
+    assert attend(ns=-1) == -1
+    assert attend(mq=0) == -1
+    assert attend(mk=0) == -1
+    assert attend(S=-1) == -1
     # fused call without k_new / v_new
     assert L.pkv_append_attend(ref, 0, 0x4000, None, None, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000,
-                               None, None, 0, 0x7000, 0, None) == -1
-
-
-def test_workspace_sizes(lib):
-    d, keep = _desc(lib)
-    L = lib.lib
-    ref = ctypes.byref(d)
-    assert L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 1) == 0          # one split: no workspace
-    w4 = L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 4)
-    w8 = L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 8)
-    assert 0 < w4 < w8
-    # 2 kv heads x 1 segment x 8 splits x 16 rows x (64 + 1) floats, plus tickets
-    assert w8 >= 2 * 8 * 16 * 65 * 4
-    assert L.pkv_attend_workspace_bytes(ref, 3, 1, 1, 512, 4) == 0          # invalid -> 0
+                               None, 0x7000, 0, None) == -1
+    # nothing to do: no rows and no segments
+    assert attend(rows=0, S=0) == 0
 
 
 def test_resize_and_prefix_host_rules(lib):

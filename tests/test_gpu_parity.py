@@ -38,13 +38,12 @@ def run(pkv, w, layer=0, fused=True, flags=0, num_splits=0, max_q_len=None, max_
     obuf, out = U.guarded_out(w.total_rows, w.q_heads, w.head_dim)
     lse = torch.full((max(w.total_rows, 1), w.q_heads), 3.0, device=dev)[:w.total_rows]
     err = pkv.new_err_flags()
-    ws = pkv.new_workspace(cache, w.q_heads, w.num_segments, mq, mk, num_splits)
     if fused:
-        pkv.append_attend(cache, layer, q, kn, vn, si, out, err, ws, mq, mk, w.scale, w.causal, w.window, lse=lse,
+        pkv.append_attend(cache, layer, q, kn, vn, si, out, err, mq, mk, w.scale, w.causal, w.window, lse=lse,
                           num_splits=num_splits, flags=flags)
     else:
         pkv.append(cache, layer, kn, vn, si, err, window=w.window)
-        pkv.attend_varlen(cache, layer, q, si, out, err, ws, mq, mk, w.scale, w.causal, w.window, lse=lse,
+        pkv.attend_varlen(cache, layer, q, si, out, err, mq, mk, w.scale, w.causal, w.window, lse=lse,
                           num_splits=num_splits, flags=flags)
     torch.cuda.synchronize()
     U.check_guarded(obuf)
