@@ -55,10 +55,13 @@ struct AttnCfg {
     static constexpr size_t kBodyBytes =
         ((kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes) + 1023) & ~size_t(1023);
     static constexpr size_t kQBytes = MMA ? (size_t)kRows * kQLd * 2 : (size_t)kRows * kQLd * 4;
-    static constexpr size_t kRowBytes = (size_t)kRows * (2 + 2 + 16 + 1) * 4;  // pm, pl, lo, hi, weights, lse
+    // per row: pm, pl, lo, hi, lse, and the cluster merge's gathered maxima / sums (16 CTAs each)
+    static constexpr size_t kRowBytes = (size_t)kRows * (2 + 2 + 1 + 16 + 16) * 4;
     static constexpr size_t kBarBytes = (size_t)KW * NST * 8;
     static constexpr size_t kSimtBytes = MMA ? 0 : (size_t)kWarps * (16 * 16 + 16) * 4;
-    static constexpr size_t kSmemBytes = 1024 + kBodyBytes + kQBytes + kRowBytes + kBarBytes + kSimtBytes + 16;
+    static constexpr size_t kFlagBytes = 32 * 4;  // this CTA's poison flag, then the cluster's flags
+    static constexpr size_t kSmemBytes =
+        1024 + kBodyBytes + kQBytes + kRowBytes + kBarBytes + kSimtBytes + kFlagBytes + 16;
     static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
     static_assert(kQBytes % 16 == 0, "smem sections stay 16-byte aligned");
     static_assert(!MMA || sizeof(T) == 2, "tensor-core path is bf16");
@@ -426,11 +429,13 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     float *sPl = sPm + R;                                   // [R] and sum
     int *sLo = reinterpret_cast<int *>(sPl + R);            // [R] key bounds per row
     int *sHi = sLo + R;
-    float *sWt = reinterpret_cast<float *>(sHi + R);        // [R][16] cluster merge weights
-    float *sLse = sWt + R * 16;                             // [R]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sLse + R);  // [KW][NST]
+    float *sLse = reinterpret_cast<float *>(sHi + R);       // [R] merged log-sum-exp
+    float *sAllM = sLse + R;                                // [R][16] cluster maxima, then merge weights
+    float *sAllL = sAllM + R * 16;                          // [R][16] cluster sums
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sAllL + R * 16);  // [KW][NST]
     float *sSimt = reinterpret_cast<float *>(bars + KW * NST);
-    int *sFlag = reinterpret_cast<int *>(sSimt + (C::kSimtBytes / 4));
+    int *sFlag = reinterpret_cast<int *>(sSimt + (C::kSimtBytes / 4));  // [1] own flag
+    int *sAllF = sFlag + 1;                                 // [16] gathered flags of the cluster
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = warp % MT, kw = warp / MT;
@@ -741,25 +746,35 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (sPm[r] + log2f(L)) * kLn2;
         }
     } else {
-        // ---- merge the cluster's partials through distributed shared memory
+        // ---- merge the cluster's partials through distributed shared memory.
+        // Every remote value a phase needs is fetched by an independent load,
+        // so each phase costs about one distributed-shared-memory round trip.
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
+        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
+            const int r = idx / ncta, c = idx - r * ncta;
+            sAllM[r * 16 + c] = *cluster.map_shared_rank(sPm + r, c);
+            sAllL[r * 16 + c] = *cluster.map_shared_rank(sPl + r, c);
+        }
+        if (tid < ncta) sAllF[tid] = *cluster.map_shared_rank(sFlag, tid);
+        __syncthreads();
         if (tid < rows_here) {
             const int r = tid;
             float M = -CUDART_INF_F;
             bool poison = false;
             for (int c = 0; c < ncta; ++c) {
-                M = fmaxf(M, *cluster.map_shared_rank(sPm + r, c));
-                poison |= *cluster.map_shared_rank(sFlag, c) != 0;
+                M = fmaxf(M, sAllM[r * 16 + c]);
+                poison |= sAllF[c] != 0;
             }
             float W = 0.f;
             for (int c = 0; c < ncta; ++c) {
-                const float w = (M == -CUDART_INF_F) ? 0.f : exp2f(*cluster.map_shared_rank(sPm + r, c) - M);
-                sWt[r * 16 + c] = w;
-                W = fmaf(w, *cluster.map_shared_rank(sPl + r, c), W);
+                const float w = (M == -CUDART_INF_F) ? 0.f : exp2f(sAllM[r * 16 + c] - M);
+                sAllM[r * 16 + c] = w;
+                W = fmaf(w, sAllL[r * 16 + c], W);
             }
             const bool zero = poison || W <= 0.f;
-            for (int c = 0; c < ncta; ++c) sWt[r * 16 + c] = zero ? 0.f : sWt[r * 16 + c] / W;
+            const float inv = zero ? 0.f : 1.f / W;
+            for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] *= inv;
             sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
         }
         __syncthreads();
@@ -768,11 +783,12 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         const int e0 = rank * per, e1 = min(E, e0 + per);
         for (int idx = e0 + tid; idx < e1; idx += NT) {
             const int r = idx / DP, d = idx - r * DP;
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
             float o = 0.f;
-            for (int c = 0; c < ncta; ++c) {
-                const float w = sWt[r * 16 + c];
-                if (w != 0.f) o = fmaf(w, *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c), o);
-            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o = fmaf(sAllM[r * 16 + c] * (c < ncta ? 1.f : 0.f), v[c], o);
             const long long orow = out_row(r);
             if (d < p.D) p.out[orow * p.D + d] = o;
             if (d == 0 && p.lse) p.lse[orow] = sLse[r];
