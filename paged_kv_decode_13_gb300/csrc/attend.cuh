@@ -774,7 +774,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             }
             const bool zero = poison || W <= 0.f;
             const float inv = zero ? 0.f : 1.f / W;
-            for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] *= inv;
+            for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] = zero ? 0.f : sAllM[r * 16 + c] * inv;
             sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
         }
         __syncthreads();
@@ -788,7 +788,11 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             for (int c = 0; c < 16; ++c) v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
             float o = 0.f;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) o = fmaf(sAllM[r * 16 + c] * (c < ncta ? 1.f : 0.f), v[c], o);
+            for (int c = 0; c < 16; ++c) {
+                // A zero weight must not touch its partial: a poisoned one may hold NaN.
+                const float w = c < ncta ? sAllM[r * 16 + c] : 0.f;
+                o += w != 0.f ? w * v[c] : 0.f;
+            }
             const long long orow = out_row(r);
             if (d < p.D) p.out[orow * p.D + d] = o;
             if (d == 0 && p.lse) p.lse[orow] = sLse[r];
