@@ -59,13 +59,18 @@ struct AttnCfg {
     static constexpr size_t kRowBytes = (size_t)kRows * (2 + 2 + 1 + 16 + 16) * 4;
     static constexpr size_t kBarBytes = (size_t)KW * NST * 8;
     static constexpr size_t kSimtBytes = MMA ? 0 : (size_t)kWarps * (16 * 16 + 16) * 4;
-    static constexpr size_t kFlagBytes = 32 * 4;  // this CTA's poison flag, then the cluster's flags
-    static constexpr size_t kSmemBytes =
-        1024 + kBodyBytes + kQBytes + kRowBytes + kBarBytes + kSimtBytes + kFlagBytes + 16;
+    static constexpr size_t kFlagBytes = 32 * 4;  // this CTA's poison flags, then the cluster's
+    static constexpr size_t kCovBytes = (size_t)kThreads * 4;  // coverage flags of the first rows
+    static constexpr size_t kBaseBytes =
+        1024 + kBodyBytes + kQBytes + kRowBytes + kBarBytes + kSimtBytes + kFlagBytes + kCovBytes + 16;
+    // Partial outputs pushed by the other CTAs of the cluster (one slice each);
+    // without room for it the merge pulls them instead.
+    static constexpr size_t kRecvNeed = ((size_t)kRows * DP + 16) * 4;
+    static constexpr bool kPush = kBaseBytes + kRecvNeed <= 232448;
+    static constexpr size_t kSmemBytes = kBaseBytes + (kPush ? kRecvNeed : 0);
     static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
     static_assert(kQBytes % 16 == 0, "smem sections stay 16-byte aligned");
     static_assert(!MMA || sizeof(T) == 2, "tensor-core path is bf16");
-    static_assert(kBodyBytes >= (size_t)kThreads * 4, "coverage pass keeps one int per thread in the body");
     static_assert(kRows <= kThreads, "one thread per row in the cluster merge");
 };
 
@@ -367,9 +372,9 @@ struct SimtWarp {
 // One CTA zeroes every output row that no segment covers and flags rows that
 // two segments claim.  Segments with a negative q_start or non-positive q_len
 // cover nothing.
-static __device__ void zero_uncovered(const AttendParams &p, int *sFlags, int nthreads) {
+static __device__ void zero_uncovered(const AttendParams &p, int *sFlags, int nthreads, int first_row) {
     const int tid = threadIdx.x;
-    for (int base = 0; base < p.total_rows; base += nthreads) {
+    for (int base = first_row; base < p.total_rows; base += nthreads) {
         const int t = base + tid;
         int cnt = 0;
         if (t < p.total_rows) {
@@ -434,8 +439,10 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     float *sAllL = sAllM + R * 16;                          // [R][16] cluster sums
     uint64_t *bars = reinterpret_cast<uint64_t *>(sAllL + R * 16);  // [KW][NST]
     float *sSimt = reinterpret_cast<float *>(bars + KW * NST);
-    int *sFlag = reinterpret_cast<int *>(sSimt + (C::kSimtBytes / 4));  // [1] own flag
-    int *sAllF = sFlag + 1;                                 // [16] gathered flags of the cluster
+    int *sFlag = reinterpret_cast<int *>(sSimt + (C::kSimtBytes / 4));  // [1] own flags: 1 bad page, 2 timeout
+    int *sAllF = sFlag + 1;                                 // [16] flags of the cluster
+    int *sCov = sFlag + 32;                                 // [NT] coverage flags of the first rows
+    float *sRecv = reinterpret_cast<float *>(sCov + NT);    // pushed partial outputs (kPush)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = warp % MT, kw = warp / MT;
@@ -445,10 +452,45 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     const int s = blockIdx.z;
     const bool first_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
 
+    // Rows no segment covers: the first CTA scans the first NT rows before the
+    // dependency wait (the segment table is not written by the previous
+    // kernel) and zeroes them after it.
+    int cov_any = 0;
+    if (first_cta) {
+        int f = 0;
+        if (tid < p.total_rows) {
+            int cnt = 0;
+            for (int s2 = 0; s2 < p.S; ++s2) {
+                const Segment o = load_segment(p.seq_info, s2);
+                if (o.q0 >= 0 && o.ql > 0 && tid >= o.q0 && (long long)tid < (long long)o.q0 + o.ql) ++cnt;
+            }
+            f = (cnt == 0 ? 1 : 0) | (cnt > 1 ? 2 : 0);
+        }
+        sCov[tid] = f;
+        cov_any = __syncthreads_or(f != 0);
+    }
+    auto apply_coverage = [&]() {  // first CTA, after the dependency wait
+        if (cov_any) {
+            const int n = min(NT, p.total_rows), per_row = p.Hq * p.D;
+            for (int r = 0; r < n; ++r) {
+                const int f = sCov[r];
+                if ((f & 2) && tid == 0) atomicOr(p.err, PKV_ERR_OVERLAP);
+                if (!(f & 1)) continue;
+                for (int e = tid; e < per_row; e += NT) p.out[(long long)r * per_row + e] = 0.f;
+                if (p.lse)
+                    for (int e = tid; e < p.Hq; e += NT) p.lse[(long long)r * p.Hq + e] = -CUDART_INF_F;
+            }
+        }
+        if (p.total_rows > NT) {
+            __syncthreads();
+            zero_uncovered(p, sCov, NT, NT);
+        }
+    };
+
     if (p.S == 0) {  // nothing but rows no segment covers
         pdl_wait();
         pdl_trigger();
-        if (first_cta) zero_uncovered(p, reinterpret_cast<int *>(body), NT);
+        if (first_cta) apply_coverage();
         return;
     }
 
@@ -465,12 +507,11 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             if (tid == 0) atomicOr(p.err, fault);
             zero_segment_rows(p, sg, g, NT);
         }
-        if (first_cta) {
-            __syncthreads();
-            zero_uncovered(p, reinterpret_cast<int *>(body), NT);
-        }
+        if (first_cta) apply_coverage();
         return;
     }
+    if (C::kPush && ncta > 1)  // announce this CTA to the cluster; waited on before any remote store
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
     const int rows_here = min(R, rows_unit - row0);
     const long long kend = sg.kend;
     const long long new_start = kend - sg.ql;  // first position appended this step
@@ -492,12 +533,31 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     const int *bt_row = p.block_table + (long long)sg.col * p.mbps;
     uint64_t *gbars = bars + kw * NST;
     unsigned char *gstage = body + (size_t)kw * NST * C::kStageBytes;
+    const long long lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
+    // This CTA's pages hold some of the step's own positions (fused call).
+    const bool has_new = fused && rt == 0 && nb > 0 && new_start < hi_pos && kend > lo_pos;
 
     if (gtid == 0) {
         for (int i = 0; i < NST; ++i) mbar_init(gbars + i, 1);
         fence_barrier_init();
     }
+    if (tid == 0) sFlag[0] = 0;
     __syncthreads();
+
+    // Fused append: written only if every slot of the segment's new rows maps
+    // to a valid page (checked here, before the dependency wait: the block
+    // table is not written by the previous kernel).
+    bool app_ok = false;
+    if (has_new) {
+        bool ok = true;
+        for (int i = tid; i < sg.ql; i += NT) {
+            const long long pos = new_start + i;
+            const long long rr = p.ring_rows ? pos % p.ring_rows : pos;
+            const int b = bt_row[rr / kPage];
+            ok &= b >= 0 && (long long)b < p.num_blocks;
+        }
+        app_ok = __syncthreads_and(ok);
+    }
 
     // Page ids of this group's pages, 32 at a time, held by the group's first
     // warp: lane l holds the id of the group's page (window + l).
@@ -556,6 +616,18 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     }
     pdl_wait();
     pdl_trigger();
+
+    if (has_new) {  // bring this step's rows towards the SM; the page fix-up reads them
+        const int lines = (p.D * C::kElem + 127) / 128;
+        const long long a = max(new_start, lo_pos), e = min(kend, hi_pos);
+        const int n = (int)(e - a) * 2 * lines;
+        for (int c = tid; c < n; c += NT) {
+            const int row = c / (2 * lines), rem = c - row * 2 * lines, kv = rem / lines, ln = rem - kv * lines;
+            const T *src = (kv ? vnew : knew) + (((long long)sg.q0 + (a + row - new_start)) * p.Hkv + g) * p.D;
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + ln * 128));
+        }
+    }
+    if (first_cta) apply_coverage();
 
     // Query rows of this tile and their key bounds.
     if constexpr (C::MMA) {
@@ -623,8 +695,11 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         unsigned char *st = gstage + (size_t)(j % NST) * C::kStageBytes;
         const long long pos0 = (cb0 + kw + (long long)j * KW) * kPage;
         // Rows outside [lo_u, kend) may hold anything (NaN included): zero them.
-        // This step's own rows come from k_new / v_new in the fused call.
+        // This step's own rows come from k_new / v_new in the fused call, and
+        // the CTA that owns them also writes them into the cache here.
         if (pos0 < lo_u || pos0 + kPage > kend || (fused && pos0 + kPage > new_start)) {
+            const bool to_pool = app_ok && pos0 + kPage > new_start;
+            const long long bpage = to_pool ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
             for (int c = gtid; c < 2 * kPage * C::kChunks; c += GT) {
                 const int kv = c / (kPage * C::kChunks);
                 const int rem = c - kv * (kPage * C::kChunks);
@@ -635,10 +710,16 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
                     *dst = make_uint4(0u, 0u, 0u, 0u);
                 } else if (fused && pos >= new_start) {
                     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (ch < dchunks)
+                    if (ch < dchunks) {
                         v = *reinterpret_cast<const uint4 *>(
                             (kv ? vnew : knew) + (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D +
                             ch * EPC);
+                        if (to_pool) {
+                            const long long slot = bpage * kPage + (p.ring_rows ? pos % p.ring_rows : pos) % kPage;
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
+                                                       (slot * p.Hkv + g) * p.D + ch * EPC) = v;
+                        }
+                    }
                     *dst = v;
                 }
             }
@@ -663,51 +744,16 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             for (int it = 0; it < kWaitProbes && !mbar_try_wait(gbars + (j % NST), (j / NST) & 1); ++it) {
             }
     }
-    const bool any_bad = __syncthreads_or(bad);
-    const bool any_timeout = __syncthreads_or(timed_out);
+    if ((bad || timed_out) && lane == 0) atomicOr(sFlag, (bad ? 1 : 0) | (timed_out ? 2 : 0));
+    __syncthreads();  // stages are free, flags are final
 
-    // ---- fused append: the CTA whose pages hold this step's positions writes them
-    if (fused && rt == 0 && nb > 0) {
-        const long long lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
-        if (new_start < hi_pos && kend > lo_pos) {
-            bool ok = true;
-            for (int i = tid; i < sg.ql; i += NT) {
-                const long long pos = new_start + i;
-                const long long rr = p.ring_rows ? pos % p.ring_rows : pos;
-                const int b = bt_row[rr / kPage];
-                ok &= b >= 0 && (long long)b < p.num_blocks;
-            }
-            if (__syncthreads_and(ok)) {
-                const long long a = max(new_start, lo_pos), e = min(kend, hi_pos);
-                const int per = (int)(e - a) * dchunks;
-                for (int c = tid; c < 2 * per; c += NT) {
-                    const int kv = c / per;
-                    const int rem = c - kv * per;
-                    const long long pos = a + rem / dchunks;
-                    const int ch = rem % dchunks;
-                    const long long rr = p.ring_rows ? pos % p.ring_rows : pos;
-                    const long long b = bt_row[rr / kPage];
-                    const T *src = (kv ? vnew : knew) +
-                                   (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D + ch * EPC;
-                    T *dst = reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
-                             ((b * kPage + rr % kPage) * p.Hkv + g) * p.D + ch * EPC;
-                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
-                }
-            }
-        }
-    }
-
-    // ---- merge the key groups of this CTA (stage memory is free again)
+    // ---- merge the key groups of this CTA
+    const int flags = sFlag[0];
     if (nrw > 0 || !C::MMA) {
         if constexpr (C::MMA) mw.store(sMo, sMm, sMl, kw, mt, lane);
         else sw.store(sMo, sMm, sMl, kw, mt, lane, nrw);
     }
-    const bool poisoned = any_bad || any_timeout;
-    if (tid == 0) {
-        sFlag[0] = poisoned;
-        if (any_bad) atomicOr(p.err, PKV_ERR_BLOCK);
-        if (any_timeout) atomicOr(p.err, PKV_ERR_TIMEOUT);
-    }
+    if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
     __syncthreads();
     for (int idx = tid; idx < rows_here * DP; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
@@ -740,16 +786,36 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         for (int idx = tid; idx < rows_here * DP; idx += NT) {
             const int r = idx / DP, d = idx - r * DP;
             const float L = sPl[r];
-            const bool zero = poisoned || L <= 0.f;
+            const bool zero = flags || L <= 0.f;
             const long long orow = out_row(r);
             if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : sMo[(size_t)r * DP + d] / L;
             if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (sPm[r] + log2f(L)) * kLn2;
         }
+        return;
+    }
+
+    // ---- merge the cluster's partials through distributed shared memory
+    cg::cluster_group cluster = cg::this_cluster();
+    const int E = rows_here * DP;
+    const int per = (E + ncta - 1) / ncta;  // output elements each CTA finishes
+    const int e0 = rank * per, e1 = min(E, e0 + per);
+    if constexpr (C::kPush) {
+        // Every CTA has started (the arrive at the top); store this CTA's
+        // row statistics into every peer and each output element into the
+        // peer that finishes it, then one cluster barrier publishes them.
+        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
+            const int r = idx / ncta, k = idx - r * ncta;
+            *cluster.map_shared_rank(sAllM + r * 16 + rank, k) = sPm[r];
+            *cluster.map_shared_rank(sAllL + r * 16 + rank, k) = sPl[r];
+        }
+        if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+        for (int e = tid; e < E; e += NT) {
+            const int k = e / per;
+            *cluster.map_shared_rank(sRecv + rank * per + (e - k * per), k) = sMo[e];
+        }
+        cluster.sync();
     } else {
-        // ---- merge the cluster's partials through distributed shared memory.
-        // Every remote value a phase needs is fetched by an independent load,
-        // so each phase costs about one distributed-shared-memory round trip.
-        cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
         for (int idx = tid; idx < rows_here * ncta; idx += NT) {
             const int r = idx / ncta, c = idx - r * ncta;
@@ -758,51 +824,49 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         }
         if (tid < ncta) sAllF[tid] = *cluster.map_shared_rank(sFlag, tid);
         __syncthreads();
-        if (tid < rows_here) {
-            const int r = tid;
-            float M = -CUDART_INF_F;
-            bool poison = false;
-            for (int c = 0; c < ncta; ++c) {
-                M = fmaxf(M, sAllM[r * 16 + c]);
-                poison |= sAllF[c] != 0;
-            }
-            float W = 0.f;
-            for (int c = 0; c < ncta; ++c) {
-                const float w = (M == -CUDART_INF_F) ? 0.f : exp2f(sAllM[r * 16 + c] - M);
-                sAllM[r * 16 + c] = w;
-                W = fmaf(w, sAllL[r * 16 + c], W);
-            }
-            const bool zero = poison || W <= 0.f;
-            const float inv = zero ? 0.f : 1.f / W;
-            for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] = zero ? 0.f : sAllM[r * 16 + c] * inv;
-            sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
-        }
-        __syncthreads();
-        const int E = rows_here * DP;
-        const int per = (E + ncta - 1) / ncta;
-        const int e0 = rank * per, e1 = min(E, e0 + per);
-        for (int idx = e0 + tid; idx < e1; idx += NT) {
-            const int r = idx / DP, d = idx - r * DP;
-            float v[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
-            float o = 0.f;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                // A zero weight must not touch its partial: a poisoned one may hold NaN.
-                const float w = c < ncta ? sAllM[r * 16 + c] : 0.f;
-                o += w != 0.f ? w * v[c] : 0.f;
-            }
-            const long long orow = out_row(r);
-            if (d < p.D) p.out[orow * p.D + d] = o;
-            if (d == 0 && p.lse) p.lse[orow] = sLse[r];
-        }
-        cluster.sync();  // partials stay readable until every CTA has merged its slice
     }
-    if (first_cta) {
-        __syncthreads();
-        zero_uncovered(p, reinterpret_cast<int *>(body), NT);
+    if (tid < rows_here) {
+        const int r = tid;
+        float M = -CUDART_INF_F;
+        bool poison = false;
+        for (int c = 0; c < ncta; ++c) {
+            M = fmaxf(M, sAllM[r * 16 + c]);
+            poison |= sAllF[c] != 0;
+        }
+        float W = 0.f;
+        for (int c = 0; c < ncta; ++c) {
+            const float w = (M == -CUDART_INF_F) ? 0.f : exp2f(sAllM[r * 16 + c] - M);
+            sAllM[r * 16 + c] = w;
+            W = fmaf(w, sAllL[r * 16 + c], W);
+        }
+        const bool zero = poison || W <= 0.f;
+        const float inv = zero ? 0.f : 1.f / W;
+        for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] = zero ? 0.f : sAllM[r * 16 + c] * inv;
+        sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
     }
+    __syncthreads();
+    for (int idx = e0 + tid; idx < e1; idx += NT) {
+        const int r = idx / DP, d = idx - r * DP;
+        float v[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            if constexpr (C::kPush)
+                v[c] = c < ncta ? sRecv[c * per + (idx - e0)] : 0.f;
+            else
+                v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
+        }
+        float o = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            // A zero weight must not touch its partial: a poisoned one may hold NaN.
+            const float w = c < ncta ? sAllM[r * 16 + c] : 0.f;
+            o += w != 0.f ? w * v[c] : 0.f;
+        }
+        const long long orow = out_row(r);
+        if (d < p.D) p.out[orow * p.D + d] = o;
+        if (d == 0 && p.lse) p.lse[orow] = sLse[r];
+    }
+    if constexpr (!C::kPush) cluster.sync();  // partials stay readable until every CTA has merged its slice
 }
 
 }  // namespace pkv
