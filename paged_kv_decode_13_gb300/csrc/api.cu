@@ -150,7 +150,12 @@ int prepare_kernel(const AttnKernel &k) {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < ndone; ++i)
         if (done[i] == k.fn) return PKV_OK;
+    // Ask for the largest shared-memory carveout so two CTAs fit on an SM:
+    // with programmatic dependent launch the next layer's CTAs can then start
+    // streaming their pages beside this layer's.
     if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem) != cudaSuccess ||
+        cudaFuncSetAttribute(k.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(k.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ECUDA;

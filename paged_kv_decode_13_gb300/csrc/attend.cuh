@@ -372,12 +372,14 @@ struct SimtWarp {
 // One CTA zeroes every output row that no segment covers and flags rows that
 // two segments claim.  Segments with a negative q_start or non-positive q_len
 // cover nothing.
-static __device__ void zero_uncovered(const AttendParams &p, int *sFlags, int nthreads, int first_row) {
+static __device__ __noinline__ void zero_uncovered(const AttendParams &p, int *sFlags, int nthreads, int first_row) {
     const int tid = threadIdx.x;
+    #pragma unroll 1
     for (int base = first_row; base < p.total_rows; base += nthreads) {
         const int t = base + tid;
         int cnt = 0;
         if (t < p.total_rows) {
+            #pragma unroll 1
             for (int s = 0; s < p.S; ++s) {
                 const Segment g = load_segment(p.seq_info, s);
                 if (g.q0 >= 0 && g.ql > 0 && t >= g.q0 && (long long)t < (long long)g.q0 + g.ql) ++cnt;
@@ -388,11 +390,14 @@ static __device__ void zero_uncovered(const AttendParams &p, int *sFlags, int nt
         __syncthreads();
         const int n = min(nthreads, p.total_rows - base);
         const int per_row = p.Hq * p.D;
+        #pragma unroll 1
         for (int r = 0; r < n; ++r) {
             if (!sFlags[r]) continue;
             const long long t2 = base + r;
+            #pragma unroll 1
             for (int e = tid; e < per_row; e += nthreads) p.out[t2 * per_row + e] = 0.f;
             if (p.lse)
+                #pragma unroll 1
                 for (int e = tid; e < p.Hq; e += nthreads) p.lse[t2 * p.Hq + e] = -CUDART_INF_F;
         }
         __syncthreads();
@@ -400,16 +405,44 @@ static __device__ void zero_uncovered(const AttendParams &p, int *sFlags, int nt
 }
 
 // Zero the rows of kv head g's group for a segment that failed validation.
-static __device__ void zero_segment_rows(const AttendParams &p, const Segment &sg, int g, int nthreads) {
+static __device__ __noinline__ void zero_segment_rows(const AttendParams &p, const Segment &sg, int g, int nthreads) {
     if (sg.ql <= 0) return;
     const long long a = max(sg.q0, 0);
     const long long b = min((long long)sg.q0 + sg.ql, (long long)p.total_rows);
     const int per = p.G * p.D;
+    #pragma unroll 1
     for (long long t = a; t < b; ++t) {
         float *o = p.out + (t * p.Hq + (long long)g * p.G) * p.D;
+        #pragma unroll 1
         for (int e = threadIdx.x; e < per; e += nthreads) o[e] = 0.f;
         if (p.lse)
+            #pragma unroll 1
             for (int e = threadIdx.x; e < p.G; e += nthreads) p.lse[t * p.Hq + g * p.G + e] = -CUDART_INF_F;
+    }
+}
+
+// First CTA, after the dependency wait: zero the rows the pre-wait scan found
+// uncovered among the first `nthreads` rows, flag double coverage, then scan
+// and zero any rows past them.
+static __device__ __noinline__ void apply_coverage(const AttendParams &p, int *sCov, int cov_any, int nthreads) {
+    const int tid = threadIdx.x;
+    if (cov_any) {
+        const int n = min(nthreads, p.total_rows), per_row = p.Hq * p.D;
+        #pragma unroll 1
+        for (int r = 0; r < n; ++r) {
+            const int f = sCov[r];
+            if ((f & 2) && tid == 0) atomicOr(p.err, PKV_ERR_OVERLAP);
+            if (!(f & 1)) continue;
+            #pragma unroll 1
+            for (int e = tid; e < per_row; e += nthreads) p.out[(long long)r * per_row + e] = 0.f;
+            if (p.lse)
+                #pragma unroll 1
+                for (int e = tid; e < p.Hq; e += nthreads) p.lse[(long long)r * p.Hq + e] = -CUDART_INF_F;
+        }
+    }
+    if (p.total_rows > nthreads) {
+        __syncthreads();
+        zero_uncovered(p, sCov, nthreads, nthreads);
     }
 }
 
@@ -460,6 +493,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         int f = 0;
         if (tid < p.total_rows) {
             int cnt = 0;
+            #pragma unroll 1
             for (int s2 = 0; s2 < p.S; ++s2) {
                 const Segment o = load_segment(p.seq_info, s2);
                 if (o.q0 >= 0 && o.ql > 0 && tid >= o.q0 && (long long)tid < (long long)o.q0 + o.ql) ++cnt;
@@ -469,28 +503,10 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         sCov[tid] = f;
         cov_any = __syncthreads_or(f != 0);
     }
-    auto apply_coverage = [&]() {  // first CTA, after the dependency wait
-        if (cov_any) {
-            const int n = min(NT, p.total_rows), per_row = p.Hq * p.D;
-            for (int r = 0; r < n; ++r) {
-                const int f = sCov[r];
-                if ((f & 2) && tid == 0) atomicOr(p.err, PKV_ERR_OVERLAP);
-                if (!(f & 1)) continue;
-                for (int e = tid; e < per_row; e += NT) p.out[(long long)r * per_row + e] = 0.f;
-                if (p.lse)
-                    for (int e = tid; e < p.Hq; e += NT) p.lse[(long long)r * p.Hq + e] = -CUDART_INF_F;
-            }
-        }
-        if (p.total_rows > NT) {
-            __syncthreads();
-            zero_uncovered(p, sCov, NT, NT);
-        }
-    };
-
     if (p.S == 0) {  // nothing but rows no segment covers
         pdl_wait();
         pdl_trigger();
-        if (first_cta) apply_coverage();
+        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
     }
 
@@ -507,23 +523,24 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             if (tid == 0) atomicOr(p.err, fault);
             zero_segment_rows(p, sg, g, NT);
         }
-        if (first_cta) apply_coverage();
+        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
     }
     if (C::kPush && ncta > 1)  // announce this CTA to the cluster; waited on before any remote store
         asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
     const int rows_here = min(R, rows_unit - row0);
-    const long long kend = sg.kend;
-    const long long new_start = kend - sg.ql;  // first position appended this step
-    long long lo_u = 0;
-    if (p.window > 0) lo_u = max(0LL, (p.causal ? new_start : kend - 1) - p.window + 1);
-    const long long pb_begin = lo_u / kPage;
-    const long long pb_end = (kend + kPage - 1) / kPage;
-    const long long nblk = pb_end - pb_begin;
-    const long long bps = (nblk + ncta - 1) / ncta;
-    const int active = (int)((nblk + bps - 1) / bps);
-    const long long cb0 = pb_begin + (long long)rank * bps;
-    const int nb = rank < active ? (int)(min(cb0 + bps, pb_end) - cb0) : 0;
+    // Positions fit in 32 bits: kv_end <= 2^31 - 33 is part of segment validity.
+    const int kend = sg.kend;
+    const int new_start = kend - sg.ql;  // first position appended this step
+    int lo_u = 0;
+    if (p.window > 0) lo_u = max(0, (p.causal ? new_start : kend - 1) - p.window + 1);
+    const int pb_begin = lo_u / kPage;
+    const int pb_end = (kend + kPage - 1) / kPage;
+    const int nblk = pb_end - pb_begin;
+    const int bps = (nblk + ncta - 1) / ncta;
+    const int active = (nblk + bps - 1) / bps;
+    const int cb0 = pb_begin + rank * bps;
+    const int nb = rank < active ? min(cb0 + bps, pb_end) - cb0 : 0;
     const int n_mine = nb > kw ? (nb - kw + KW - 1) / KW : 0;
 
     const T *knew = reinterpret_cast<const T *>(p.k_new);
@@ -533,11 +550,12 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     const int *bt_row = p.block_table + (long long)sg.col * p.mbps;
     uint64_t *gbars = bars + kw * NST;
     unsigned char *gstage = body + (size_t)kw * NST * C::kStageBytes;
-    const long long lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
+    const int lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
     // This CTA's pages hold some of the step's own positions (fused call).
     const bool has_new = fused && rt == 0 && nb > 0 && new_start < hi_pos && kend > lo_pos;
 
     if (gtid == 0) {
+        #pragma unroll 1
         for (int i = 0; i < NST; ++i) mbar_init(gbars + i, 1);
         fence_barrier_init();
     }
@@ -550,9 +568,10 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     bool app_ok = false;
     if (has_new) {
         bool ok = true;
+        #pragma unroll 1
         for (int i = tid; i < sg.ql; i += NT) {
-            const long long pos = new_start + i;
-            const long long rr = p.ring_rows ? pos % p.ring_rows : pos;
+            const int pos = new_start + i;
+            const int rr = p.ring_rows ? pos % p.ring_rows : pos;
             const int b = bt_row[rr / kPage];
             ok &= b >= 0 && (long long)b < p.num_blocks;
         }
@@ -593,12 +612,13 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     };
     // Pages wholly below new_start hold keys written before this step, so they
     // may be fetched before the dependency wait.
-    auto early_ok = [&](int j) { return (cb0 + kw + (long long)j * KW + 1) * kPage <= new_start; };
+    auto early_ok = [&](int j) { return (cb0 + kw + j * KW + 1) * kPage <= new_start; };
     // Bounded wait for the j-th page of the group; warp-uniform result.
     auto wait_page = [&](int j) {
         if (timed_out) return;
         bool done = false;
         if (lane == 0) {
+            #pragma unroll 1
             for (int it = 0; it < kWaitProbes && !done; ++it) done = mbar_try_wait(gbars + (j % NST), (j / NST) & 1);
         }
         done = __shfl_sync(0xffffffffu, done, 0);
@@ -609,6 +629,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     int issued = 0;
     if (mt == 0) {
         load_ids(0);
+        #pragma unroll 1
         for (; issued < NST && issued < n_mine; ++issued) {
             if (!early_ok(issued)) break;
             issue(issued);
@@ -619,19 +640,21 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
 
     if (has_new) {  // bring this step's rows towards the SM; the page fix-up reads them
         const int lines = (p.D * C::kElem + 127) / 128;
-        const long long a = max(new_start, lo_pos), e = min(kend, hi_pos);
-        const int n = (int)(e - a) * 2 * lines;
+        const int a = max(new_start, lo_pos), e = min(kend, hi_pos);
+        const int n = (e - a) * 2 * lines;
+        #pragma unroll 1
         for (int c = tid; c < n; c += NT) {
             const int row = c / (2 * lines), rem = c - row * 2 * lines, kv = rem / lines, ln = rem - kv * lines;
             const T *src = (kv ? vnew : knew) + (((long long)sg.q0 + (a + row - new_start)) * p.Hkv + g) * p.D;
             asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + ln * 128));
         }
     }
-    if (first_cta) apply_coverage();
+    if (first_cta) apply_coverage(p, sCov, cov_any, NT);
 
     // Query rows of this tile and their key bounds.
     if constexpr (C::MMA) {
         T *sQ = reinterpret_cast<T *>(qarea);
+        #pragma unroll 1
         for (int c = tid; c < R * C::kChunks; c += NT) {
             const int r = c / C::kChunks, ch = c - r * C::kChunks;
             const int ur = row0 + r;
@@ -646,6 +669,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         }
     } else {
         float *sQf = reinterpret_cast<float *>(qarea);
+        #pragma unroll 1
         for (int c = tid; c < R * C::kChunks; c += NT) {
             const int r = c / C::kChunks, ch = c - r * C::kChunks;
             const int ur = row0 + r;
@@ -662,19 +686,21 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             for (int e = 0; e < EPC; ++e) sQf[r * C::kQLd + ch * EPC + e] = f[e];
         }
     }
+    #pragma unroll 1
     for (int r = tid; r < R; r += NT) {
         const int ur = row0 + r;
         int lo = 0, hi = 0;
         if (ur < rows_unit) {
-            const long long pos = new_start + ur / p.G;
-            const long long newest = p.causal ? pos : kend - 1;
-            hi = (int)(p.causal ? pos + 1 : kend);
-            lo = p.window > 0 ? (int)max(0LL, newest - p.window + 1) : 0;
+            const int pos = new_start + ur / p.G;
+            const int newest = p.causal ? pos : kend - 1;
+            hi = p.causal ? pos + 1 : kend;
+            lo = p.window > 0 ? max(0, newest - p.window + 1) : 0;
         }
         sLo[r] = lo;
         sHi[r] = hi;
     }
     if (mt == 0) {
+        #pragma unroll 1
         for (; issued < NST && issued < n_mine; ++issued) issue(issued);
     }
     __syncthreads();
@@ -690,21 +716,24 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         if constexpr (MT == 1) __syncwarp(); else named_barrier(1 + kw, GT);
     };
 
+    #pragma unroll 1
     for (int j = 0; j < n_mine; ++j) {
         wait_page(j);
         unsigned char *st = gstage + (size_t)(j % NST) * C::kStageBytes;
-        const long long pos0 = (cb0 + kw + (long long)j * KW) * kPage;
+        const int pos0 = (cb0 + kw + j * KW) * kPage;
         // Rows outside [lo_u, kend) may hold anything (NaN included): zero them.
         // This step's own rows come from k_new / v_new in the fused call, and
         // the CTA that owns them also writes them into the cache here.
         if (pos0 < lo_u || pos0 + kPage > kend || (fused && pos0 + kPage > new_start)) {
             const bool to_pool = app_ok && pos0 + kPage > new_start;
             const long long bpage = to_pool ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
+            const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;  // slot of the page's first row
+            #pragma unroll 1
             for (int c = gtid; c < 2 * kPage * C::kChunks; c += GT) {
                 const int kv = c / (kPage * C::kChunks);
                 const int rem = c - kv * (kPage * C::kChunks);
                 const int o = rem / C::kChunks, ch = rem - o * C::kChunks;
-                const long long pos = pos0 + o;
+                const int pos = pos0 + o;
                 uint4 *dst = reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch));
                 if (pos < lo_u || pos >= kend) {
                     *dst = make_uint4(0u, 0u, 0u, 0u);
@@ -715,7 +744,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
                             (kv ? vnew : knew) + (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D +
                             ch * EPC);
                         if (to_pool) {
-                            const long long slot = bpage * kPage + (p.ring_rows ? pos % p.ring_rows : pos) % kPage;
+                            const long long slot = bpage * kPage + (ring_base + o) % kPage;
                             *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
                                                        (slot * p.Hkv + g) * p.D + ch * EPC) = v;
                         }
@@ -740,7 +769,9 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     if (timed_out && lane == 0 && mt == 0) {
         // Give the copies still in flight a bounded chance to land before the
         // stage memory is reused.
+        #pragma unroll 1
         for (int j = max(0, n_mine - NST); j < n_mine; ++j)
+            #pragma unroll 1
             for (int it = 0; it < kWaitProbes && !mbar_try_wait(gbars + (j % NST), (j / NST) & 1); ++it) {
             }
     }
@@ -755,6 +786,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     }
     if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
     __syncthreads();
+    #pragma unroll 1
     for (int idx = tid; idx < rows_here * DP; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
         float M = -CUDART_INF_F;
@@ -783,6 +815,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
     };
     if (ncta == 1) {
+        #pragma unroll 1
         for (int idx = tid; idx < rows_here * DP; idx += NT) {
             const int r = idx / DP, d = idx - r * DP;
             const float L = sPl[r];
@@ -804,12 +837,14 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         // row statistics into every peer and each output element into the
         // peer that finishes it, then one cluster barrier publishes them.
         asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+        #pragma unroll 1
         for (int idx = tid; idx < rows_here * ncta; idx += NT) {
             const int r = idx / ncta, k = idx - r * ncta;
             *cluster.map_shared_rank(sAllM + r * 16 + rank, k) = sPm[r];
             *cluster.map_shared_rank(sAllL + r * 16 + rank, k) = sPl[r];
         }
         if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+        #pragma unroll 1
         for (int e = tid; e < E; e += NT) {
             const int k = e / per;
             *cluster.map_shared_rank(sRecv + rank * per + (e - k * per), k) = sMo[e];
@@ -817,6 +852,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         cluster.sync();
     } else {
         cluster.sync();
+        #pragma unroll 1
         for (int idx = tid; idx < rows_here * ncta; idx += NT) {
             const int r = idx / ncta, c = idx - r * ncta;
             sAllM[r * 16 + c] = *cluster.map_shared_rank(sPm + r, c);
@@ -829,11 +865,13 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         const int r = tid;
         float M = -CUDART_INF_F;
         bool poison = false;
+        #pragma unroll 1
         for (int c = 0; c < ncta; ++c) {
             M = fmaxf(M, sAllM[r * 16 + c]);
             poison |= sAllF[c] != 0;
         }
         float W = 0.f;
+        #pragma unroll 1
         for (int c = 0; c < ncta; ++c) {
             const float w = (M == -CUDART_INF_F) ? 0.f : exp2f(sAllM[r * 16 + c] - M);
             sAllM[r * 16 + c] = w;
@@ -841,10 +879,12 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         }
         const bool zero = poison || W <= 0.f;
         const float inv = zero ? 0.f : 1.f / W;
+        #pragma unroll 1
         for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] = zero ? 0.f : sAllM[r * 16 + c] * inv;
         sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
     }
     __syncthreads();
+    #pragma unroll 1
     for (int idx = e0 + tid; idx < e1; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
         float v[16];

@@ -166,7 +166,7 @@ __device__ __forceinline__ unsigned segment_fault(const Segment &s, int total_ro
                                                   int mbps, int ring_rows, int window) {
     if (s.q0 < 0 || s.ql < 0 || (long long)s.q0 + s.ql > total_rows) return PKV_ERR_SEGMENT;
     if (s.col < 0 || s.col >= max_seqs) return PKV_ERR_SEGMENT;
-    if (s.kend < s.ql) return PKV_ERR_SEGMENT;
+    if (s.kend < s.ql || s.kend > 0x7fffffff - 2 * kPage) return PKV_ERR_SEGMENT;
     if (ring_rows) {
         if (window <= 0 || (long long)window + s.ql - 1 > ring_rows) return PKV_ERR_RING;
     } else if ((long long)s.kend > (long long)mbps * kPage) {
@@ -178,8 +178,8 @@ __device__ __forceinline__ unsigned segment_fault(const Segment &s, int total_ro
 // Page index in the sequence's table row for logical position-block `pb`
 // (positions pb*16 .. pb*16+15).  Ring rows are a multiple of 16, so a page
 // of positions never straddles the wrap.
-__device__ __forceinline__ int table_page(long long pb, int ring_rows) {
-    return ring_rows ? (int)(pb % (ring_rows / kPage)) : (int)pb;
+__device__ __forceinline__ int table_page(int pb, int ring_rows) {
+    return ring_rows ? pb % (ring_rows >> 4) : pb;
 }
 
 __device__ __forceinline__ Segment load_segment(const int4 *seq_info, int s) {
