@@ -611,8 +611,9 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         }
     };
     // Pages wholly below new_start hold keys written before this step, so they
-    // may be fetched before the dependency wait.
-    auto early_ok = [&](int j) { return (cb0 + kw + j * KW + 1) * kPage <= new_start; };
+    // may be fetched before the dependency wait.  In the fused call every page
+    // may: the step's own rows are replaced from k_new / v_new after the wait.
+    auto early_ok = [&](int j) { return fused || (cb0 + kw + j * KW + 1) * kPage <= new_start; };
     // Bounded wait for the j-th page of the group; warp-uniform result.
     auto wait_page = [&](int j) {
         if (timed_out) return;
@@ -624,6 +625,30 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         done = __shfl_sync(0xffffffffu, done, 0);
         if (!done) timed_out = true;
     };
+
+    // Warm L2 with the rows read right after the wait: this tile's queries and,
+    // in the fused call, this step's K/V rows.  A prefetch returns nothing, so
+    // issuing it before the dependency wait cannot observe stale data.
+    {
+        const int lines = (p.D * C::kElem + 127) / 128;
+        const int nq = rows_here * lines;
+#pragma unroll 1
+        for (int c = tid; c < nq; c += NT) {
+            const int r = c / lines, ln = c - r * lines, ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
+            const T *src = reinterpret_cast<const T *>(p.q) + (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D;
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + ln * 128));
+        }
+        if (has_new) {
+            const int a = max(new_start, lo_pos), e = min(kend, hi_pos);
+            const int n = (e - a) * 2 * lines;
+#pragma unroll 1
+            for (int c = tid; c < n; c += NT) {
+                const int row = c / (2 * lines), rem = c - row * 2 * lines, kv = rem / lines, ln = rem - kv * lines;
+                const T *src = (kv ? vnew : knew) + (((long long)sg.q0 + (a + row - new_start)) * p.Hkv + g) * p.D;
+                asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + ln * 128));
+            }
+        }
+    }
 
     // ---- prologue: start the first stages before waiting on the previous kernel
     int issued = 0;
@@ -638,55 +663,41 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     pdl_wait();
     pdl_trigger();
 
-    if (has_new) {  // bring this step's rows towards the SM; the page fix-up reads them
-        const int lines = (p.D * C::kElem + 127) / 128;
-        const int a = max(new_start, lo_pos), e = min(kend, hi_pos);
-        const int n = (e - a) * 2 * lines;
-        #pragma unroll 1
-        for (int c = tid; c < n; c += NT) {
-            const int row = c / (2 * lines), rem = c - row * 2 * lines, kv = rem / lines, ln = rem - kv * lines;
-            const T *src = (kv ? vnew : knew) + (((long long)sg.q0 + (a + row - new_start)) * p.Hkv + g) * p.D;
-            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + ln * 128));
-        }
-    }
     if (first_cta) apply_coverage(p, sCov, cov_any, NT);
 
-    // Query rows of this tile and their key bounds.
-    if constexpr (C::MMA) {
-        T *sQ = reinterpret_cast<T *>(qarea);
-        #pragma unroll 1
-        for (int c = tid; c < R * C::kChunks; c += NT) {
-            const int r = c / C::kChunks, ch = c - r * C::kChunks;
-            const int ur = row0 + r;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (ur < rows_unit && ch < dchunks) {
+    // Query rows of this tile (all loads issued before any store) and their key bounds.
+    {
+        constexpr int kQIt = (R * C::kChunks + NT - 1) / NT;
+        uint4 qv[kQIt];
+#pragma unroll
+        for (int it = 0; it < kQIt; ++it) {
+            const int c = tid + it * NT;
+            const int r = c / C::kChunks, ch = c - r * C::kChunks, ur = row0 + r;
+            qv[it] = make_uint4(0u, 0u, 0u, 0u);
+            if (c < R * C::kChunks && ur < rows_unit && ch < dchunks) {
                 const int i = ur / p.G, jh = ur - i * p.G;
-                const T *src = reinterpret_cast<const T *>(p.q) +
-                               (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D + ch * EPC;
-                v = *reinterpret_cast<const uint4 *>(src);
+                qv[it] = *reinterpret_cast<const uint4 *>(
+                    reinterpret_cast<const T *>(p.q) +
+                    (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D + ch * EPC);
             }
-            *reinterpret_cast<uint4 *>(sQ + r * C::kQLd + ch * EPC) = v;
         }
-    } else {
-        float *sQf = reinterpret_cast<float *>(qarea);
-        #pragma unroll 1
-        for (int c = tid; c < R * C::kChunks; c += NT) {
+#pragma unroll
+        for (int it = 0; it < kQIt; ++it) {
+            const int c = tid + it * NT;
+            if (c >= R * C::kChunks) continue;
             const int r = c / C::kChunks, ch = c - r * C::kChunks;
-            const int ur = row0 + r;
-            float f[EPC];
+            if constexpr (C::MMA) {
+                *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(qarea) + r * C::kQLd + ch * EPC) = qv[it];
+            } else {
+                float f[EPC];
+                load_f32<T, EPC>(f, reinterpret_cast<const T *>(&qv[it]));
+                float *dst = reinterpret_cast<float *>(qarea) + r * C::kQLd + ch * EPC;
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) f[e] = 0.f;
-            if (ur < rows_unit && ch < dchunks) {
-                const int i = ur / p.G, jh = ur - i * p.G;
-                const T *src = reinterpret_cast<const T *>(p.q) +
-                               (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D + ch * EPC;
-                load_f32<T, EPC>(f, src);
+                for (int e = 0; e < EPC; ++e) dst[e] = f[e];
             }
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) sQf[r * C::kQLd + ch * EPC + e] = f[e];
         }
     }
-    #pragma unroll 1
+#pragma unroll 1
     for (int r = tid; r < R; r += NT) {
         const int ur = row0 + r;
         int lo = 0, hi = 0;
@@ -786,8 +797,25 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     }
     if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
     __syncthreads();
-    #pragma unroll 1
-    for (int idx = tid; idx < rows_here * DP; idx += NT) {
+
+    constexpr float kLn2 = 0.6931471805599453f;
+    auto out_row = [&](int r) {
+        const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
+        return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
+    };
+    cg::cluster_group cluster = cg::this_cluster();
+    const int E = rows_here * DP;
+    const int per = (E + ncta - 1) / ncta;  // output elements each CTA of the cluster finishes
+    if (C::kPush && ncta > 1) {
+        // Every CTA of the cluster has started (the arrive at the top), so
+        // peers' shared memory may be written from here on.
+        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+        if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+    }
+    // Merge the key groups element by element; finish each element here when
+    // the CTA is alone, otherwise hand it to the CTA that finishes it.
+#pragma unroll 1
+    for (int idx = tid; idx < E; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
         float M = -CUDART_INF_F;
 #pragma unroll
@@ -801,58 +829,37 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
                 o = fmaf(w, sMo[((size_t)k * R + r) * DP + d], o);
             }
         }
-        sMo[(size_t)r * DP + d] = o;  // element owned by this thread alone: merged in place
-        if (d == 0) {
-            sPm[r] = M;
-            sPl[r] = L;
-        }
-    }
-    __syncthreads();
-
-    constexpr float kLn2 = 0.6931471805599453f;
-    auto out_row = [&](int r) {
-        const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
-        return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
-    };
-    if (ncta == 1) {
-        #pragma unroll 1
-        for (int idx = tid; idx < rows_here * DP; idx += NT) {
-            const int r = idx / DP, d = idx - r * DP;
-            const float L = sPl[r];
+        if (ncta == 1) {
             const bool zero = flags || L <= 0.f;
             const long long orow = out_row(r);
-            if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : sMo[(size_t)r * DP + d] / L;
-            if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (sPm[r] + log2f(L)) * kLn2;
+            if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / L;
+            if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
+        } else if constexpr (C::kPush) {
+            const int k = idx / per;
+            *cluster.map_shared_rank(sRecv + rank * per + (idx - k * per), k) = o;
+            if (d == 0) {
+#pragma unroll 1
+                for (int c = 0; c < ncta; ++c) {
+                    *cluster.map_shared_rank(sAllM + r * 16 + rank, c) = M;
+                    *cluster.map_shared_rank(sAllL + r * 16 + rank, c) = L;
+                }
+            }
+        } else {
+            sMo[(size_t)r * DP + d] = o;  // element owned by this thread alone: merged in place
+            if (d == 0) {
+                sPm[r] = M;
+                sPl[r] = L;
+            }
         }
-        return;
     }
+    if (ncta == 1) return;
 
-    // ---- merge the cluster's partials through distributed shared memory
-    cg::cluster_group cluster = cg::this_cluster();
-    const int E = rows_here * DP;
-    const int per = (E + ncta - 1) / ncta;  // output elements each CTA finishes
-    const int e0 = rank * per, e1 = min(E, e0 + per);
+    // ---- merge the cluster's partials (distributed shared memory)
     if constexpr (C::kPush) {
-        // Every CTA has started (the arrive at the top); store this CTA's
-        // row statistics into every peer and each output element into the
-        // peer that finishes it, then one cluster barrier publishes them.
-        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
-        #pragma unroll 1
-        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
-            const int r = idx / ncta, k = idx - r * ncta;
-            *cluster.map_shared_rank(sAllM + r * 16 + rank, k) = sPm[r];
-            *cluster.map_shared_rank(sAllL + r * 16 + rank, k) = sPl[r];
-        }
-        if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
-        #pragma unroll 1
-        for (int e = tid; e < E; e += NT) {
-            const int k = e / per;
-            *cluster.map_shared_rank(sRecv + rank * per + (e - k * per), k) = sMo[e];
-        }
-        cluster.sync();
+        cluster.sync();  // publishes every CTA's pushed partials
     } else {
         cluster.sync();
-        #pragma unroll 1
+#pragma unroll 1
         for (int idx = tid; idx < rows_here * ncta; idx += NT) {
             const int r = idx / ncta, c = idx - r * ncta;
             sAllM[r * 16 + c] = *cluster.map_shared_rank(sPm + r, c);
@@ -861,50 +868,38 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         if (tid < ncta) sAllF[tid] = *cluster.map_shared_rank(sFlag, tid);
         __syncthreads();
     }
-    if (tid < rows_here) {
-        const int r = tid;
-        float M = -CUDART_INF_F;
-        bool poison = false;
-        #pragma unroll 1
-        for (int c = 0; c < ncta; ++c) {
-            M = fmaxf(M, sAllM[r * 16 + c]);
-            poison |= sAllF[c] != 0;
-        }
-        float W = 0.f;
-        #pragma unroll 1
-        for (int c = 0; c < ncta; ++c) {
-            const float w = (M == -CUDART_INF_F) ? 0.f : exp2f(sAllM[r * 16 + c] - M);
-            sAllM[r * 16 + c] = w;
-            W = fmaf(w, sAllL[r * 16 + c], W);
-        }
-        const bool zero = poison || W <= 0.f;
-        const float inv = zero ? 0.f : 1.f / W;
-        #pragma unroll 1
-        for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] = zero ? 0.f : sAllM[r * 16 + c] * inv;
-        sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
-    }
-    __syncthreads();
-    #pragma unroll 1
+    int poison = 0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
+    const int e0 = rank * per, e1 = min(E, e0 + per);
+#pragma unroll 1
     for (int idx = e0 + tid; idx < e1; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
-        float v[16];
+        float m[16], l[16], v[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
+            m[c] = c < ncta ? sAllM[r * 16 + c] : -CUDART_INF_F;
+            l[c] = c < ncta ? sAllL[r * 16 + c] : 0.f;
             if constexpr (C::kPush)
                 v[c] = c < ncta ? sRecv[c * per + (idx - e0)] : 0.f;
             else
                 v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
         }
-        float o = 0.f;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) M = fmaxf(M, m[c]);
+        float W = 0.f, o = 0.f;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             // A zero weight must not touch its partial: a poisoned one may hold NaN.
-            const float w = c < ncta ? sAllM[r * 16 + c] : 0.f;
+            const float w = (M == -CUDART_INF_F || m[c] == -CUDART_INF_F) ? 0.f : exp2f(m[c] - M);
+            W = fmaf(w, l[c], W);
             o += w != 0.f ? w * v[c] : 0.f;
         }
+        const bool zero = poison || W <= 0.f;
         const long long orow = out_row(r);
-        if (d < p.D) p.out[orow * p.D + d] = o;
-        if (d == 0 && p.lse) p.lse[orow] = sLse[r];
+        if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / W;
+        if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
     }
     if constexpr (!C::kPush) cluster.sync();  // partials stay readable until every CTA has merged its slice
 }
