@@ -663,6 +663,26 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     pdl_wait();
     pdl_trigger();
 
+    // This step's rows that fall in the CTA's last page (decode: the one new
+    // row) are loaded now, next to the query loads, by the key group that
+    // consumes that page; the page fix-up stores them.
+    const int last_li = nb - 1, last_pos0 = (cb0 + last_li) * kPage;
+    const int pre_a = max(new_start, last_pos0), pre_n = has_new ? max(0, kend - pre_a) : 0;
+    const bool pre_mine = pre_n > 0 && kw == last_li % KW;
+    uint4 pre[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        pre[it] = make_uint4(0u, 0u, 0u, 0u);
+        const int c = gtid + it * GT;
+        if (pre_mine && c < 2 * pre_n * dchunks) {
+            const int kv = c / (pre_n * dchunks), rem = c - kv * pre_n * dchunks;
+            const int row = rem / dchunks, ch = rem - row * dchunks;
+            pre[it] = *reinterpret_cast<const uint4 *>((kv ? vnew : knew) +
+                                                       (((long long)sg.q0 + (pre_a + row - new_start)) * p.Hkv + g) * p.D +
+                                                       ch * EPC);
+        }
+    }
+
     if (first_cta) apply_coverage(p, sCov, cov_any, NT);
 
     // Query rows of this tile (all loads issued before any store) and their key bounds.
@@ -735,32 +755,45 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         // Rows outside [lo_u, kend) may hold anything (NaN included): zero them.
         // This step's own rows come from k_new / v_new in the fused call, and
         // the CTA that owns them also writes them into the cache here.
-        if (pos0 < lo_u || pos0 + kPage > kend || (fused && pos0 + kPage > new_start)) {
-            const bool to_pool = app_ok && pos0 + kPage > new_start;
-            const long long bpage = to_pool ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
-            const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;  // slot of the page's first row
-            #pragma unroll 1
-            for (int c = gtid; c < 2 * kPage * C::kChunks; c += GT) {
-                const int kv = c / (kPage * C::kChunks);
-                const int rem = c - kv * (kPage * C::kChunks);
-                const int o = rem / C::kChunks, ch = rem - o * C::kChunks;
-                const int pos = pos0 + o;
-                uint4 *dst = reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch));
-                if (pos < lo_u || pos >= kend) {
-                    *dst = make_uint4(0u, 0u, 0u, 0u);
-                } else if (fused && pos >= new_start) {
+        const int zlo = min(max(lo_u - pos0, 0), kPage);          // rows [0, zlo) precede the window
+        const int zhi = min(max(kend - pos0, 0), kPage);          // rows [zhi, 16) are past kv_end
+        const int na = fused ? min(max(new_start - pos0, 0), kPage) : zhi;  // rows [na, zhi) are new
+        if (zlo > 0 || zhi < kPage || na < zhi) {
+            const int nz = (zlo + kPage - zhi) * C::kChunks;
+#pragma unroll 1
+            for (int c = gtid; c < 2 * nz; c += GT) {
+                const int kv = c >= nz, rem = c - kv * nz, o0 = rem / C::kChunks, ch = rem - o0 * C::kChunks;
+                const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
+                *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            const int nn = (zhi - na) * C::kChunks;
+            if (nn > 0) {
+                const bool to_pool = app_ok;
+                const long long bpage = to_pool ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
+                const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;  // slot of the page's first row
+                const bool preloaded = pre_mine && j == last_li / KW && pos0 + na == pre_a;
+#pragma unroll 1
+                for (int c = gtid, it = 0; c < 2 * nn; c += GT, ++it) {
+                    const int kv = c >= nn, rem = c - kv * nn, r0 = rem / C::kChunks, ch = rem - r0 * C::kChunks;
+                    const int o = na + r0;
                     uint4 v = make_uint4(0u, 0u, 0u, 0u);
                     if (ch < dchunks) {
-                        v = *reinterpret_cast<const uint4 *>(
-                            (kv ? vnew : knew) + (((long long)sg.q0 + (pos - new_start)) * p.Hkv + g) * p.D +
-                            ch * EPC);
+                        // the preload enumerated (kv, row, real chunk); map this chunk onto it
+                        const int pc = kv * pre_n * dchunks + r0 * dchunks + ch;
+                        const int q = pc - gtid;
+                        if (preloaded && q >= 0 && q % GT == 0 && q / GT < 2)
+                            v = q == 0 ? pre[0] : pre[1];
+                        else
+                            v = *reinterpret_cast<const uint4 *>(
+                                (kv ? vnew : knew) + (((long long)sg.q0 + (pos0 + o - new_start)) * p.Hkv + g) * p.D +
+                                ch * EPC);
                         if (to_pool) {
                             const long long slot = bpage * kPage + (ring_base + o) % kPage;
                             *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
                                                        (slot * p.Hkv + g) * p.D + ch * EPC) = v;
                         }
                     }
-                    *dst = v;
+                    *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = v;
                 }
             }
             fence_proxy_async();
@@ -806,28 +839,51 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     cg::cluster_group cluster = cg::this_cluster();
     const int E = rows_here * DP;
     const int per = (E + ncta - 1) / ncta;  // output elements each CTA of the cluster finishes
+    // Row statistics of the key-group merge: max and sum per row.
+    if (tid < rows_here) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) M = fmaxf(M, sMm[k * R + tid]);
+        float L = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int k = 0; k < KW; ++k) L = fmaf(exp2f(sMm[k * R + tid] - M), sMl[k * R + tid], L);
+        }
+        sPm[tid] = M;
+        sPl[tid] = L;
+    }
+    __syncthreads();
+    // Owner of output element idx in the cluster: idx / per without an
+    // integer division in the loop.
+    const float inv_per = 1.f / (float)per;
+    auto owner = [&](int idx) {
+        int k = __float2int_rz((float)idx * inv_per);
+        k -= k * per > idx;
+        k += (k + 1) * per <= idx;
+        return k;
+    };
     if (C::kPush && ncta > 1) {
         // Every CTA of the cluster has started (the arrive at the top), so
         // peers' shared memory may be written from here on.
         asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
         if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+#pragma unroll 1
+        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
+            const int r = idx / ncta, c = idx - r * ncta;
+            *cluster.map_shared_rank(sAllM + r * 16 + rank, c) = sPm[r];
+            *cluster.map_shared_rank(sAllL + r * 16 + rank, c) = sPl[r];
+        }
     }
     // Merge the key groups element by element; finish each element here when
     // the CTA is alone, otherwise hand it to the CTA that finishes it.
 #pragma unroll 1
     for (int idx = tid; idx < E; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int k = 0; k < KW; ++k) M = fmaxf(M, sMm[k * R + r]);
-        float L = 0.f, o = 0.f;
+        const float M = sPm[r], L = sPl[r];
+        float o = 0.f;
         if (M != -CUDART_INF_F) {
 #pragma unroll
-            for (int k = 0; k < KW; ++k) {
-                const float w = exp2f(sMm[k * R + r] - M);
-                L = fmaf(w, sMl[k * R + r], L);
-                o = fmaf(w, sMo[((size_t)k * R + r) * DP + d], o);
-            }
+            for (int k = 0; k < KW; ++k) o = fmaf(exp2f(sMm[k * R + r] - M), sMo[((size_t)k * R + r) * DP + d], o);
         }
         if (ncta == 1) {
             const bool zero = flags || L <= 0.f;
@@ -835,21 +891,10 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / L;
             if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
         } else if constexpr (C::kPush) {
-            const int k = idx / per;
+            const int k = owner(idx);
             *cluster.map_shared_rank(sRecv + rank * per + (idx - k * per), k) = o;
-            if (d == 0) {
-#pragma unroll 1
-                for (int c = 0; c < ncta; ++c) {
-                    *cluster.map_shared_rank(sAllM + r * 16 + rank, c) = M;
-                    *cluster.map_shared_rank(sAllL + r * 16 + rank, c) = L;
-                }
-            }
         } else {
             sMo[(size_t)r * DP + d] = o;  // element owned by this thread alone: merged in place
-            if (d == 0) {
-                sPm[r] = M;
-                sPl[r] = L;
-            }
         }
     }
     if (ncta == 1) return;
