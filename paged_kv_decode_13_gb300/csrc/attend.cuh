@@ -839,18 +839,28 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     cg::cluster_group cluster = cg::this_cluster();
     const int E = rows_here * DP;
     const int per = (E + ncta - 1) / ncta;  // output elements each CTA of the cluster finishes
-    // Row statistics of the key-group merge: max and sum per row.
+    // Row statistics of the key-group merge, one thread per row: the max and
+    // sum, and each key group's weight 2^(m_k - M), left in sMm for the
+    // element pass.  A CTA alone in its cluster also keeps 1/L and the lse.
     if (tid < rows_here) {
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int k = 0; k < KW; ++k) M = fmaxf(M, sMm[k * R + tid]);
         float L = 0.f;
-        if (M != -CUDART_INF_F) {
 #pragma unroll
-            for (int k = 0; k < KW; ++k) L = fmaf(exp2f(sMm[k * R + tid] - M), sMl[k * R + tid], L);
+        for (int k = 0; k < KW; ++k) {
+            const float w = M == -CUDART_INF_F ? 0.f : exp2f(sMm[k * R + tid] - M);
+            L = fmaf(w, sMl[k * R + tid], L);
+            sMm[k * R + tid] = w;
         }
         sPm[tid] = M;
-        sPl[tid] = L;
+        if (ncta == 1) {
+            const bool zero = flags || L <= 0.f;
+            sPl[tid] = zero ? 0.f : 1.f / L;
+            sLse[tid] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
+        } else {
+            sPl[tid] = L;
+        }
     }
     __syncthreads();
     // Owner of output element idx in the cluster: idx / per without an
@@ -876,20 +886,19 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     }
     // Merge the key groups element by element; finish each element here when
     // the CTA is alone, otherwise hand it to the CTA that finishes it.
-#pragma unroll 1
+#pragma unroll 4
     for (int idx = tid; idx < E; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
-        const float M = sPm[r], L = sPl[r];
         float o = 0.f;
-        if (M != -CUDART_INF_F) {
 #pragma unroll
-            for (int k = 0; k < KW; ++k) o = fmaf(exp2f(sMm[k * R + r] - M), sMo[((size_t)k * R + r) * DP + d], o);
+        for (int k = 0; k < KW; ++k) {
+            // a key group with no visible key has weight 0 and a zero accumulator
+            o = fmaf(sMm[k * R + r], sMo[((size_t)k * R + r) * DP + d], o);
         }
         if (ncta == 1) {
-            const bool zero = flags || L <= 0.f;
             const long long orow = out_row(r);
-            if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / L;
-            if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
+            if (d < p.D) p.out[orow * p.D + d] = flags ? 0.f : o * sPl[r];
+            if (d == 0 && p.lse) p.lse[orow] = sLse[r];
         } else if constexpr (C::kPush) {
             const int k = owner(idx);
             *cluster.map_shared_rank(sRecv + rank * per + (idx - k * per), k) = o;
@@ -913,38 +922,54 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         if (tid < ncta) sAllF[tid] = *cluster.map_shared_rank(sFlag, tid);
         __syncthreads();
     }
-    int poison = 0;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
+    // Per row: the cluster max, each CTA's normalised weight (left in sAllM)
+    // and the log-sum-exp.
+    if (tid < rows_here) {
+        const int r = tid;
+        int poison = 0;
+        float M = -CUDART_INF_F;
+#pragma unroll 1
+        for (int c = 0; c < ncta; ++c) {
+            poison |= sAllF[c];
+            M = fmaxf(M, sAllM[r * 16 + c]);
+        }
+        float W = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < ncta; ++c) {
+            const float m = sAllM[r * 16 + c];
+            const float w = (M == -CUDART_INF_F || m == -CUDART_INF_F) ? 0.f : exp2f(m - M);
+            sAllM[r * 16 + c] = w;
+            W = fmaf(w, sAllL[r * 16 + c], W);
+        }
+        const bool zero = poison || W <= 0.f;
+        const float inv = zero ? 0.f : 1.f / W;
+#pragma unroll 1
+        for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] = zero ? 0.f : sAllM[r * 16 + c] * inv;
+        sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+    }
+    __syncthreads();
     const int e0 = rank * per, e1 = min(E, e0 + per);
 #pragma unroll 1
     for (int idx = e0 + tid; idx < e1; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
-        float m[16], l[16], v[16];
+        float v[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-            m[c] = c < ncta ? sAllM[r * 16 + c] : -CUDART_INF_F;
-            l[c] = c < ncta ? sAllL[r * 16 + c] : 0.f;
             if constexpr (C::kPush)
                 v[c] = c < ncta ? sRecv[c * per + (idx - e0)] : 0.f;
             else
                 v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
         }
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) M = fmaxf(M, m[c]);
-        float W = 0.f, o = 0.f;
+        float o = 0.f;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             // A zero weight must not touch its partial: a poisoned one may hold NaN.
-            const float w = (M == -CUDART_INF_F || m[c] == -CUDART_INF_F) ? 0.f : exp2f(m[c] - M);
-            W = fmaf(w, l[c], W);
+            const float w = c < ncta ? sAllM[r * 16 + c] : 0.f;
             o += w != 0.f ? w * v[c] : 0.f;
         }
-        const bool zero = poison || W <= 0.f;
         const long long orow = out_row(r);
-        if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / W;
-        if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+        if (d < p.D) p.out[orow * p.D + d] = o;
+        if (d == 0 && p.lse) p.lse[orow] = sLse[r];
     }
     if constexpr (!C::kPush) cluster.sync();  // partials stay readable until every CTA has merged its slice
 }
