@@ -796,7 +796,8 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
                     *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = v;
                 }
             }
-            fence_proxy_async();
+            // The stage is rewritten by TMA only if it is refilled.
+            if (j + NST < n_mine) fence_proxy_async();
             group_sync();
         }
         if (nrw > 0) {
@@ -922,54 +923,38 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         if (tid < ncta) sAllF[tid] = *cluster.map_shared_rank(sFlag, tid);
         __syncthreads();
     }
-    // Per row: the cluster max, each CTA's normalised weight (left in sAllM)
-    // and the log-sum-exp.
-    if (tid < rows_here) {
-        const int r = tid;
-        int poison = 0;
-        float M = -CUDART_INF_F;
-#pragma unroll 1
-        for (int c = 0; c < ncta; ++c) {
-            poison |= sAllF[c];
-            M = fmaxf(M, sAllM[r * 16 + c]);
-        }
-        float W = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < ncta; ++c) {
-            const float m = sAllM[r * 16 + c];
-            const float w = (M == -CUDART_INF_F || m == -CUDART_INF_F) ? 0.f : exp2f(m - M);
-            sAllM[r * 16 + c] = w;
-            W = fmaf(w, sAllL[r * 16 + c], W);
-        }
-        const bool zero = poison || W <= 0.f;
-        const float inv = zero ? 0.f : 1.f / W;
-#pragma unroll 1
-        for (int c = 0; c < ncta; ++c) sAllM[r * 16 + c] = zero ? 0.f : sAllM[r * 16 + c] * inv;
-        sLse[r] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
-    }
-    __syncthreads();
+    int poison = 0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
     const int e0 = rank * per, e1 = min(E, e0 + per);
 #pragma unroll 1
     for (int idx = e0 + tid; idx < e1; idx += NT) {
         const int r = idx / DP, d = idx - r * DP;
-        float v[16];
+        float m[16], l[16], v[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
+            m[c] = c < ncta ? sAllM[r * 16 + c] : -CUDART_INF_F;
+            l[c] = c < ncta ? sAllL[r * 16 + c] : 0.f;
             if constexpr (C::kPush)
                 v[c] = c < ncta ? sRecv[c * per + (idx - e0)] : 0.f;
             else
                 v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
         }
-        float o = 0.f;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) M = fmaxf(M, m[c]);
+        float W = 0.f, o = 0.f;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             // A zero weight must not touch its partial: a poisoned one may hold NaN.
-            const float w = c < ncta ? sAllM[r * 16 + c] : 0.f;
+            const float w = (M == -CUDART_INF_F || m[c] == -CUDART_INF_F) ? 0.f : exp2f(m[c] - M);
+            W = fmaf(w, l[c], W);
             o += w != 0.f ? w * v[c] : 0.f;
         }
+        const bool zero = poison || W <= 0.f;
         const long long orow = out_row(r);
-        if (d < p.D) p.out[orow * p.D + d] = o;
-        if (d == 0 && p.lse) p.lse[orow] = sLse[r];
+        if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / W;
+        if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
     }
     if constexpr (!C::kPush) cluster.sync();  // partials stay readable until every CTA has merged its slice
 }
