@@ -660,6 +660,22 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             issue(issued);
         }
     }
+    // Pages past the shared-memory stages (up to ~128 KB per key group) are
+    // prefetched into L2 now, so their HBM traffic overlaps the previous
+    // kernel's tail and the later TMA copies hit L2.  Lane l of the group's
+    // first warp holds page l's id.
+    if (mt == 0) {
+        constexpr int kL2Pages = (131072 / (int)C::kStageBytes) > 0 ? 131072 / (int)C::kStageBytes : 1;
+        const int pf_end = min(min(n_mine, 32), NST + kL2Pages);
+        const int bid = id_reg;
+        if (lane >= issued && lane < pf_end && bid >= 0 && (long long)bid < p.num_blocks) {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
+            }
+        }
+    }
     pdl_wait();
     pdl_trigger();
 

@@ -70,6 +70,14 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Bring one 4-D tiled box into L2 without writing shared memory.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a page tile
 // loaded with 128-byte swizzling: the tile is a run of 2 KB boxes (16 rows x
 // 128 B), and inside each 1 KB half the chunk index is XOR-ed with row % 8.
