@@ -141,11 +141,16 @@ struct MmaWarp {
         }
     }
 
-    __device__ void consume(const __nv_bfloat16 *sQ, const unsigned char *sK, const unsigned char *sV,
-                            long long pos0, const int *sLo, const int *sHi, int mt, int lane,
-                            float scale_log2) {
-        // S = Q K^T over the page's 16 keys.
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // NP pages (16 keys each) in one pass: their Q.K^T and P.V products are
+    // independent MMA chains, so two pages cost little more latency than one.
+    template <int NP>
+    __device__ void consume(const __nv_bfloat16 *sQ, const unsigned char *const *sK,
+                            const unsigned char *const *sV, const int *pos0, const int *sLo, const int *sHi,
+                            int mt, int lane, float scale_log2) {
+        constexpr int NT = 2 * NP;  // 8-key column tiles of S
+        float sc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
         const int krow = (lane & 7) + ((lane >> 4) << 3);
         const int kchk = (lane >> 3) & 1;
 #pragma unroll
@@ -156,10 +161,13 @@ struct MmaWarp {
             } else {
                 ldmatrix_x4(a, sQ + (mt * 16 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
             }
-            unsigned b[4];
-            ldmatrix_x4(b, sK + swz(krow, 2 * kk + kchk));
-            mma_bf16_16816(sc[0], a, b[0], b[1]);
-            mma_bf16_16816(sc[1], a, b[2], b[3]);
+#pragma unroll
+            for (int pg = 0; pg < NP; ++pg) {
+                unsigned b[4];
+                ldmatrix_x4(b, sK[pg] + swz(krow, 2 * kk + kchk));
+                mma_bf16_16816(sc[2 * pg], a, b[0], b[1]);
+                mma_bf16_16816(sc[2 * pg + 1], a, b[2], b[3]);
+            }
         }
         // Mask, online softmax (base 2).
         const int t4 = lane & 3;
@@ -167,13 +175,13 @@ struct MmaWarp {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int r = mt * 16 + (lane >> 2) + 8 * e;
-            const long long lo = sLo[r], hi = sHi[r];
+            const int lo = sLo[r], hi = sHi[r];
             float best = -CUDART_INF_F;
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
+            for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    const long long pos = pos0 + n * 8 + 2 * t4 + c;
+                    const int pos = pos0[n >> 1] + (n & 1) * 8 + 2 * t4 + c;
                     float v = sc[n][2 * e + c] * scale_log2;
                     v = (pos >= lo && pos < hi) ? v : -CUDART_INF_F;
                     sc[n][2 * e + c] = v;
@@ -189,7 +197,7 @@ struct MmaWarp {
         }
         float rs[2] = {0.f, 0.f};
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const float pr = exp2f(sc[n][c] - mx[c >> 1]);
@@ -206,19 +214,25 @@ struct MmaWarp {
             }
         }
         // P (bf16, A layout straight from the S accumulators) times V.
-        unsigned pa[4];
-        pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-        pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-        pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-        pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+        unsigned pa[NP][4];
+#pragma unroll
+        for (int pg = 0; pg < NP; ++pg) {
+            pa[pg][0] = pack_bf16x2(sc[2 * pg][0], sc[2 * pg][1]);
+            pa[pg][1] = pack_bf16x2(sc[2 * pg][2], sc[2 * pg][3]);
+            pa[pg][2] = pack_bf16x2(sc[2 * pg + 1][0], sc[2 * pg + 1][1]);
+            pa[pg][3] = pack_bf16x2(sc[2 * pg + 1][2], sc[2 * pg + 1][3]);
+        }
         const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);
         const int vchk = lane >> 4;
 #pragma unroll
         for (int dn = 0; dn < DP / 16; ++dn) {
-            unsigned b[4];
-            ldmatrix_x4_trans(b, sV + swz(vrow, 2 * dn + vchk));
-            mma_bf16_16816(acc[2 * dn], pa, b[0], b[1]);
-            mma_bf16_16816(acc[2 * dn + 1], pa, b[2], b[3]);
+#pragma unroll
+            for (int pg = 0; pg < NP; ++pg) {
+                unsigned b[4];
+                ldmatrix_x4_trans(b, sV[pg] + swz(vrow, 2 * dn + vchk));
+                mma_bf16_16816(acc[2 * dn], pa[pg], b[0], b[1]);
+                mma_bf16_16816(acc[2 * dn + 1], pa[pg], b[2], b[3]);
+            }
         }
     }
 
@@ -764,68 +778,95 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     };
 
     #pragma unroll 1
-    for (int j = 0; j < n_mine; ++j) {
-        wait_page(j);
-        unsigned char *st = gstage + (size_t)(j % NST) * C::kStageBytes;
-        const int pos0 = (cb0 + kw + j * KW) * kPage;
-        // Rows outside [lo_u, kend) may hold anything (NaN included): zero them.
-        // This step's own rows come from k_new / v_new in the fused call, and
-        // the CTA that owns them also writes them into the cache here.
+    // Rows outside [lo_u, kend) may hold anything (NaN included): zero them.
+    // This step's own rows come from k_new / v_new in the fused call, and
+    // the CTA that owns them also writes them into the cache here.
+    auto fix_page = [&](int j, unsigned char *st, int pos0) {
         const int zlo = min(max(lo_u - pos0, 0), kPage);          // rows [0, zlo) precede the window
         const int zhi = min(max(kend - pos0, 0), kPage);          // rows [zhi, 16) are past kv_end
         const int na = fused ? min(max(new_start - pos0, 0), kPage) : zhi;  // rows [na, zhi) are new
-        if (zlo > 0 || zhi < kPage || na < zhi) {
-            const int nz = (zlo + kPage - zhi) * C::kChunks;
+        if (!(zlo > 0 || zhi < kPage || na < zhi)) return;
+        const int nz = (zlo + kPage - zhi) * C::kChunks;
 #pragma unroll 1
-            for (int c = gtid; c < 2 * nz; c += GT) {
-                const int kv = c >= nz, rem = c - kv * nz, o0 = rem / C::kChunks, ch = rem - o0 * C::kChunks;
-                const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
-                *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            const int nn = (zhi - na) * C::kChunks;
-            if (nn > 0) {
-                const bool to_pool = app_ok;
-                const long long bpage = to_pool ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
-                const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;  // slot of the page's first row
-                const bool preloaded = pre_mine && j == last_li / KW && pos0 + na == pre_a;
+        for (int c = gtid; c < 2 * nz; c += GT) {
+            const int kv = c >= nz, rem = c - kv * nz, o0 = rem / C::kChunks, ch = rem - o0 * C::kChunks;
+            const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
+            *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int nn = (zhi - na) * C::kChunks;
+        if (nn > 0) {
+            const bool to_pool = app_ok;
+            const long long bpage = to_pool ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
+            const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;  // slot of the page's first row
+            const bool preloaded = pre_mine && j == last_li / KW && pos0 + na == pre_a;
 #pragma unroll 1
-                for (int c = gtid, it = 0; c < 2 * nn; c += GT, ++it) {
-                    const int kv = c >= nn, rem = c - kv * nn, r0 = rem / C::kChunks, ch = rem - r0 * C::kChunks;
-                    const int o = na + r0;
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (ch < dchunks) {
-                        // the preload enumerated (kv, row, real chunk); map this chunk onto it
-                        const int pc = kv * pre_n * dchunks + r0 * dchunks + ch;
-                        const int q = pc - gtid;
-                        if (preloaded && q >= 0 && q % GT == 0 && q / GT < 2)
-                            v = q == 0 ? pre[0] : pre[1];
-                        else
-                            v = *reinterpret_cast<const uint4 *>(
-                                (kv ? vnew : knew) + (((long long)sg.q0 + (pos0 + o - new_start)) * p.Hkv + g) * p.D +
-                                ch * EPC);
-                        if (to_pool) {
-                            const long long slot = bpage * kPage + (ring_base + o) % kPage;
-                            *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
-                                                       (slot * p.Hkv + g) * p.D + ch * EPC) = v;
-                        }
+            for (int c = gtid; c < 2 * nn; c += GT) {
+                const int kv = c >= nn, rem = c - kv * nn, r0 = rem / C::kChunks, ch = rem - r0 * C::kChunks;
+                const int o = na + r0;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (ch < dchunks) {
+                    // the preload enumerated (kv, row, real chunk); map this chunk onto it
+                    const int pc = kv * pre_n * dchunks + r0 * dchunks + ch;
+                    const int q = pc - gtid;
+                    if (preloaded && q >= 0 && q % GT == 0 && q / GT < 2)
+                        v = q == 0 ? pre[0] : pre[1];
+                    else
+                        v = *reinterpret_cast<const uint4 *>(
+                            (kv ? vnew : knew) + (((long long)sg.q0 + (pos0 + o - new_start)) * p.Hkv + g) * p.D +
+                            ch * EPC);
+                    if (to_pool) {
+                        const long long slot = bpage * kPage + (ring_base + o) % kPage;
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
+                                                   (slot * p.Hkv + g) * p.D + ch * EPC) = v;
                     }
-                    *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = v;
                 }
+                *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = v;
             }
-            // The stage is rewritten by TMA only if it is refilled.
-            if (j + NST < n_mine) fence_proxy_async();
-            group_sync();
+        }
+        // The stage is rewritten by TMA only if it is refilled.
+        if (j + NST < n_mine) fence_proxy_async();
+        group_sync();
+    };
+
+    // Two pages per pass where the ring holds them (independent MMA chains).
+    constexpr int kPair = C::MMA && NST >= 2 ? 2 : 1;
+#pragma unroll 1
+    for (int j = 0; j < n_mine; j += kPair) {
+        const int np = min(kPair, n_mine - j);
+        unsigned char *st[2];
+        int pos0[2];
+#pragma unroll
+        for (int u = 0; u < kPair; ++u) {
+            const int jj = j + min(u, np - 1);
+            st[u] = gstage + (size_t)(jj % NST) * C::kStageBytes;
+            pos0[u] = (cb0 + kw + jj * KW) * kPage;
+        }
+        wait_page(j);
+        fix_page(j, st[0], pos0[0]);
+        if (np > 1) {
+            wait_page(j + 1);
+            fix_page(j + 1, st[1], pos0[1]);
         }
         if (nrw > 0) {
-            if constexpr (C::MMA)
-                mw.consume(reinterpret_cast<const T *>(qarea), st, st + C::kTileBytes, pos0, sLo, sHi, mt, lane,
-                           p.scale_log2);
-            else
-                sw.consume(reinterpret_cast<const float *>(qarea), st, st + C::kTileBytes, pos0, sLo, sHi, mt,
-                           lane, nrw, p.scale_log2, sPw);
+            if constexpr (C::MMA) {
+                const unsigned char *ks[2] = {st[0], st[kPair - 1]};
+                const unsigned char *vs[2] = {st[0] + C::kTileBytes, st[kPair - 1] + C::kTileBytes};
+                if (np == 2)
+                    mw.template consume<2>(reinterpret_cast<const T *>(qarea), ks, vs, pos0, sLo, sHi, mt, lane,
+                                           p.scale_log2);
+                else
+                    mw.template consume<1>(reinterpret_cast<const T *>(qarea), ks, vs, pos0, sLo, sHi, mt, lane,
+                                           p.scale_log2);
+            } else {
+                sw.consume(reinterpret_cast<const float *>(qarea), st[0], st[0] + C::kTileBytes, pos0[0], sLo, sHi,
+                           mt, lane, nrw, p.scale_log2, sPw);
+            }
         }
-        group_sync();  // every warp of the group is done with this stage
-        if (mt == 0 && j + NST < n_mine) issue(j + NST);
+        group_sync();  // every warp of the group is done with these stages
+        if (mt == 0) {
+            if (j + NST < n_mine) issue(j + NST);
+            if (np > 1 && j + 1 + NST < n_mine) issue(j + 1 + NST);
+        }
     }
     if (timed_out && lane == 0 && mt == 0) {
         // Give the copies still in flight a bounded chance to land before the
