@@ -123,7 +123,9 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
     const long long rows_max = (long long)pl->G * max_q_len;
     if (rows_max > (1 << 20)) return PKV_EINVAL;
     pl->rows_max = (int)rows_max;
-    const int rc = rows_max <= 16 ? 0 : rows_max <= 32 ? 1 : rows_max <= 64 ? 2 : 3;
+    // Groups of at most 8 rows take the decode kernel (rows as the MMA's N side).
+    const int rc = (variant == kMmaBf16 && rows_max <= 8) ? 4
+                   : rows_max <= 16 ? 0 : rows_max <= 32 ? 1 : rows_max <= 64 ? 2 : 3;
     pl->k = pick(variant, dp, rc);
     if (!pl->k.fn) return PKV_EUNSUPPORTED;
     pl->row_tiles = (int)((rows_max + pl->k.rows - 1) / pl->k.rows);

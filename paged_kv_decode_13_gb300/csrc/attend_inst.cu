@@ -7,6 +7,7 @@
 // allows (two CTAs per SM), and fp32 / wide heads drop to fewer key groups or
 // a 64-row cap to stay inside the 227 KB limit.
 #include "attend.cuh"
+#include "decode.cuh"
 #include "launch.h"
 
 #ifndef PKV_INST_VARIANT
@@ -25,6 +26,14 @@ static AttnKernel info() {
                       C::kRows, C::DP, C::MMA};
 }
 
+// Decode kernel for groups of at most 8 query rows (row class 4).
+template <class C>
+static AttnKernel dinfo() {
+    static_assert(C::kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
+    return AttnKernel{reinterpret_cast<const void *>(&decode_kernel<C>), C::kThreads, C::kSmemBytes,
+                      C::kRows, C::DP, true};
+}
+
 using B16 = __nv_bfloat16;
 #define CFG(T, MT, KW, NST, MMA) info<AttnCfg<T, PKV_INST_DP, MT, KW, NST, MMA>>()
 
@@ -35,6 +44,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
 #if PKV_INST_VARIANT == 0
 #if PKV_INST_DP == 64
     {
+        if (rc == 4) return dinfo<DecCfg<64, 4, 6>>();
         if (rc == 0) return CFG(B16, 1, 4, 4, true);
         if (rc == 1) return CFG(B16, 2, 2, 4, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);
@@ -42,6 +52,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #elif PKV_INST_DP == 128
     {
+        if (rc == 4) return dinfo<DecCfg<128, 4, 3>>();
         if (rc == 0) return CFG(B16, 1, 4, 3, true);
         if (rc == 1) return CFG(B16, 2, 2, 4, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);
@@ -49,6 +60,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #else
     {
+        if (rc == 4) return dinfo<DecCfg<256, 4, 2>>();
         if (rc == 0) return CFG(B16, 1, 4, 2, true);
         if (rc == 1) return CFG(B16, 2, 2, 3, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);

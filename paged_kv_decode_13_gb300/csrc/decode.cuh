@@ -1,0 +1,555 @@
+// Split-K decode attention for narrow query groups (sm_103a).
+//
+// Same semantics and launch shape as attend_kernel (grid (C, kv_heads,
+// segments), the C CTAs of a (segment, kv head) forming one cluster), for the
+// decode case where a kv head's query group has at most 8 rows (G * q_len <=
+// 8: one token of a GQA group, or a few tokens of a narrow group).  Such a
+// group is too narrow for the 16-row side of an MMA tile, so the products are
+// taken transposed, with the query rows as the 8-wide N side:
+//
+//   S^T (16 keys x 8 rows)   = K (16 keys x D) . Q^T        keys as M
+//   O^T (D x 8 rows)        += V^T (D x 16 keys) . P^T      head_dim as M
+//
+// Q^T stays in registers as B fragments for the whole key range; P^T comes
+// from the S^T accumulators through one in-register 8x8 transpose
+// (movmatrix) per half page.  Every MMA row is a real key or a real head_dim
+// column, where a 16-row query tile would leave 12 of its 16 rows empty for
+// the common 4-head group.
+//
+// Each warp is a key group with its own ring of NST page stages (TMA,
+// 128-byte swizzle, one mbarrier per stage) and takes every KW-th page of the
+// CTA's range.  At the end the warps merge in shared memory (each writes its
+// partial over its own, now idle, stages) and the CTAs merge through
+// distributed shared memory: every CTA pushes its merged partial for each
+// output slice straight into the shared memory of the CTA that owns that
+// slice, one cluster barrier later the owner finishes its slice.
+//
+// Semantics follow the segment-table attention of ExecuTorch PR #24072
+// (triton::sdpa_varlen) over the paged layout of vLLM-Omni's SenseNova-U1
+// PagedDecodeCache, exactly as attend_kernel.
+#pragma once
+
+#include "attend.cuh"
+
+namespace pkv {
+
+template <int DP_, int KW_, int NST_>
+struct DecCfg {
+    using T = __nv_bfloat16;
+    static constexpr int DP = DP_;      // head_dim rounded up to 64 / 128 / 256
+    static constexpr int KW = KW_;      // warps = key groups
+    static constexpr int NST = NST_;    // page stages per warp
+    static constexpr int kThreads = KW * 32;
+    static constexpr int kRows = 8;                      // query rows per CTA (the MMA N side)
+    static constexpr int kKT = DP / 16;                  // 16-wide steps over head_dim
+    static constexpr int kEpc = 8;                       // bf16 elements per 16-byte chunk
+    static constexpr int kChunks = DP / kEpc;
+    static constexpr int kBoxEl = 64;                    // elements per 128-byte swizzle box row
+    static constexpr int kBoxes = DP / kBoxEl;
+    static constexpr unsigned kTileBytes = kPage * DP * 2;
+    static constexpr unsigned kStageBytes = 2 * kTileBytes;
+    static constexpr size_t kPipeBytes = (size_t)KW * NST * kStageBytes;
+    static constexpr int kPartLd = DP + 4;               // padded row of a warp's partial (bank spread)
+    static constexpr size_t kPartBytes = (size_t)kRows * kPartLd * 4 + 2 * kRows * 4;
+    // Pushed by the cluster: C CTAs x 8 rows x ceil(DP / C) columns, at most
+    // 8 * (DP + 15) floats for C <= 16; then (max, sum) per CTA and row.
+    static constexpr int kRecvLd = DP + 16;
+    static constexpr size_t kRecvBytes = (size_t)kRows * kRecvLd * 4;
+    static constexpr size_t kStatBytes = (size_t)16 * kRows * 8;
+    static constexpr size_t kBarBytes = (size_t)KW * NST * 8;
+    static constexpr size_t kFlagBytes = 32 * 4;
+    static constexpr size_t kCovBytes = (size_t)kThreads * 4;
+    static constexpr size_t kSmemBytes =
+        1024 + kPipeBytes + kRecvBytes + kStatBytes + kBarBytes + kFlagBytes + kCovBytes;
+    static_assert(kPartBytes <= NST * kStageBytes, "a warp's partial fits over its own stages");
+    static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
+};
+
+// Transpose of the 8x8 bf16 matrix whose row lane/4, columns 2*(lane%4) and
+// 2*(lane%4)+1 this thread holds.
+__device__ __forceinline__ unsigned movmatrix_trans(unsigned x) {
+    unsigned y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_constant__ AttendParams p) {
+    using T = __nv_bfloat16;
+    namespace cg = cooperative_groups;
+    constexpr int DP = C::DP, KW = C::KW, NST = C::NST, NT = C::kThreads, KT = C::kKT, LD = C::kPartLd;
+    constexpr int EPC = C::kEpc;
+    constexpr float kLn2 = 0.6931471805599453f;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *pipe = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *sRecv = reinterpret_cast<float *>(pipe + C::kPipeBytes);      // [ncta][8][per]
+    float2 *sStat = reinterpret_cast<float2 *>(sRecv + C::kRows * C::kRecvLd);  // [16][8] (max, sum)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sStat + 16 * C::kRows);  // [KW][NST]
+    int *sFlag = reinterpret_cast<int *>(bars + KW * NST);  // [0] own flags: 1 bad page, 2 timeout
+    int *sAllF = sFlag + 1;                                 // [16] flags of the cluster
+    int *sCov = sFlag + 32;                                 // [NT] coverage flags of the first rows
+
+    const int tid = threadIdx.x, kw = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
+    const int rank = blockIdx.x, ncta = gridDim.x;
+    const int g = blockIdx.y;  // one CTA row per kv head: the whole group fits the 8 rows
+    const int s = blockIdx.z;
+    const bool first_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+
+    // Rows no segment covers: scanned before the dependency wait, zeroed after.
+    int cov_any = 0;
+    if (first_cta) {
+        int f = 0;
+        if (tid < p.total_rows) {
+            int cnt = 0;
+            #pragma unroll 1
+            for (int s2 = 0; s2 < p.S; ++s2) {
+                const Segment o = load_segment(p.seq_info, s2);
+                if (o.q0 >= 0 && o.ql > 0 && tid >= o.q0 && (long long)tid < (long long)o.q0 + o.ql) ++cnt;
+            }
+            f = (cnt == 0 ? 1 : 0) | (cnt > 1 ? 2 : 0);
+        }
+        sCov[tid] = f;
+        cov_any = __syncthreads_or(f != 0);
+    }
+    if (p.S == 0) {
+        pdl_wait();
+        pdl_trigger();
+        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+        return;
+    }
+
+    // ---- segment and its key range (reads allowed before the dependency wait)
+    const Segment sg = load_segment(p.seq_info, s);
+    unsigned fault = segment_fault(sg, p.total_rows, p.max_seqs, p.mbps, p.ring_rows, p.window);
+    if (!fault && sg.ql > p.max_q_len) fault = PKV_ERR_QLEN;
+    const int rows_unit = fault ? 0 : sg.ql * p.G;  // <= 8: max_q_len * G <= 8 selects this kernel
+    if (fault || rows_unit == 0) {  // uniform across the cluster
+        pdl_wait();
+        pdl_trigger();
+        if (fault && rank == 0) {
+            if (tid == 0) atomicOr(p.err, fault);
+            zero_segment_rows(p, sg, g, NT);
+        }
+        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+        return;
+    }
+    if (ncta > 1)  // announce this CTA to the cluster; waited on before any remote store
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+    const int kend = sg.kend;
+    const int new_start = kend - sg.ql;
+    int lo_u = 0;
+    if (p.window > 0) lo_u = max(0, (p.causal ? new_start : kend - 1) - p.window + 1);
+    const int pb_begin = lo_u / kPage;
+    const int pb_end = (kend + kPage - 1) / kPage;
+    const int nblk = pb_end - pb_begin;
+    const int bps = (nblk + ncta - 1) / ncta;
+    const int active = (nblk + bps - 1) / bps;
+    const int cb0 = pb_begin + rank * bps;
+    const int nb = rank < active ? min(cb0 + bps, pb_end) - cb0 : 0;
+    const int n_mine = nb > kw ? (nb - kw + KW - 1) / KW : 0;
+
+    const T *knew = reinterpret_cast<const T *>(p.k_new);
+    const T *vnew = reinterpret_cast<const T *>(p.v_new);
+    const bool fused = knew != nullptr;
+    const int dchunks = p.D / EPC;
+    const int *bt_row = p.block_table + (long long)sg.col * p.mbps;
+    uint64_t *wbars = bars + kw * NST;
+    unsigned char *wstage = pipe + (size_t)kw * NST * C::kStageBytes;
+    const int lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
+    const bool has_new = fused && nb > 0 && new_start < hi_pos && kend > lo_pos;
+
+    if (lane == 0) {
+        #pragma unroll 1
+        for (int i = 0; i < NST; ++i) mbar_init(wbars + i, 1);
+        fence_barrier_init();
+    }
+    if (tid == 0) sFlag[0] = 0;
+    __syncthreads();
+
+    // ---- page ids and TMA issue (lane l of the warp holds the id of its page window + l)
+    int id_reg = -1, id_window = -1;
+    bool bad = false, timed_out = false;
+    auto load_ids = [&](int j) {
+        id_window = j & ~31;
+        const int li = kw + (id_window + lane) * KW;
+        id_reg = -1;
+        if (li < nb) id_reg = bt_row[table_page(cb0 + li, p.ring_rows)];
+    };
+    auto issue = [&](int j) {
+        if ((j & ~31) != id_window) load_ids(j);
+        const int bid = __shfl_sync(0xffffffffu, id_reg, j & 31);
+        const bool ok = bid >= 0 && (long long)bid < p.num_blocks;
+        bad |= !ok;
+        if (lane == 0) {
+            uint64_t *bar = wbars + (j % NST);
+            unsigned char *st = wstage + (size_t)(j % NST) * C::kStageBytes;
+            if (ok) {
+                fence_proxy_async();
+                mbar_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+                for (int b = 0; b < C::kBoxes; ++b) {
+                    tma_load_4d(st + b * 2048, &p.tmap_k, bar, b * C::kBoxEl, g, 0, bid);
+                    tma_load_4d(st + C::kTileBytes + b * 2048, &p.tmap_v, bar, b * C::kBoxEl, g, 0, bid);
+                }
+            } else {
+                mbar_arrive(bar);  // nothing to fetch: complete the phase, the result is discarded
+            }
+        }
+    };
+    // Pages wholly below new_start were written before this step and may be
+    // fetched before the dependency wait; in the fused call every page may
+    // (the step's own rows are replaced from k_new / v_new after it).
+    auto early_ok = [&](int j) { return fused || (cb0 + kw + j * KW + 1) * kPage <= new_start; };
+    // Bounded wait for the warp's j-th page; every lane observes the phase.
+    auto wait_page = [&](int j) {
+        if (timed_out) return;
+        bool done = false;
+        #pragma unroll 1
+        for (int it = 0; it < kWaitProbes && !done; ++it) done = mbar_try_wait(wbars + (j % NST), (j / NST) & 1);
+        if (!__all_sync(0xffffffffu, done)) timed_out = true;
+    };
+
+    int issued = 0;
+    load_ids(0);
+    #pragma unroll 1
+    for (; issued < NST && issued < n_mine; ++issued) {
+        if (!early_ok(issued)) break;
+        issue(issued);
+    }
+    // Later pages (up to ~128 KB per warp) go to L2 now, so their HBM traffic
+    // overlaps the previous kernel's tail.
+    {
+        constexpr int kL2Pages = (131072 / (int)C::kStageBytes) > 0 ? 131072 / (int)C::kStageBytes : 1;
+        const int pf_end = min(min(n_mine, 32), NST + kL2Pages);
+        const int bid = id_reg;
+        if (lane >= issued && lane < pf_end && bid >= 0 && (long long)bid < p.num_blocks) {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
+            }
+        }
+    }
+    // Append validity (all-or-nothing over the segment's new rows): the block
+    // table is not written by the previous kernel.
+    bool app_ok = false;
+    if (has_new) {
+        bool ok = true;
+        #pragma unroll 1
+        for (int i = lane; i < sg.ql; i += 32) {
+            const int pos = new_start + i;
+            const int rr = p.ring_rows ? pos % p.ring_rows : pos;
+            const int b = bt_row[rr / kPage];
+            ok &= b >= 0 && (long long)b < p.num_blocks;
+        }
+        app_ok = __all_sync(0xffffffffu, ok);
+    }
+    // Warm L2 with what is read right after the wait: the group's query rows
+    // and this step's K/V rows.
+    if (kw == 0) {
+        const int lines = (p.D * 2 + 127) / 128;
+        #pragma unroll 1
+        for (int c = lane; c < rows_unit * lines; c += 32) {
+            const int r = c / lines, ln = c - r * lines, i = r / p.G, jh = r - i * p.G;
+            const T *src = reinterpret_cast<const T *>(p.q) + (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D;
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + ln * 128));
+        }
+    }
+    if (has_new && kw == 1 % KW) {
+        const int lines = (p.D * 2 + 127) / 128;
+        const int a = max(new_start, lo_pos), e = min(kend, hi_pos);
+        #pragma unroll 1
+        for (int c = lane; c < (e - a) * 2 * lines; c += 32) {
+            const int row = c / (2 * lines), rem = c - row * 2 * lines, kv = rem / lines, ln = rem - kv * lines;
+            const T *src = (kv ? vnew : knew) + (((long long)sg.q0 + (a + row - new_start)) * p.Hkv + g) * p.D;
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + ln * 128));
+        }
+    }
+
+    pdl_wait();
+    pdl_trigger();
+
+    // ---- after the wait: Q^T fragments, this step's new rows, row bounds
+    unsigned qb[KT][2];
+    {
+        const bool real = gq < rows_unit;
+        const int i = gq / p.G, jh = gq - i * p.G;
+        const T *qrow = reinterpret_cast<const T *>(p.q) +
+                        (((long long)sg.q0 + (real ? i : 0)) * p.Hq + (long long)g * p.G + (real ? jh : 0)) * p.D;
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            const int d0 = kk * 16 + 2 * tq, d1 = d0 + 8;
+            qb[kk][0] = real && d0 < p.D ? *reinterpret_cast<const unsigned *>(qrow + d0) : 0u;
+            qb[kk][1] = real && d1 < p.D ? *reinterpret_cast<const unsigned *>(qrow + d1) : 0u;
+        }
+    }
+    // The step's rows in the warp's last page (decode: the one new row),
+    // loaded beside the queries; the page fix-up stores them.
+    const int last_li = nb - 1, last_pos0 = (cb0 + last_li) * kPage;
+    const int pre_a = max(new_start, last_pos0), pre_n = has_new ? max(0, kend - pre_a) : 0;
+    const bool pre_mine = pre_n > 0 && kw == last_li % KW;
+    uint4 pre[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        pre[it] = make_uint4(0u, 0u, 0u, 0u);
+        const int c = lane + it * 32;
+        if (pre_mine && c < 2 * pre_n * dchunks) {
+            const int kv = c / (pre_n * dchunks), rem = c - kv * pre_n * dchunks;
+            const int row = rem / dchunks, ch = rem - row * dchunks;
+            pre[it] = *reinterpret_cast<const uint4 *>((kv ? vnew : knew) +
+                                                       (((long long)sg.q0 + (pre_a + row - new_start)) * p.Hkv + g) * p.D +
+                                                       ch * EPC);
+        }
+    }
+    // Key bounds of the two rows this thread's fragments hold (2tq, 2tq+1);
+    // padding rows see no key.
+    int lo_r[2], hi_r[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int n = 2 * tq + e;
+        lo_r[e] = 0;
+        hi_r[e] = 0;
+        if (n < rows_unit) {
+            const int pos = new_start + n / p.G;
+            const int newest = p.causal ? pos : kend - 1;
+            hi_r[e] = p.causal ? pos + 1 : kend;
+            lo_r[e] = p.window > 0 ? max(0, newest - p.window + 1) : 0;
+        }
+    }
+    if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+    #pragma unroll 1
+    for (; issued < NST && issued < n_mine; ++issued) issue(issued);
+
+    // ---- main loop over the warp's pages
+    float acc[KT][4];
+#pragma unroll
+    for (int dt = 0; dt < KT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+    float m_r[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_r[2] = {0.f, 0.f};
+    const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), kchk = lane >> 4;
+    const int vrow = (lane & 7) + ((lane >> 4) << 3), vchk = (lane >> 3) & 1;
+
+    // Rows outside [lo_u, kend) may hold anything (NaN included): their V rows
+    // are zeroed (their scores are masked).  This step's own rows come from
+    // k_new / v_new in the fused call, and the warp that holds them also
+    // writes them into the cache.
+    auto fix_page = [&](int j, unsigned char *st, int pos0) {
+        const int zlo = min(max(lo_u - pos0, 0), kPage);
+        const int zhi = min(max(kend - pos0, 0), kPage);
+        const int na = fused ? min(max(new_start - pos0, 0), kPage) : zhi;
+        if (!(zlo > 0 || zhi < kPage || na < zhi)) return;
+        const int nz = (zlo + kPage - zhi) * C::kChunks;
+        #pragma unroll 1
+        for (int c = lane; c < nz; c += 32) {
+            const int o0 = c / C::kChunks, ch = c - o0 * C::kChunks;
+            const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
+            *reinterpret_cast<uint4 *>(st + C::kTileBytes + swz(o, ch)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int nnr = zhi - na;  // new rows in this page
+        if (nnr > 0) {
+            const long long bpage = app_ok ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
+            const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;
+            const bool preloaded = pre_mine && j == last_li / KW && pos0 + na == pre_a;
+            const int nn = nnr * dchunks;
+            #pragma unroll 1
+            for (int it = 0; it * 32 < 2 * nn; ++it) {
+                const int c = lane + it * 32;
+                if (c < 2 * nn) {
+                    const int kv = c / nn, rem = c - kv * nn, r0 = rem / dchunks, ch = rem - r0 * dchunks;
+                    const int o = na + r0;
+                    uint4 v;
+                    if (preloaded && it < 2)
+                        v = it == 0 ? pre[0] : pre[1];
+                    else
+                        v = *reinterpret_cast<const uint4 *>(
+                            (kv ? vnew : knew) + (((long long)sg.q0 + (pos0 + o - new_start)) * p.Hkv + g) * p.D +
+                            ch * EPC);
+                    if (app_ok) {
+                        const long long slot = bpage * kPage + (ring_base + o) % kPage;
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
+                                                   (slot * p.Hkv + g) * p.D + ch * EPC) = v;
+                    }
+                    *reinterpret_cast<uint4 *>(st + kv * C::kTileBytes + swz(o, ch)) = v;
+                }
+            }
+        }
+        if (j + NST < n_mine) fence_proxy_async();  // the stage is rewritten by TMA only if refilled
+        __syncwarp();
+    };
+
+    #pragma unroll 1
+    for (int j = 0; j < n_mine; ++j) {
+        unsigned char *st = wstage + (size_t)(j % NST) * C::kStageBytes;
+        const int pos0 = (cb0 + kw + j * KW) * kPage;
+        wait_page(j);
+        fix_page(j, st, pos0);
+        // S^T = K . Q^T, two accumulation chains over head_dim.
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            unsigned a[4];
+            ldmatrix_x4(a, st + swz(krow, 2 * kk + kchk));
+            if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
+            else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
+        }
+        // This thread holds keys gq, gq + 8 of rows 2tq, 2tq + 1: mask, online softmax (base 2).
+        const int p0 = pos0 + gq, p1 = p0 + 8;
+        float v[4];
+        v[0] = (p0 >= lo_r[0] && p0 < hi_r[0]) ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
+        v[1] = (p0 >= lo_r[1] && p0 < hi_r[1]) ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
+        v[2] = (p1 >= lo_r[0] && p1 < hi_r[0]) ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
+        v[3] = (p1 >= lo_r[1] && p1 < hi_r[1]) ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
+        float mx0 = fmaxf(v[0], v[2]), mx1 = fmaxf(v[1], v[3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
+        const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0, mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+        const float al0 = exp2f(m_r[0] - mu0), al1 = exp2f(m_r[1] - mu1);
+        m_r[0] = mn0;
+        m_r[1] = mn1;
+        const float p00 = exp2f(v[0] - mu0), p01 = exp2f(v[1] - mu1);
+        const float p10 = exp2f(v[2] - mu0), p11 = exp2f(v[3] - mu1);
+        l_r[0] = fmaf(l_r[0], al0, p00 + p10);
+        l_r[1] = fmaf(l_r[1], al1, p01 + p11);
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int dt = 0; dt < KT; ++dt) {
+                acc[dt][0] *= al0; acc[dt][1] *= al1;
+                acc[dt][2] *= al0; acc[dt][3] *= al1;
+            }
+        }
+        // P^T as B fragments: transpose the (key x row) halves in registers.
+        const unsigned b0 = movmatrix_trans(pack_bf16x2(p00, p01));
+        const unsigned b1 = movmatrix_trans(pack_bf16x2(p10, p11));
+        // O^T += V^T . P^T, one independent MMA per 16 columns of head_dim.
+        const unsigned char *sv = st + C::kTileBytes;
+#pragma unroll
+        for (int dt = 0; dt < KT; ++dt) {
+            unsigned a[4];
+            ldmatrix_x4_trans(a, sv + swz(vrow, 2 * dt + vchk));
+            mma_bf16_16816(acc[dt], a, b0, b1);
+        }
+        __syncwarp();  // every lane is done with the stage
+        if (j + NST < n_mine) issue(j + NST);
+    }
+    if (timed_out && lane == 0) {
+        // Give copies still in flight a bounded chance to land before the
+        // stage memory is reused.
+        #pragma unroll 1
+        for (int j = max(0, n_mine - NST); j < n_mine; ++j)
+            #pragma unroll 1
+            for (int it = 0; it < kWaitProbes && !mbar_try_wait(wbars + (j % NST), (j / NST) & 1); ++it) {
+            }
+    }
+    if ((bad || timed_out) && lane == 0) atomicOr(sFlag, (bad ? 1 : 0) | (timed_out ? 2 : 0));
+
+    // ---- the warp's partial, written over its own stages: O^T as [row][col], max and sum per row
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], o);
+        l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], o);
+    }
+    {
+        float *part = reinterpret_cast<float *>(wstage);
+        float *pm = part + C::kRows * LD, *pl = pm + C::kRows;
+#pragma unroll
+        for (int dt = 0; dt < KT; ++dt) {
+            const int d = dt * 16 + gq;
+            part[(2 * tq) * LD + d] = acc[dt][0];
+            part[(2 * tq + 1) * LD + d] = acc[dt][1];
+            part[(2 * tq) * LD + d + 8] = acc[dt][2];
+            part[(2 * tq + 1) * LD + d + 8] = acc[dt][3];
+        }
+        if (gq == 0) {
+            pm[2 * tq] = m_r[0];
+            pm[2 * tq + 1] = m_r[1];
+            pl[2 * tq] = l_r[0];
+            pl[2 * tq + 1] = l_r[1];
+        }
+    }
+    __syncthreads();
+    const int flags = sFlag[0];
+    if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
+
+    auto out_row = [&](int n) {
+        const int i = n / p.G, jh = n - i * p.G;
+        return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
+    };
+    cg::cluster_group cluster = cg::this_cluster();
+    const int per = (DP + ncta - 1) / ncta;  // output columns each CTA of the cluster finishes
+    if (ncta > 1) {
+        // Every CTA of the cluster has started (the arrive at the top), so
+        // peers' shared memory may be written from here on.
+        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+        if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+    }
+    // Merge the warps element by element; finish the element here when the
+    // CTA is alone, otherwise push it to the CTA that finishes its columns.
+    #pragma unroll 1
+    for (int idx = tid; idx < rows_unit * DP; idx += NT) {
+        const int n = idx / DP, d = idx - n * DP;
+        float mk[KW], M = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) {
+            mk[k] = reinterpret_cast<const float *>(pipe + (size_t)k * NST * C::kStageBytes)[C::kRows * LD + n];
+            M = fmaxf(M, mk[k]);
+        }
+        float L = 0.f, o = 0.f;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) {
+            const float *part = reinterpret_cast<const float *>(pipe + (size_t)k * NST * C::kStageBytes);
+            // a warp with no visible key has weight 0 and a zero accumulator
+            const float w = (M == -CUDART_INF_F || mk[k] == -CUDART_INF_F) ? 0.f : exp2f(mk[k] - M);
+            L = fmaf(w, part[C::kRows * LD + C::kRows + n], L);
+            o = fmaf(w, part[n * LD + d], o);
+        }
+        if (ncta == 1) {
+            const long long orow = out_row(n);
+            const bool zero = flags || L <= 0.f;
+            if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / L;
+            if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
+        } else {
+            const int k = d / per, dl = d - k * per;
+            *cluster.map_shared_rank(sRecv + (rank * C::kRows + n) * per + dl, k) = o;
+            if (dl == 0) *cluster.map_shared_rank(sStat + rank * C::kRows + n, k) = make_float2(M, L);
+        }
+    }
+    if (ncta == 1) return;
+
+    // ---- merge the cluster's partials of this CTA's columns
+    cluster.sync();  // publishes every CTA's pushed partials
+    int poison = 0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
+    #pragma unroll 1
+    for (int idx = tid; idx < rows_unit * per; idx += NT) {
+        const int n = idx / per, dl = idx - n * per, d = rank * per + dl;
+        if (d >= DP) continue;  // the last CTA's slice may be short
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            if (c < ncta) M = fmaxf(M, sStat[c * C::kRows + n].x);
+        float W = 0.f, o = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            if (c < ncta) {
+                const float2 st = sStat[c * C::kRows + n];
+                // A zero weight must not touch its partial: a poisoned one may hold NaN.
+                const float w = (M == -CUDART_INF_F || st.x == -CUDART_INF_F) ? 0.f : exp2f(st.x - M);
+                W = fmaf(w, st.y, W);
+                o += w != 0.f ? w * sRecv[(c * C::kRows + n) * per + dl] : 0.f;
+            }
+        }
+        const bool zero = poison || W <= 0.f;
+        const long long orow = out_row(n);
+        if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / W;
+        if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+    }
+}
+
+}  // namespace pkv
