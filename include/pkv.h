@@ -68,6 +68,7 @@ typedef enum pkv_dtype { PKV_BF16 = 0, PKV_F32 = 1 } pkv_dtype;
 /* Flags for the attention calls. */
 #define PKV_FLAG_SIMT  (1u << 0)  /* bf16: use the CUDA-core kernel instead of the tensor-core one */
 #define PKV_FLAG_PDL   (1u << 1)  /* launch with programmatic dependent launch; see pkv_attend_varlen */
+#define PKV_FLAG_PREFETCH_NEXT (1u << 2)  /* warm L2 with layer + 1's pages; see pkv_attend_varlen */
 
 /*
  * One paged K/V cache: per layer, a K pool and a V pool, each
@@ -180,7 +181,11 @@ int pkv_append(const pkv_cache *cache, int32_t layer,
  * the block table and seq_info while the previous kernel on the stream is
  * still running, so set it only when that previous kernel writes none of
  * those; q, k_new, v_new, out, lse and err_flags are touched only after it
- * has finished.
+ * has finished.  PKV_FLAG_PREFETCH_NEXT (ignored for the last layer) also
+ * brings into L2 the pages of layer + 1 that cover the same key ranges, for
+ * a caller whose next call attends layer + 1 with the same block table and
+ * segments (one decode step): a hint only, it changes no result.  The
+ * prefetch is capped at about 48 MB per call.
  *
  * Device pointers must be 16-byte aligned (out and lse: 4-byte).
  */

@@ -139,6 +139,12 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
         n = 1;
         while (n < want && n < kMaxCluster) n *= 2;
     }
+    if (rc == 4 && num_splits == 0) {
+        // decode kernel: no more CTAs than keep each of their 4 warps a page
+        long long cap = 1;
+        while (cap * 2 <= max_pages / 4 && cap * 2 <= kMaxCluster) cap *= 2;
+        n = std::min(n, cap);
+    }
     n = std::max<long long>(1, std::min<long long>(n, max_pages));
     pl->ncta = (int)n;
     return PKV_OK;
@@ -256,6 +262,16 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     p.causal = causal;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.pf_next = 0;
+    if ((flags & PKV_FLAG_PREFETCH_NEXT) && layer + 1 < c->num_layers && S > 0 && !check_layer(c, layer + 1)) {
+        if ((st = encode_pool(&p.tmap_k_next, c->k[layer + 1], c)) ||
+            (st = encode_pool(&p.tmap_v_next, c->v[layer + 1], c)))
+            return st;
+        // L2 budget: ~48 MB over every warp of the launch.
+        const long long warps = (long long)ncta * c->kv_heads * pl.row_tiles * S * (pl.k.threads / 32);
+        const long long stage = 2LL * PKV_BLOCK_SIZE * pl.k.dp * elem_bytes(c->dtype);
+        p.pf_next = (int)std::max<long long>(0, std::min<long long>(32, (48LL << 20) / (warps * stage)));
+    }
 
     cudaLaunchConfig_t cfg = {};
     if (S == 0)

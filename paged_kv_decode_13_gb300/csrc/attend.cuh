@@ -777,7 +777,6 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         if constexpr (MT == 1) __syncwarp(); else named_barrier(1 + kw, GT);
     };
 
-    #pragma unroll 1
     // Rows outside [lo_u, kend) may hold anything (NaN included): zero them.
     // This step's own rows come from k_new / v_new in the fused call, and
     // the CTA that owns them also writes them into the cache here.

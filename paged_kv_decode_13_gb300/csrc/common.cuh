@@ -154,6 +154,11 @@ struct AttendParams {
     int row_tiles;          // CTAs along the rows of one (segment, kv head)
     int causal, window;
     float scale_log2;       // softmax_scale * log2(e)
+    // Optional L2 warm-up of the next layer's pages of the same key ranges
+    // (the next call reads the same table and segments): pages per warp, 0 = off.
+    int pf_next;
+    CUtensorMap tmap_k_next;
+    CUtensorMap tmap_v_next;
 };
 
 struct AppendParams {

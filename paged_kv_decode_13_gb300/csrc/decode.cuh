@@ -51,16 +51,18 @@ struct DecCfg {
     static constexpr size_t kPipeBytes = (size_t)KW * NST * kStageBytes;
     static constexpr int kPartLd = DP + 4;               // padded row of a warp's partial (bank spread)
     static constexpr size_t kPartBytes = (size_t)kRows * kPartLd * 4 + 2 * kRows * 4;
-    // Pushed by the cluster: C CTAs x 8 rows x ceil(DP / C) columns, at most
-    // 8 * (DP + 15) floats for C <= 16; then (max, sum) per CTA and row.
-    static constexpr int kRecvLd = DP + 16;
+    // Pushed by the cluster: C CTAs x 8 rows x per columns (per = the power
+    // of two >= DP / C, so C * per < 2 * DP); then (max, sum) per CTA and row.
+    static constexpr int kRecvLd = 2 * DP;
     static constexpr size_t kRecvBytes = (size_t)kRows * kRecvLd * 4;
+    static constexpr size_t kWnBytes = (size_t)kRows * 16 * 4 + kRows * 4;  // merge weights, lse per row
     static constexpr size_t kStatBytes = (size_t)16 * kRows * 8;
     static constexpr size_t kBarBytes = (size_t)KW * NST * 8;
     static constexpr size_t kFlagBytes = 32 * 4;
     static constexpr size_t kCovBytes = (size_t)kThreads * 4;
     static constexpr size_t kSmemBytes =
-        1024 + kPipeBytes + kRecvBytes + kStatBytes + kBarBytes + kFlagBytes + kCovBytes;
+        1024 + kPipeBytes + kRecvBytes + kStatBytes + kBarBytes + kFlagBytes + kCovBytes + kWnBytes;
+    static_assert(kThreads == 128, "the cluster merge maps 8 rows x 16 CTAs onto the threads");
     static_assert(kPartBytes <= NST * kStageBytes, "a warp's partial fits over its own stages");
     static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
 };
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     int *sFlag = reinterpret_cast<int *>(bars + KW * NST);  // [0] own flags: 1 bad page, 2 timeout
     int *sAllF = sFlag + 1;                                 // [16] flags of the cluster
     int *sCov = sFlag + 32;                                 // [NT] coverage flags of the first rows
+    float *sWn = reinterpret_cast<float *>(sCov + NT);      // [8][16] normalised cluster merge weights
+    float *sLseR = sWn + C::kRows * 16;                     // [8] lse per row
 
     const int tid = threadIdx.x, kw = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
@@ -230,6 +234,18 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
             for (int b = 0; b < C::kBoxes; ++b) {
                 tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
                 tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
+            }
+        }
+    }
+    // The next layer's pages of the same range (same table and segments), so
+    // its HBM traffic runs under this layer's compute.
+    if (p.pf_next > 0) {
+        const int bid = id_reg;
+        if (lane < min(n_mine, p.pf_next) && bid >= 0 && (long long)bid < p.num_blocks) {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_4d(&p.tmap_k_next, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(&p.tmap_v_next, b * C::kBoxEl, g, 0, bid);
             }
         }
     }
@@ -480,43 +496,73 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         const int i = n / p.G, jh = n - i * p.G;
         return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
     };
+    auto part_of = [&](int k) { return reinterpret_cast<const float *>(pipe + (size_t)k * NST * C::kStageBytes); };
+
+    // Merge weights of the warps' partials, row by row: every warp computes
+    // them in its lanes (lane n * KW + k: warp k's weight for row n, plus the
+    // row's max and sum) and hands them out by shuffles.
+    float wk, Mr, Lr;
+    {
+        const int n = lane / KW, k = lane - n * KW;
+        float mk = -CUDART_INF_F, lk = 0.f;
+        if (lane < C::kRows * KW) {
+            mk = part_of(k)[C::kRows * LD + n];
+            lk = part_of(k)[C::kRows * LD + C::kRows + n];
+        }
+        Mr = mk;
+#pragma unroll
+        for (int o = 1; o < KW; o <<= 1) Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, o));
+        // a warp with no visible key has weight 0 and a zero accumulator
+        wk = (Mr == -CUDART_INF_F || mk == -CUDART_INF_F) ? 0.f : exp2f(mk - Mr);
+        Lr = wk * lk;
+#pragma unroll
+        for (int o = 1; o < KW; o <<= 1) Lr += __shfl_xor_sync(0xffffffffu, Lr, o);
+    }
+
     cg::cluster_group cluster = cg::this_cluster();
-    const int per = (DP + ncta - 1) / ncta;  // output columns each CTA of the cluster finishes
+    // Output columns each CTA of the cluster finishes: a power of two, so the
+    // last CTAs may get none.
+    int lg = 0;
+    while ((1 << lg) * ncta < DP) ++lg;
+    const int per = 1 << lg;
     if (ncta > 1) {
         // Every CTA of the cluster has started (the arrive at the top), so
         // peers' shared memory may be written from here on.
         asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
         if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+        {   // (max, sum) of each row to every CTA that finishes columns
+            const int n = tid & 7, k = tid >> 3;
+            const float Mn = __shfl_sync(0xffffffffu, Mr, n * KW), Ln = __shfl_sync(0xffffffffu, Lr, n * KW);
+            if (k < ncta && n < rows_unit) *cluster.map_shared_rank(sStat + rank * C::kRows + n, k) = make_float2(Mn, Ln);
+        }
     }
-    // Merge the warps element by element; finish the element here when the
-    // CTA is alone, otherwise push it to the CTA that finishes its columns.
-    #pragma unroll 1
-    for (int idx = tid; idx < rows_unit * DP; idx += NT) {
-        const int n = idx / DP, d = idx - n * DP;
-        float mk[KW], M = -CUDART_INF_F;
+    // Element pass: thread = column (x CPT) and a set of rows.
+    constexpr int CW = DP < NT ? DP : NT, CPT = DP / CW, RS = NT / CW, RPT = C::kRows / RS;
+    const int c0 = tid % CW, r0 = tid / CW;
 #pragma unroll
-        for (int k = 0; k < KW; ++k) {
-            mk[k] = reinterpret_cast<const float *>(pipe + (size_t)k * NST * C::kStageBytes)[C::kRows * LD + n];
-            M = fmaxf(M, mk[k]);
-        }
-        float L = 0.f, o = 0.f;
+    for (int i = 0; i < RPT; ++i) {
+        const int n = r0 + i * RS;
+        float w[KW];
 #pragma unroll
-        for (int k = 0; k < KW; ++k) {
-            const float *part = reinterpret_cast<const float *>(pipe + (size_t)k * NST * C::kStageBytes);
-            // a warp with no visible key has weight 0 and a zero accumulator
-            const float w = (M == -CUDART_INF_F || mk[k] == -CUDART_INF_F) ? 0.f : exp2f(mk[k] - M);
-            L = fmaf(w, part[C::kRows * LD + C::kRows + n], L);
-            o = fmaf(w, part[n * LD + d], o);
-        }
-        if (ncta == 1) {
-            const long long orow = out_row(n);
-            const bool zero = flags || L <= 0.f;
-            if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / L;
-            if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
-        } else {
-            const int k = d / per, dl = d - k * per;
-            *cluster.map_shared_rank(sRecv + (rank * C::kRows + n) * per + dl, k) = o;
-            if (dl == 0) *cluster.map_shared_rank(sStat + rank * C::kRows + n, k) = make_float2(M, L);
+        for (int k = 0; k < KW; ++k) w[k] = __shfl_sync(0xffffffffu, wk, n * KW + k);
+        const float Mn = __shfl_sync(0xffffffffu, Mr, n * KW), Ln = __shfl_sync(0xffffffffu, Lr, n * KW);
+        if (n < rows_unit) {
+            const bool zero = flags || !(Ln > 0.f);
+            const float inv = zero ? 0.f : 1.f / Ln;
+            const long long orow = ncta == 1 ? out_row(n) : 0;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                const int d = c0 + j * CW;
+                float o = 0.f;
+#pragma unroll
+                for (int k = 0; k < KW; ++k) o = fmaf(w[k], part_of(k)[n * LD + d], o);
+                if (ncta == 1) {
+                    if (d < p.D) p.out[orow * p.D + d] = o * inv;
+                    if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (Mn + log2f(Ln)) * kLn2;
+                } else {
+                    *cluster.map_shared_rank(sRecv + ((rank * C::kRows + n) << lg) + (d & (per - 1)), d >> lg) = o;
+                }
+            }
         }
     }
     if (ncta == 1) return;
@@ -526,29 +572,38 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     int poison = 0;
 #pragma unroll
     for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
-    #pragma unroll 1
-    for (int idx = tid; idx < rows_unit * per; idx += NT) {
-        const int n = idx / per, dl = idx - n * per, d = rank * per + dl;
-        if (d >= DP) continue;  // the last CTA's slice may be short
-        float M = -CUDART_INF_F;
+    {   // normalised weight of CTA c for row n (thread n * 16 + c), and the row's lse
+        const int n = tid >> 4, c = tid & 15;
+        const float2 st = (c < ncta && n < rows_unit) ? sStat[c * C::kRows + n] : make_float2(-CUDART_INF_F, 0.f);
+        float M = st.x;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-            if (c < ncta) M = fmaxf(M, sStat[c * C::kRows + n].x);
-        float W = 0.f, o = 0.f;
+        for (int o = 1; o < 16; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        // A zero weight must not touch its partial: a poisoned one may hold NaN.
+        const float w = (M == -CUDART_INF_F || st.x == -CUDART_INF_F) ? 0.f : exp2f(st.x - M);
+        float W = w * st.y;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+        const bool zero = poison || !(W > 0.f);
+        if (tid < C::kRows * 16) sWn[n * 16 + c] = zero ? 0.f : w / W;
+        if (c == 0 && n < C::kRows) sLseR[n] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+    }
+    __syncthreads();
+    #pragma unroll 1
+    for (int e = tid; e < (rows_unit << lg); e += NT) {
+        const int n = e >> lg, dl = e & (per - 1), d = (rank << lg) + dl;
+        if (d >= DP) continue;
+        float o = 0.f;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             if (c < ncta) {
-                const float2 st = sStat[c * C::kRows + n];
-                // A zero weight must not touch its partial: a poisoned one may hold NaN.
-                const float w = (M == -CUDART_INF_F || st.x == -CUDART_INF_F) ? 0.f : exp2f(st.x - M);
-                W = fmaf(w, st.y, W);
-                o += w != 0.f ? w * sRecv[(c * C::kRows + n) * per + dl] : 0.f;
+                const float w = sWn[n * 16 + c];
+                const float v = sRecv[((c * C::kRows + n) << lg) + dl];
+                o += w != 0.f ? w * v : 0.f;
             }
         }
-        const bool zero = poison || W <= 0.f;
         const long long orow = out_row(n);
-        if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / W;
-        if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+        if (d < p.D) p.out[orow * p.D + d] = o;
+        if (d == 0 && p.lse) p.lse[orow] = sLseR[n];
     }
 }
 

@@ -36,7 +36,7 @@ class DecodeStep:
     def __init__(self, cache: PagedKVCache, num_q_heads: int, rows: int = 1, num_segments: int = 1,
                  max_q_len: int = 1, max_kv: Optional[int] = None, scale: Optional[float] = None,
                  causal: bool = False, window: int = 0, fused: bool = True, pdl: bool = True,
-                 flags: int = 0, num_splits: int = 0, with_lse: bool = False):
+                 flags: int = 0, num_splits: int = 0, with_lse: bool = False, prefetch_next: bool = True):
         dev = cache.k[0].device
         L, Hkv, D = cache.num_layers, cache.kv_heads, cache.head_dim
         self.cache = cache
@@ -46,6 +46,7 @@ class DecodeStep:
         self.scale = scale if scale is not None else 1.0 / math.sqrt(D)
         self.causal, self.window = causal, window
         self.fused, self.pdl, self.flags, self.num_splits = fused, pdl, flags, num_splits
+        self.prefetch_next = prefetch_next
         self.q = [torch.zeros(rows, num_q_heads, D, dtype=cache.dtype, device=dev) for _ in range(L)]
         self.k_new = [torch.zeros(rows, Hkv, D, dtype=cache.dtype, device=dev) for _ in range(L)]
         self.v_new = [torch.zeros(rows, Hkv, D, dtype=cache.dtype, device=dev) for _ in range(L)]
@@ -65,6 +66,8 @@ class DecodeStep:
             flags = self.flags
             if self.pdl and layer > 0 and self.fused:
                 flags |= _lib.FLAG_PDL
+            if self.prefetch_next and layer + 1 < c.num_layers:
+                flags |= _lib.FLAG_PREFETCH_NEXT  # the next call attends layer + 1 over the same segments
             if self.fused:
                 append_attend(c, layer, self.q[layer], self.k_new[layer], self.v_new[layer], self.seq_info,
                               self.out[layer], self.err, self.max_q_len, self.max_kv, self.scale, self.causal,

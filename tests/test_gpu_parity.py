@@ -119,6 +119,45 @@ def test_spec_verify(pkv, q_heads, causal):
         check_against_oracle(w, 0, out, lse, cache)
 
 
+@pytest.mark.parametrize("q_heads,max_q", [(8, 8), (16, 4), (32, 2), (64, 1)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_narrow_groups_multi_row(pkv, q_heads, max_q, causal):
+    # G * max_q_len <= 8: the decode kernel with several rows per token group
+    w = U.nan_tails(workloads.spec_verify(S=6, max_q=max_q, len_lo=1, len_hi=1500, causal=causal,
+                                          seed=q_heads + max_q, q_heads=q_heads))
+    out, lse, err, cache = run(pkv, w, max_kv=1500)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+def test_prefetch_next_hint_changes_nothing(pkv):
+    # The next-layer L2 warm-up is a hint: results are bitwise those without it,
+    # and on the last layer it is ignored.
+    w = workloads.sensenova(1000, 1024, num_layers=3, seed=5)
+    res = {}
+    for flags in (0, pkv.FLAG_PREFETCH_NEXT):
+        cache = U.device_cache(pkv, w)
+        outs = []
+        for layer in range(3):
+            dev = torch.device("cuda")
+            out = torch.zeros(1, w.q_heads, w.head_dim, device=dev)
+            lse = torch.zeros(1, w.q_heads, device=dev)
+            err = pkv.new_err_flags()
+            pkv.append_attend(cache, layer, w.q[layer].to(dev), w.k_new[layer].to(dev), w.v_new[layer].to(dev),
+                              w.seq_info.to(dev), out, err, 1, 1024, w.scale, lse=lse, flags=flags)
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0
+            outs.append((out.clone(), lse.clone()))
+        res[flags] = (outs, [U.pool_bytes(t) for t in cache.k + cache.v])
+    for (a, la), (b, lb) in zip(res[0][0], res[pkv.FLAG_PREFETCH_NEXT][0]):
+        assert torch.equal(a, b) and torch.equal(la, lb)
+    assert res[0][1] == res[pkv.FLAG_PREFETCH_NEXT][1]
+    for layer in range(3):
+        ref, _ = U.oracle_attend(w, layer)
+        assert float(np.abs(U.f64(res[0][0][layer][0]) - ref).max()) <= U.TOL[w.dtype]
+
+
 @pytest.mark.parametrize("window,ring", [(0, 0), (1000, 0), (1024, 1024), (300, 320)])
 def test_long_context(pkv, window, ring):
     w = U.nan_tails(workloads.long_context(S=2, kv_len=20000, window=window, ring_rows=ring, seed=5))
