@@ -75,6 +75,21 @@ __device__ __forceinline__ unsigned movmatrix_trans(unsigned x) {
     return y;
 }
 
+// One halving step of a reduce-scatter across lanes: the lane whose bit `m`
+// is set keeps the upper HALF values, the other the lower, each adding its
+// partner's copy.  Returns the offset of the kept half.
+template <int HALF>
+__device__ __forceinline__ int rs_halve(float (&x)[16], int lane_bits, int m) {
+    const bool upper = (lane_bits & m) != 0;
+#pragma unroll
+    for (int e = 0; e < HALF; ++e) {
+        const float send = upper ? x[e] : x[e + HALF];
+        const float keep = upper ? x[e + HALF] : x[e];
+        x[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+    return upper ? HALF : 0;
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_constant__ AttendParams p) {
     using T = __nv_bfloat16;
@@ -93,7 +108,6 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     int *sAllF = sFlag + 1;                                 // [16] flags of the cluster
     int *sCov = sFlag + 32;                                 // [NT] coverage flags of the first rows
     float *sWn = reinterpret_cast<float *>(sCov + NT);      // [8][16] normalised cluster merge weights
-    float *sLseR = sWn + C::kRows * 16;                     // [8] lse per row
 
     const int tid = threadIdx.x, kw = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
@@ -498,27 +512,6 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     };
     auto part_of = [&](int k) { return reinterpret_cast<const float *>(pipe + (size_t)k * NST * C::kStageBytes); };
 
-    // Merge weights of the warps' partials, row by row: every warp computes
-    // them in its lanes (lane n * KW + k: warp k's weight for row n, plus the
-    // row's max and sum) and hands them out by shuffles.
-    float wk, Mr, Lr;
-    {
-        const int n = lane / KW, k = lane - n * KW;
-        float mk = -CUDART_INF_F, lk = 0.f;
-        if (lane < C::kRows * KW) {
-            mk = part_of(k)[C::kRows * LD + n];
-            lk = part_of(k)[C::kRows * LD + C::kRows + n];
-        }
-        Mr = mk;
-#pragma unroll
-        for (int o = 1; o < KW; o <<= 1) Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, o));
-        // a warp with no visible key has weight 0 and a zero accumulator
-        wk = (Mr == -CUDART_INF_F || mk == -CUDART_INF_F) ? 0.f : exp2f(mk - Mr);
-        Lr = wk * lk;
-#pragma unroll
-        for (int o = 1; o < KW; o <<= 1) Lr += __shfl_xor_sync(0xffffffffu, Lr, o);
-    }
-
     cg::cluster_group cluster = cg::this_cluster();
     // Output columns each CTA of the cluster finishes: a power of two, so the
     // last CTAs may get none.
@@ -530,38 +523,54 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         // peers' shared memory may be written from here on.
         asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
         if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
-        {   // (max, sum) of each row to every CTA that finishes columns
-            const int n = tid & 7, k = tid >> 3;
-            const float Mn = __shfl_sync(0xffffffffu, Mr, n * KW), Ln = __shfl_sync(0xffffffffu, Lr, n * KW);
-            if (k < ncta && n < rows_unit) *cluster.map_shared_rank(sStat + rank * C::kRows + n, k) = make_float2(Mn, Ln);
-        }
     }
-    // Element pass: thread = column (x CPT) and a set of rows.
-    constexpr int CW = DP < NT ? DP : NT, CPT = DP / CW, RS = NT / CW, RPT = C::kRows / RS;
-    const int c0 = tid % CW, r0 = tid / CW;
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        const int n = r0 + i * RS;
-        float w[KW];
-#pragma unroll
-        for (int k = 0; k < KW; ++k) w[k] = __shfl_sync(0xffffffffu, wk, n * KW + k);
-        const float Mn = __shfl_sync(0xffffffffu, Mr, n * KW), Ln = __shfl_sync(0xffffffffu, Lr, n * KW);
+    // ---- merge the warps: thread = (row n, block of CB columns); the
+    // block goes whole to the CTA that finishes those columns (per >= CB).
+    constexpr int CB = DP / 16;
+    {
+        const int n = tid >> 4, cq = tid & 15, d0 = cq * CB;
         if (n < rows_unit) {
-            const bool zero = flags || !(Ln > 0.f);
-            const float inv = zero ? 0.f : 1.f / Ln;
-            const long long orow = ncta == 1 ? out_row(n) : 0;
+            float mk[KW], M = -CUDART_INF_F;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                const int d = c0 + j * CW;
-                float o = 0.f;
+            for (int k = 0; k < KW; ++k) {
+                mk[k] = part_of(k)[C::kRows * LD + n];
+                M = fmaxf(M, mk[k]);
+            }
+            float w[KW], L = 0.f;
 #pragma unroll
-                for (int k = 0; k < KW; ++k) o = fmaf(w[k], part_of(k)[n * LD + d], o);
-                if (ncta == 1) {
-                    if (d < p.D) p.out[orow * p.D + d] = o * inv;
-                    if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (Mn + log2f(Ln)) * kLn2;
-                } else {
-                    *cluster.map_shared_rank(sRecv + ((rank * C::kRows + n) << lg) + (d & (per - 1)), d >> lg) = o;
+            for (int k = 0; k < KW; ++k) {
+                // a warp with no visible key has weight 0 and a zero accumulator
+                w[k] = (M == -CUDART_INF_F || mk[k] == -CUDART_INF_F) ? 0.f : exp2f(mk[k] - M);
+                L = fmaf(w[k], part_of(k)[C::kRows * LD + C::kRows + n], L);
+            }
+            float o[CB];
+#pragma unroll
+            for (int e = 0; e < CB; ++e) o[e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < KW; ++k) {
+#pragma unroll
+                for (int e = 0; e < CB; e += 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(part_of(k) + n * LD + d0 + e);
+                    o[e] = fmaf(w[k], v.x, o[e]);
+                    o[e + 1] = fmaf(w[k], v.y, o[e + 1]);
+                    o[e + 2] = fmaf(w[k], v.z, o[e + 2]);
+                    o[e + 3] = fmaf(w[k], v.w, o[e + 3]);
                 }
+            }
+            if (ncta == 1) {
+                const long long orow = out_row(n);
+                const bool zero = flags || !(L > 0.f);
+                const float inv = zero ? 0.f : 1.f / L;
+#pragma unroll
+                for (int e = 0; e < CB; ++e)
+                    if (d0 + e < p.D) p.out[orow * p.D + d0 + e] = o[e] * inv;
+                if (cq == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
+            } else {
+                float *dst = cluster.map_shared_rank(sRecv + ((rank * C::kRows + n) << lg) + (d0 & (per - 1)), d0 >> lg);
+#pragma unroll
+                for (int e = 0; e < CB; e += 4)
+                    *reinterpret_cast<float4 *>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                if (cq < ncta) *cluster.map_shared_rank(sStat + rank * C::kRows + n, cq) = make_float2(M, L);
             }
         }
     }
@@ -572,8 +581,10 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     int poison = 0;
 #pragma unroll
     for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
-    {   // normalised weight of CTA c for row n (thread n * 16 + c), and the row's lse
-        const int n = tid >> 4, c = tid & 15;
+    // thread = (row n, source CTA c): normalised weight by 16-lane shuffles
+    const int n = tid >> 4, c = tid & 15;
+    float wn;
+    {
         const float2 st = (c < ncta && n < rows_unit) ? sStat[c * C::kRows + n] : make_float2(-CUDART_INF_F, 0.f);
         float M = st.x;
 #pragma unroll
@@ -584,26 +595,62 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
         const bool zero = poison || !(W > 0.f);
-        if (tid < C::kRows * 16) sWn[n * 16 + c] = zero ? 0.f : w / W;
-        if (c == 0 && n < C::kRows) sLseR[n] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+        wn = zero ? 0.f : w / W;
+        if (c == 0 && n < rows_unit && rank == 0 && p.lse)
+            p.lse[out_row(n)] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
     }
+    const int d_base = rank << lg;
+    if (per == 8 || per == 16) {
+        // Each thread weighs its source's slice; a reduce-scatter over the
+        // 16 sources leaves each lane one column's sum.
+        float x[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = 0.f;
+        if (c < ncta && n < rows_unit && wn != 0.f && d_base < DP) {
+            const float *src = sRecv + ((c * C::kRows + n) << lg);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                if (e < per) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src + e);
+                    x[e] = wn * v.x; x[e + 1] = wn * v.y; x[e + 2] = wn * v.z; x[e + 3] = wn * v.w;
+                }
+            }
+        }
+        // halving steps over lane bits 8, 4, 2 (and 1 for 16 columns): keep the
+        // half this lane's bit selects, add the partner's copy of it
+        int idx = 0;
+        if (per == 16) {
+            idx += rs_halve<8>(x, c, 8);
+            idx += rs_halve<4>(x, c, 4);
+            idx += rs_halve<2>(x, c, 2);
+            idx += rs_halve<1>(x, c, 1);
+        } else {
+            idx += rs_halve<4>(x, c, 8);
+            idx += rs_halve<2>(x, c, 4);
+            idx += rs_halve<1>(x, c, 2);
+            x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
+        }
+        const int d = d_base + idx;
+        if (n < rows_unit && (per == 16 || (c & 1) == 0) && d < p.D) p.out[out_row(n) * p.D + d] = x[0];
+        return;
+    }
+    // wider slices (small clusters): weights through shared memory
+    if (tid < C::kRows * 16) sWn[n * 16 + c] = wn;
     __syncthreads();
     #pragma unroll 1
     for (int e = tid; e < (rows_unit << lg); e += NT) {
-        const int n = e >> lg, dl = e & (per - 1), d = (rank << lg) + dl;
+        const int nn = e >> lg, dl = e & (per - 1), d = d_base + dl;
         if (d >= DP) continue;
         float o = 0.f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            if (c < ncta) {
-                const float w = sWn[n * 16 + c];
-                const float v = sRecv[((c * C::kRows + n) << lg) + dl];
+        for (int cc = 0; cc < 16; ++cc) {
+            if (cc < ncta) {
+                const float w = sWn[nn * 16 + cc];
+                const float v = sRecv[((cc * C::kRows + nn) << lg) + dl];
                 o += w != 0.f ? w * v : 0.f;
             }
         }
-        const long long orow = out_row(n);
-        if (d < p.D) p.out[orow * p.D + d] = o;
-        if (d == 0 && p.lse) p.lse[orow] = sLseR[n];
+        if (d < p.D) p.out[out_row(nn) * p.D + d] = o;
     }
 }
 
