@@ -217,6 +217,28 @@ int encode_pool(CUtensorMap *map, const void *pool, const pkv_cache *c) {
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ECUDA;
 }
 
+// 5-D view (64, 16, D / 64, kv_heads, num_blocks) of one pool, head_dim
+// split into 64-element halves (or quarters) ordered after the 16 tokens: one
+// box is a whole page tile of one kv head, laid out in shared memory exactly
+// as the 4-D view's D / 64 boxes back to back (128-byte swizzle).  Needs
+// head_dim a multiple of 64 (no partial last part).
+int encode_pool_pages(CUtensorMap *map, const void *pool, const pkv_cache *c) {
+    auto fn = encode_fn();
+    if (!fn) return PKV_ECUDA;
+    const int eb = elem_bytes(c->dtype);
+    const cuuint64_t D = (cuuint64_t)c->head_dim, H = (cuuint64_t)c->kv_heads;
+    const cuuint64_t part = 128 / eb;
+    cuuint64_t dims[5] = {part, (cuuint64_t)PKV_BLOCK_SIZE, D / part, H, (cuuint64_t)c->num_blocks};
+    cuuint64_t strides[4] = {H * D * eb, part * eb, D * eb, (cuuint64_t)PKV_BLOCK_SIZE * H * D * eb};
+    cuuint32_t box[5] = {(cuuint32_t)part, (cuuint32_t)PKV_BLOCK_SIZE, (cuuint32_t)(D / part), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    5, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ECUDA;
+}
+
 int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_new, const void *v_new,
                   int Hq, int total_rows, const int *seq_info, int S, int max_q_len, long long max_kv,
                   int num_splits, float scale, int causal, int window, float *out, float *lse,
@@ -236,7 +258,14 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     const int ncta = S == 0 ? 1 : schedulable_cluster(pl.k, pl.ncta);
 
     AttendParams p;
-    if ((st = encode_pool(&p.tmap_k, c->k[layer], c)) || (st = encode_pool(&p.tmap_v, c->v[layer], c))) return st;
+    // The decode kernel takes a page tile in one box when head_dim fills its
+    // padded width exactly (128 or 256; the other kernels use the 4-D view).
+    const bool page_box = pl.k.rows == 8 && c->dtype == PKV_BF16 && c->head_dim == pl.k.dp && c->head_dim > 64;
+    auto encode = [&](CUtensorMap *m, const void *pool) {
+        return page_box ? encode_pool_pages(m, pool, c) : encode_pool(m, pool, c);
+    };
+    p.page_box = page_box ? 1 : 0;
+    if ((st = encode(&p.tmap_k, c->k[layer])) || (st = encode(&p.tmap_v, c->v[layer]))) return st;
     p.q = q;
     p.k_new = k_new;
     p.v_new = v_new;
@@ -264,8 +293,7 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     p.scale_log2 = scale * 1.4426950408889634f;
     p.pf_next = 0;
     if ((flags & PKV_FLAG_PREFETCH_NEXT) && layer + 1 < c->num_layers && S > 0 && !check_layer(c, layer + 1)) {
-        if ((st = encode_pool(&p.tmap_k_next, c->k[layer + 1], c)) ||
-            (st = encode_pool(&p.tmap_v_next, c->v[layer + 1], c)))
+        if ((st = encode(&p.tmap_k_next, c->k[layer + 1])) || (st = encode(&p.tmap_v_next, c->v[layer + 1])))
             return st;
         // L2 budget: ~48 MB over every warp of the launch.
         const long long warps = (long long)ncta * c->kv_heads * pl.row_tiles * S * (pl.k.threads / 32);

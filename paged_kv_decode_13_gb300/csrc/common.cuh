@@ -70,6 +70,24 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 5-D tiled TMA load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1, int c2,
+                                            int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bring one 5-D tiled box into L2 without writing shared memory.
+__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap *map, int c0, int c1, int c2, int c3, int c4) {
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+                 : "memory");
+}
+
 // Bring one 4-D tiled box into L2 without writing shared memory.
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3) {
     asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
@@ -154,6 +172,10 @@ struct AttendParams {
     int row_tiles;          // CTAs along the rows of one (segment, kv head)
     int causal, window;
     float scale_log2;       // softmax_scale * log2(e)
+    // 1: the four maps are the 5-D page view (64, 16, D / 64, Hkv, num_blocks)
+    // that brings one kv head's page tile in one box; 0: the 4-D view
+    // (D, Hkv, 16, num_blocks) with 64-element boxes.
+    int page_box;
     // Optional L2 warm-up of the next layer's pages of the same key ranges
     // (the next call reads the same table and segments): pages per warp, 0 = off.
     int pf_next;

@@ -207,10 +207,15 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
             if (ok) {
                 fence_proxy_async();
                 mbar_expect_tx(bar, C::kStageBytes);
+                if (p.page_box) {
+                    tma_load_5d(st, &p.tmap_k, bar, 0, 0, 0, g, bid);
+                    tma_load_5d(st + C::kTileBytes, &p.tmap_v, bar, 0, 0, 0, g, bid);
+                } else {
 #pragma unroll
-                for (int b = 0; b < C::kBoxes; ++b) {
-                    tma_load_4d(st + b * 2048, &p.tmap_k, bar, b * C::kBoxEl, g, 0, bid);
-                    tma_load_4d(st + C::kTileBytes + b * 2048, &p.tmap_v, bar, b * C::kBoxEl, g, 0, bid);
+                    for (int b = 0; b < C::kBoxes; ++b) {
+                        tma_load_4d(st + b * 2048, &p.tmap_k, bar, b * C::kBoxEl, g, 0, bid);
+                        tma_load_4d(st + C::kTileBytes + b * 2048, &p.tmap_v, bar, b * C::kBoxEl, g, 0, bid);
+                    }
                 }
             } else {
                 mbar_arrive(bar);  // nothing to fetch: complete the phase, the result is discarded
@@ -230,6 +235,20 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         if (!__all_sync(0xffffffffu, done)) timed_out = true;
     };
 
+    // Warm L2 with page `bid` of this kv head (K and V).
+    auto prefetch_page = [&](const CUtensorMap *mk, const CUtensorMap *mv, int bid) {
+        if (p.page_box) {
+            tma_prefetch_l2_5d(mk, 0, 0, 0, g, bid);
+            tma_prefetch_l2_5d(mv, 0, 0, 0, g, bid);
+        } else {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_4d(mk, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(mv, b * C::kBoxEl, g, 0, bid);
+            }
+        }
+    };
+
     int issued = 0;
     load_ids(0);
     #pragma unroll 1
@@ -243,25 +262,15 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         constexpr int kL2Pages = (131072 / (int)C::kStageBytes) > 0 ? 131072 / (int)C::kStageBytes : 1;
         const int pf_end = min(min(n_mine, 32), NST + kL2Pages);
         const int bid = id_reg;
-        if (lane >= issued && lane < pf_end && bid >= 0 && (long long)bid < p.num_blocks) {
-#pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b) {
-                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
-                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
-            }
-        }
+        if (lane >= issued && lane < pf_end && bid >= 0 && (long long)bid < p.num_blocks)
+            prefetch_page(&p.tmap_k, &p.tmap_v, bid);
     }
     // The next layer's pages of the same range (same table and segments), so
     // its HBM traffic runs under this layer's compute.
     if (p.pf_next > 0) {
         const int bid = id_reg;
-        if (lane < min(n_mine, p.pf_next) && bid >= 0 && (long long)bid < p.num_blocks) {
-#pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b) {
-                tma_prefetch_l2_4d(&p.tmap_k_next, b * C::kBoxEl, g, 0, bid);
-                tma_prefetch_l2_4d(&p.tmap_v_next, b * C::kBoxEl, g, 0, bid);
-            }
-        }
+        if (lane < min(n_mine, p.pf_next) && bid >= 0 && (long long)bid < p.num_blocks)
+            prefetch_page(&p.tmap_k_next, &p.tmap_v_next, bid);
     }
     // Append validity (all-or-nothing over the segment's new rows): the block
     // table is not written by the previous kernel.
