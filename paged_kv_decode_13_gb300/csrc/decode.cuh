@@ -33,6 +33,9 @@
 
 namespace pkv {
 
+// Key ranges of at most this many pages per compute warp run on one CTA.
+constexpr int kSoloPages = 3;
+
 template <int DP_, int KW_, int NST_>
 struct DecCfg {
     using T = __nv_bfloat16;
@@ -154,8 +157,6 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         if (first_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
     }
-    if (ncta > 1)  // announce this CTA to the cluster; waited on before any remote store
-        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
     const int kend = sg.kend;
     const int new_start = kend - sg.ql;
     int lo_u = 0;
@@ -163,11 +164,19 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     const int pb_begin = lo_u / kPage;
     const int pb_end = (kend + kPage - 1) / kPage;
     const int nblk = pb_end - pb_begin;
-    const int bps = (nblk + ncta - 1) / ncta;
-    const int active = (nblk + bps - 1) / bps;
+    // A short range (a few pages per warp) is cheaper on one CTA than split
+    // and merged across the cluster: the first CTA then takes it alone and
+    // the cluster's merge is skipped (uniformly: it depends on kv_end only).
+    const bool solo = nblk <= kSoloPages * KW;
+    const int ncl = solo ? 1 : ncta;  // CTAs that share the range
+    const int bps = solo ? nblk : (nblk + ncta - 1) / ncta;
+    const int active = bps > 0 ? (nblk + bps - 1) / bps : 0;
     const int cb0 = pb_begin + rank * bps;
     const int nb = rank < active ? min(cb0 + bps, pb_end) - cb0 : 0;
     const int n_mine = nb > kw ? (nb - kw + KW - 1) / KW : 0;
+    if (solo && rank > 0 && !first_cta) return;  // nothing to read or write
+    if (ncl > 1)  // announce this CTA to the cluster; waited on before any remote store
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
 
     const T *knew = reinterpret_cast<const T *>(p.k_new);
     const T *vnew = reinterpret_cast<const T *>(p.v_new);
@@ -256,6 +265,32 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         if (!early_ok(issued)) break;
         issue(issued);
     }
+    // V rows outside [lo_u, kend) may hold anything (NaN included) and are
+    // zeroed in shared memory (their scores are masked).
+    auto zero_stale = [&](unsigned char *st, int zlo, int zhi) {
+        const int nz = (zlo + kPage - zhi) * C::kChunks;
+        #pragma unroll 1
+        for (int c = lane; c < nz; c += 32) {
+            const int o0 = c / C::kChunks, ch = c - o0 * C::kChunks;
+            const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
+            *reinterpret_cast<uint4 *>(st + C::kTileBytes + swz(o, ch)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    // Edge pages already in flight (the last page past kv_end, the first
+    // before the window) are zeroed now, while the previous kernel runs.
+    unsigned prezero = 0;
+    #pragma unroll 1
+    for (int j = 0; j < issued; ++j) {
+        const int pos0 = (cb0 + kw + j * KW) * kPage;
+        const int zlo = min(max(lo_u - pos0, 0), kPage), zhi = min(max(kend - pos0, 0), kPage);
+        if (zlo > 0 || zhi < kPage) {
+            wait_page(j);
+            if (!timed_out) {
+                zero_stale(wstage + (size_t)(j % NST) * C::kStageBytes, zlo, zhi);
+                prezero |= 1u << j;
+            }
+        }
+    }
     // Later pages (up to ~128 KB per warp) go to L2 now, so their HBM traffic
     // overlaps the previous kernel's tail.
     {
@@ -272,10 +307,19 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         if (lane < min(n_mine, p.pf_next) && bid >= 0 && (long long)bid < p.num_blocks)
             prefetch_page(&p.tmap_k_next, &p.tmap_v_next, bid);
     }
+    // The step's rows in the CTA's last page (decode: the one new row) are
+    // handled by the warp that computes that page.
+    const int last_li = nb - 1, last_pos0 = (cb0 + last_li) * kPage;
+    const int pre_a = max(new_start, last_pos0), pre_n = has_new ? max(0, kend - pre_a) : 0;
+    const bool pre_mine = pre_n > 0 && kw == last_li % KW;
     // Append validity (all-or-nothing over the segment's new rows): the block
-    // table is not written by the previous kernel.
+    // table is not written by the previous kernel.  One new row lives in the
+    // last page, whose id this warp already holds; more rows are looked up.
     bool app_ok = false;
-    if (has_new) {
+    if (has_new && sg.ql == 1 && last_li / KW < 32) {
+        const int bid = __shfl_sync(0xffffffffu, id_reg, last_li / KW);
+        app_ok = bid >= 0 && (long long)bid < p.num_blocks;
+    } else if (has_new) {
         bool ok = true;
         #pragma unroll 1
         for (int i = lane; i < sg.ql; i += 32) {
@@ -325,11 +369,8 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
             qb[kk][1] = real && d1 < p.D ? *reinterpret_cast<const unsigned *>(qrow + d1) : 0u;
         }
     }
-    // The step's rows in the warp's last page (decode: the one new row),
-    // loaded beside the queries; the page fix-up stores them.
-    const int last_li = nb - 1, last_pos0 = (cb0 + last_li) * kPage;
-    const int pre_a = max(new_start, last_pos0), pre_n = has_new ? max(0, kend - pre_a) : 0;
-    const bool pre_mine = pre_n > 0 && kw == last_li % KW;
+    // This step's rows in the CTA's last page, loaded beside the queries; the
+    // page fix-up stores them.
     uint4 pre[2];
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
@@ -370,22 +411,15 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), kchk = lane >> 4;
     const int vrow = (lane & 7) + ((lane >> 4) << 3), vchk = (lane >> 3) & 1;
 
-    // Rows outside [lo_u, kend) may hold anything (NaN included): their V rows
-    // are zeroed (their scores are masked).  This step's own rows come from
-    // k_new / v_new in the fused call, and the warp that holds them also
-    // writes them into the cache.
+    // Edge pages: stale V rows zeroed (unless done before the wait).  This
+    // step's own rows come from k_new / v_new in the fused call, and the warp
+    // that holds them also writes them into the cache.
     auto fix_page = [&](int j, unsigned char *st, int pos0) {
         const int zlo = min(max(lo_u - pos0, 0), kPage);
         const int zhi = min(max(kend - pos0, 0), kPage);
         const int na = fused ? min(max(new_start - pos0, 0), kPage) : zhi;
         if (!(zlo > 0 || zhi < kPage || na < zhi)) return;
-        const int nz = (zlo + kPage - zhi) * C::kChunks;
-        #pragma unroll 1
-        for (int c = lane; c < nz; c += 32) {
-            const int o0 = c / C::kChunks, ch = c - o0 * C::kChunks;
-            const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
-            *reinterpret_cast<uint4 *>(st + C::kTileBytes + swz(o, ch)) = make_uint4(0u, 0u, 0u, 0u);
-        }
+        if (!(j < 32 && ((prezero >> j) & 1u))) zero_stale(st, zlo, zhi);
         const int nnr = zhi - na;  // new rows in this page
         if (nnr > 0) {
             const long long bpage = app_ok ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
@@ -525,13 +559,13 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     // Output columns each CTA of the cluster finishes: a power of two, so the
     // last CTAs may get none.
     int lg = 0;
-    while ((1 << lg) * ncta < DP) ++lg;
+    while ((1 << lg) * ncl < DP) ++lg;
     const int per = 1 << lg;
-    if (ncta > 1) {
+    if (ncl > 1) {
         // Every CTA of the cluster has started (the arrive at the top), so
         // peers' shared memory may be written from here on.
         asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
-        if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+        if (tid < ncl) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
     }
     // ---- merge the warps: thread = (row n, block of CB columns); the
     // block goes whole to the CTA that finishes those columns (per >= CB).
@@ -566,35 +600,35 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
                     o[e + 3] = fmaf(w[k], v.w, o[e + 3]);
                 }
             }
-            if (ncta == 1) {
+            if (ncl == 1) {
                 const long long orow = out_row(n);
                 const bool zero = flags || !(L > 0.f);
                 const float inv = zero ? 0.f : 1.f / L;
 #pragma unroll
                 for (int e = 0; e < CB; ++e)
-                    if (d0 + e < p.D) p.out[orow * p.D + d0 + e] = o[e] * inv;
+                    if (d0 + e < p.D) p.out[orow * p.D + d0 + e] = zero ? 0.f : o[e] * inv;  // o may be NaN when poisoned
                 if (cq == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
             } else {
                 float *dst = cluster.map_shared_rank(sRecv + ((rank * C::kRows + n) << lg) + (d0 & (per - 1)), d0 >> lg);
 #pragma unroll
                 for (int e = 0; e < CB; e += 4)
                     *reinterpret_cast<float4 *>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                if (cq < ncta) *cluster.map_shared_rank(sStat + rank * C::kRows + n, cq) = make_float2(M, L);
+                if (cq < ncl) *cluster.map_shared_rank(sStat + rank * C::kRows + n, cq) = make_float2(M, L);
             }
         }
     }
-    if (ncta == 1) return;
+    if (ncl == 1) return;
 
     // ---- merge the cluster's partials of this CTA's columns
     cluster.sync();  // publishes every CTA's pushed partials
     int poison = 0;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
+    for (int c = 0; c < 16; ++c) poison |= c < ncl ? sAllF[c] : 0;
     // thread = (row n, source CTA c): normalised weight by 16-lane shuffles
     const int n = tid >> 4, c = tid & 15;
     float wn;
     {
-        const float2 st = (c < ncta && n < rows_unit) ? sStat[c * C::kRows + n] : make_float2(-CUDART_INF_F, 0.f);
+        const float2 st = (c < ncl && n < rows_unit) ? sStat[c * C::kRows + n] : make_float2(-CUDART_INF_F, 0.f);
         float M = st.x;
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -615,7 +649,7 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         float x[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) x[e] = 0.f;
-        if (c < ncta && n < rows_unit && wn != 0.f && d_base < DP) {
+        if (c < ncl && n < rows_unit && wn != 0.f && d_base < DP) {
             const float *src = sRecv + ((c * C::kRows + n) << lg);
 #pragma unroll
             for (int e = 0; e < 16; e += 4) {
@@ -653,7 +687,7 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         float o = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
-            if (cc < ncta) {
+            if (cc < ncl) {
                 const float w = sWn[nn * 16 + cc];
                 const float v = sRecv[((cc * C::kRows + nn) << lg) + dl];
                 o += w != 0.f ? w * v : 0.f;

@@ -140,12 +140,13 @@ def test_prefetch_next_hint_changes_nothing(pkv):
         cache = U.device_cache(pkv, w)
         outs = []
         for layer in range(3):
+            fl = flags
             dev = torch.device("cuda")
             out = torch.zeros(1, w.q_heads, w.head_dim, device=dev)
             lse = torch.zeros(1, w.q_heads, device=dev)
             err = pkv.new_err_flags()
             pkv.append_attend(cache, layer, w.q[layer].to(dev), w.k_new[layer].to(dev), w.v_new[layer].to(dev),
-                              w.seq_info.to(dev), out, err, 1, 1024, w.scale, lse=lse, flags=flags)
+                              w.seq_info.to(dev), out, err, 1, 1024, w.scale, lse=lse, flags=fl)
             torch.cuda.synchronize()
             assert int(err.item()) == 0
             outs.append((out.clone(), lse.clone()))
