@@ -31,9 +31,10 @@ SWEEP = (256, 512, 1024, 2048, 4096, 6144, 8192)
 METRIC = "paged decode attention µs/step and achieved HBM GB/s (% of peak) vs KV length"
 WORKLOAD = ("SenseNova-style decode: 42 layers, 32 q / 8 kv heads, head_dim 128, bf16, one sequence, "
             "identity block table, KV length 8192 in the 8192 bucket, one captured graph per bucket")
-KERNEL_SOURCES = ("paged_kv_decode_13_gb300/csrc/attend.cuh", "paged_kv_decode_13_gb300/csrc/common.cuh",
+KERNEL_SOURCES = ("paged_kv_decode_13_gb300/csrc/decode.cuh", "paged_kv_decode_13_gb300/csrc/attend.cuh",
+                  "paged_kv_decode_13_gb300/csrc/common.cuh",
                   "paged_kv_decode_13_gb300/csrc/attend_inst.cu")
-PROFILE = os.path.join(ROOT, "profiles", "attend_sensenova_8192_traffic.json")
+PROFILE = os.path.join(ROOT, "profiles", "decode_sensenova_8192_traffic.json")
 
 
 def algorithmic_bytes_per_layer(L: int) -> int:
@@ -333,7 +334,7 @@ def gpu_arm(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (STREAM-style copy)",
-                         "kernel": "attend_kernel (fused append + split-K attention), one launch per layer",
+                         "kernel": "decode_kernel (fused append + split-K attention, 16-CTA clusters), one launch per layer",
                          "algorithmic_bytes_per_launch": bytes_layer,
                          "launch_ms": round(per_launch_ms, 6)},
             "by_kv_len": by_len,
