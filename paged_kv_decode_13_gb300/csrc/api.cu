@@ -291,14 +291,14 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     p.causal = causal;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.k_next = p.v_next = nullptr;
     p.pf_next = 0;
     if ((flags & PKV_FLAG_PREFETCH_NEXT) && layer + 1 < c->num_layers && S > 0 && !check_layer(c, layer + 1)) {
-        if ((st = encode(&p.tmap_k_next, c->k[layer + 1])) || (st = encode(&p.tmap_v_next, c->v[layer + 1])))
-            return st;
-        // L2 budget: ~48 MB over every warp of the launch.
-        const long long warps = (long long)ncta * c->kv_heads * pl.row_tiles * S * (pl.k.threads / 32);
-        const long long stage = 2LL * PKV_BLOCK_SIZE * pl.k.dp * elem_bytes(c->dtype);
-        p.pf_next = (int)std::max<long long>(0, std::min<long long>(32, (48LL << 20) / (warps * stage)));
+        p.k_next = c->k[layer + 1];
+        p.v_next = c->v[layer + 1];
+        // L2 budget: ~48 MB; a page is warmed once for all kv heads (K and V).
+        const long long page = 2LL * PKV_BLOCK_SIZE * c->kv_heads * c->head_dim * elem_bytes(c->dtype);
+        p.pf_next = (int)std::max<long long>(0, std::min<long long>(1 << 20, (48LL << 20) / ((long long)ncta * S * page)));
     }
 
     cudaLaunchConfig_t cfg = {};

@@ -88,6 +88,12 @@ __device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap *map, int c
                  : "memory");
 }
 
+// Bring `bytes` contiguous bytes (16-byte aligned, a multiple of 16) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // Bring one 4-D tiled box into L2 without writing shared memory.
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3) {
     asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
@@ -177,10 +183,11 @@ struct AttendParams {
     // (D, Hkv, 16, num_blocks) with 64-element boxes.
     int page_box;
     // Optional L2 warm-up of the next layer's pages of the same key ranges
-    // (the next call reads the same table and segments): pages per warp, 0 = off.
+    // (the next call reads the same table and segments): the next layer's
+    // pools, and how many pages of each CTA's range to warm (0 = off).
+    const void *k_next;
+    const void *v_next;
     int pf_next;
-    CUtensorMap tmap_k_next;
-    CUtensorMap tmap_v_next;
 };
 
 struct AppendParams {

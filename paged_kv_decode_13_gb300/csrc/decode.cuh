@@ -65,7 +65,7 @@ struct DecCfg {
     static constexpr size_t kCovBytes = (size_t)kThreads * 4;
     static constexpr size_t kSmemBytes =
         1024 + kPipeBytes + kRecvBytes + kStatBytes + kBarBytes + kFlagBytes + kCovBytes + kWnBytes;
-    static_assert(kThreads == 128, "the cluster merge maps 8 rows x 16 CTAs onto the threads");
+    static_assert(kThreads >= 128, "the merges map 8 rows x 16 onto the first 128 threads");
     static_assert(kPartBytes <= NST * kStageBytes, "a warp's partial fits over its own stages");
     static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
 };
@@ -245,17 +245,24 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     };
 
     // Warm L2 with page `bid` of this kv head (K and V).
-    auto prefetch_page = [&](const CUtensorMap *mk, const CUtensorMap *mv, int bid) {
+    auto prefetch_page = [&](int bid) {
         if (p.page_box) {
-            tma_prefetch_l2_5d(mk, 0, 0, 0, g, bid);
-            tma_prefetch_l2_5d(mv, 0, 0, 0, g, bid);
+            tma_prefetch_l2_5d(&p.tmap_k, 0, 0, 0, g, bid);
+            tma_prefetch_l2_5d(&p.tmap_v, 0, 0, 0, g, bid);
         } else {
 #pragma unroll
             for (int b = 0; b < C::kBoxes; ++b) {
-                tma_prefetch_l2_4d(mk, b * C::kBoxEl, g, 0, bid);
-                tma_prefetch_l2_4d(mv, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
             }
         }
+    };
+    // A whole page of the next layer (every kv head, K and V: one contiguous
+    // block each), one bulk prefetch per tensor.
+    const unsigned page_bytes = (unsigned)(kPage * p.Hkv * p.D * (int)sizeof(T));
+    auto warm_next = [&](int bid) {
+        bulk_prefetch_l2(reinterpret_cast<const char *>(p.k_next) + (size_t)bid * page_bytes, page_bytes);
+        bulk_prefetch_l2(reinterpret_cast<const char *>(p.v_next) + (size_t)bid * page_bytes, page_bytes);
     };
 
     int issued = 0;
@@ -291,21 +298,22 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
             }
         }
     }
-    // Later pages (up to ~128 KB per warp) go to L2 now, so their HBM traffic
-    // overlaps the previous kernel's tail.
+    // The warp's pages past its stages go to L2 now (up to ~128 KB per warp),
+    // so their HBM traffic overlaps the previous kernel's tail.  Lane l holds
+    // the id of the warp's page kw + l * KW.
     {
         constexpr int kL2Pages = (131072 / (int)C::kStageBytes) > 0 ? 131072 / (int)C::kStageBytes : 1;
-        const int pf_end = min(min(n_mine, 32), NST + kL2Pages);
         const int bid = id_reg;
-        if (lane >= issued && lane < pf_end && bid >= 0 && (long long)bid < p.num_blocks)
-            prefetch_page(&p.tmap_k, &p.tmap_v, bid);
+        if (lane >= issued && lane < min(min(n_mine, 32), NST + kL2Pages) && bid >= 0 &&
+            (long long)bid < p.num_blocks)
+            prefetch_page(bid);
     }
     // The next layer's pages of the same range (same table and segments), so
-    // its HBM traffic runs under this layer's compute.
+    // its HBM traffic runs under this layer's compute: whole pages, warmed by
+    // the CTAs of the same cluster rank in turn (page li by kv head li % Hkv).
     if (p.pf_next > 0) {
-        const int bid = id_reg;
-        if (lane < min(n_mine, p.pf_next) && bid >= 0 && (long long)bid < p.num_blocks)
-            prefetch_page(&p.tmap_k_next, &p.tmap_v_next, bid);
+        const int li = kw + lane * KW, bid = id_reg;
+        if (li < min(nb, p.pf_next) && li % p.Hkv == g && bid >= 0 && (long long)bid < p.num_blocks) warm_next(bid);
     }
     // The step's rows in the CTA's last page (decode: the one new row) are
     // handled by the warp that computes that page.
