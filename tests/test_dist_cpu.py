@@ -1,0 +1,73 @@
+"""The multi-rank host logic of bench.py, run as two gloo ranks on the CPU.
+
+Each rank of `bench.py --gpus N` decodes its own sequence (independent
+replicas, no data-path collective); the only cross-rank steps are the
+barrier around the timed region and the max over ranks of the step time.
+These tests run that logic with world_size 2 over gloo, and check that the
+reference arm prints from rank 0 only.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, r, local = bench.dist_env()
+        assert (w, r, local) == (world, rank, rank)
+        dist.barrier()
+        # every rank times a different step; all report the slowest
+        got = bench.reduce_max(1.5 + rank, world, torch.device("cpu"))
+        results[rank] = got
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    port = _free_port()
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(_rank_main, args=(2, port, results), nprocs=2, join=True)
+        assert dict(results) == {0: 2.5, 1: 2.5}
+
+
+def test_reduce_max_single_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max(3.25, 1, torch.device("cpu")) == 3.25
+
+
+@pytest.mark.parametrize("rank", [0, 1])
+def test_reference_arm_prints_on_rank0_only(rank):
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank))
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    if rank == 0:
+        line = json.loads(lines[-1])
+        assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+        assert line["e2e"]["h2d_bytes_per_step"] == 0
+    else:
+        assert lines == []
