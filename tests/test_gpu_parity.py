@@ -131,22 +131,33 @@ def test_narrow_groups_multi_row(pkv, q_heads, max_q, causal):
     check_against_oracle(w, 0, out, lse, cache)
 
 
-def test_prefetch_next_hint_changes_nothing(pkv):
+def _prefetch_workload(kind):
+    if kind == "single":
+        return workloads.sensenova(1000, 1024, num_layers=3, seed=5)
+    if kind == "batched":
+        return workloads.batched(S=8, max_len=2000, num_layers=3, seed=6, kv_heads=8, q_heads=32)
+    return workloads.long_context(S=2, kv_len=5000, window=300, ring_rows=320, num_layers=3, seed=7, q_heads=16,
+                                  kv_heads=4, head_dim=128)
+
+
+@pytest.mark.parametrize("kind", ["single", "batched", "ring"])
+def test_prefetch_next_hint_changes_nothing(pkv, kind):
     # The next-layer L2 warm-up is a hint: results are bitwise those without it,
     # and on the last layer it is ignored.
-    w = workloads.sensenova(1000, 1024, num_layers=3, seed=5)
+    w = _prefetch_workload(kind)
+    dev = torch.device("cuda")
+    max_kv = int(w.seq_info[:, 3].max())
     res = {}
     for flags in (0, pkv.FLAG_PREFETCH_NEXT):
         cache = U.device_cache(pkv, w)
         outs = []
         for layer in range(3):
-            fl = flags
-            dev = torch.device("cuda")
-            out = torch.zeros(1, w.q_heads, w.head_dim, device=dev)
-            lse = torch.zeros(1, w.q_heads, device=dev)
+            out = torch.zeros(w.total_rows, w.q_heads, w.head_dim, device=dev)
+            lse = torch.zeros(w.total_rows, w.q_heads, device=dev)
             err = pkv.new_err_flags()
             pkv.append_attend(cache, layer, w.q[layer].to(dev), w.k_new[layer].to(dev), w.v_new[layer].to(dev),
-                              w.seq_info.to(dev), out, err, 1, 1024, w.scale, lse=lse, flags=fl)
+                              w.seq_info.to(dev), out, err, 1, max_kv, w.scale, w.causal, w.window, lse=lse,
+                              flags=flags)
             torch.cuda.synchronize()
             assert int(err.item()) == 0
             outs.append((out.clone(), lse.clone()))
@@ -157,6 +168,36 @@ def test_prefetch_next_hint_changes_nothing(pkv):
     for layer in range(3):
         ref, _ = U.oracle_attend(w, layer)
         assert float(np.abs(U.f64(res[0][0][layer][0]) - ref).max()) <= U.TOL[w.dtype]
+
+
+@pytest.mark.parametrize("seqused", [176, 192, 193, 208, 4099])
+@pytest.mark.parametrize("num_splits", [0, 5, 16])
+def test_decode_one_cta_or_cluster(pkv, seqused, num_splits):
+    # Up to 12 pages a key range runs on one CTA without the cluster merge;
+    # from 13 pages on it is split across the cluster (any split count).
+    w = U.nan_tails(workloads.sensenova(seqused, pkv.bucket_for(seqused), num_layers=1, seed=seqused))
+    out, lse, err, cache = run(pkv, w, max_kv=w.bucket, num_splits=num_splits)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+@pytest.mark.parametrize("window", [5, 40, 180, 700])
+def test_decode_windows_edge_pages(pkv, window):
+    # windows whose first page starts mid-page (stale rows before the window
+    # zeroed), with single and clustered ranges
+    w = U.nan_tails(workloads.batched(S=6, max_len=3000, seed=window, kv_heads=8, q_heads=32, min_len=100))
+    w.causal, w.window = True, window
+    # slots before each window hold NaN too: they must never reach the output
+    bt, si = w.block_table.numpy(), w.seq_info.numpy()
+    for q0, ql, col, kend in si:
+        for pos in range(max(0, int(kend) - window)):
+            b = int(bt[col, pos // 16])
+            for t in w.k + w.v:
+                t[b, pos % 16] = float("nan")
+    out, lse, err, cache = run(pkv, w, max_kv=3000)
+    assert err == 0
+    check_against_oracle(w, 0, out, lse, cache)
 
 
 @pytest.mark.parametrize("window,ring", [(0, 0), (1000, 0), (1024, 1024), (300, 320)])
