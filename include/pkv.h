@@ -170,7 +170,8 @@ int pkv_append(const pkv_cache *cache, int32_t layer,
  * length up to them.  num_splits (0..16) is the number of CTAs that share one
  * (segment, kv head) key range as a thread-block cluster; their partial
  * softmax results are merged by log-sum-exp through distributed shared
- * memory in the same launch, so no workspace is needed.  0 picks the count
+ * memory in the same launch, so no workspace is needed (workspace NULL,
+ * workspace_bytes 0; see pkv_attend_workspace_bytes for the other mode).  0 picks the count
  * from the launch shape (and a smaller one if the device cannot co-schedule
  * the cluster); a larger count than the segment has 16-token pages leaves
  * CTAs idle.
@@ -195,6 +196,7 @@ int pkv_attend_varlen(const pkv_cache *cache, int32_t layer,
                       int32_t max_q_len, int64_t max_kv, int32_t num_splits,
                       float softmax_scale, int32_t causal, int32_t window,
                       float *out, float *lse,
+                      void *workspace, int64_t workspace_bytes,
                       uint32_t *err_flags, uint32_t flags, void *stream);
 
 /*
@@ -211,7 +213,27 @@ int pkv_append_attend(const pkv_cache *cache, int32_t layer,
                       int32_t max_q_len, int64_t max_kv, int32_t num_splits,
                       float softmax_scale, int32_t causal, int32_t window,
                       float *out, float *lse,
+                      void *workspace, int64_t workspace_bytes,
                       uint32_t *err_flags, uint32_t flags, void *stream);
+
+/*
+ * Bytes of workspace the two calls above need for these launch bounds when
+ * given one (0: the launch never uses it).  With a workspace, the decode
+ * kernel (at most 8 query rows per segment and kv head: G * max_q_len <= 8,
+ * bf16, tensor-core path) splits a key range over independent CTAs (up to 64
+ * per range, num_splits 0..64) that merge through it: each writes its
+ * partial rows, and the last to finish (counted with an atomic it resets)
+ * merges them.  Without one (NULL), the splits form a thread-block cluster
+ * and merge through distributed shared memory (num_splits 0..16).  The
+ * workspace is device memory the caller owns, 16-byte aligned, zero-filled
+ * before its first use and not touched by the caller between calls (each
+ * call leaves its counters at zero); calls that may run concurrently need
+ * their own.  A workspace smaller than this size is rejected with
+ * PKV_EINVAL.  Returns a negative pkv_status for invalid bounds.
+ */
+int64_t pkv_attend_workspace_bytes(const pkv_cache *cache, int32_t num_q_heads,
+                                   int32_t num_segments, int32_t max_q_len,
+                                   int64_t max_kv, int32_t num_splits, uint32_t flags);
 
 /*
  * Build a segment table from the flash-attention argument form

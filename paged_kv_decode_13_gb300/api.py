@@ -125,31 +125,49 @@ def append(cache: PagedKVCache, layer: int, k_new: torch.Tensor, v_new: torch.Te
 
 
 def _attend(fn_name, cache, layer, q, k_new, v_new, seq_info, out, lse, err, max_q_len, max_kv, scale, causal,
-            window, num_splits, flags, stream):
+            window, num_splits, flags, stream, workspace):
     rows, hq = int(q.shape[0]), int(q.shape[1])
     args = [cache.ref(), layer, _ptr(_contig(q, "q"))]
     if fn_name == "pkv_append_attend":
         args += [_ptr(_contig(k_new, "k_new")), _ptr(_contig(v_new, "v_new"))]
+    ws_bytes = int(workspace.numel() * workspace.element_size()) if workspace is not None else 0
     args += [hq, rows, _ptr(_contig(seq_info, "seq_info")), int(seq_info.shape[0]), int(max_q_len), int(max_kv),
              int(num_splits), float(scale), int(bool(causal)), int(window), _ptr(_contig(out, "out")),
-             _ptr(lse), _ptr(err), int(flags), _stream(stream)]
+             _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err), int(flags), _stream(stream)]
     _lib.check(fn_name, getattr(lib, fn_name)(*args))
 
 
 def attend_varlen(cache: PagedKVCache, layer: int, q: torch.Tensor, seq_info: torch.Tensor, out: torch.Tensor,
                   err: torch.Tensor, max_q_len: int, max_kv: int, scale: float, causal: bool = False,
                   window: int = 0, lse: Optional[torch.Tensor] = None, num_splits: int = 0, flags: int = 0,
-                  stream=None) -> None:
+                  stream=None, workspace: Optional[torch.Tensor] = None) -> None:
     _attend("pkv_attend_varlen", cache, layer, q, None, None, seq_info, out, lse, err, max_q_len, max_kv, scale,
-            causal, window, num_splits, flags, stream)
+            causal, window, num_splits, flags, stream, workspace)
 
 
 def append_attend(cache: PagedKVCache, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                   seq_info: torch.Tensor, out: torch.Tensor, err: torch.Tensor, max_q_len: int, max_kv: int,
                   scale: float, causal: bool = False, window: int = 0, lse: Optional[torch.Tensor] = None,
-                  num_splits: int = 0, flags: int = 0, stream=None) -> None:
+                  num_splits: int = 0, flags: int = 0, stream=None, workspace: Optional[torch.Tensor] = None) -> None:
     _attend("pkv_append_attend", cache, layer, q, k_new, v_new, seq_info, out, lse, err, max_q_len, max_kv, scale,
-            causal, window, num_splits, flags, stream)
+            causal, window, num_splits, flags, stream, workspace)
+
+
+def attend_workspace_bytes(cache: PagedKVCache, num_q_heads: int, num_segments: int, max_q_len: int, max_kv: int,
+                           num_splits: int = 0, flags: int = 0) -> int:
+    """pkv_attend_workspace_bytes: workspace the attention calls need for these bounds (0: none)."""
+    n = int(lib.pkv_attend_workspace_bytes(cache.ref(), int(num_q_heads), int(num_segments), int(max_q_len),
+                                           int(max_kv), int(num_splits), int(flags)))
+    if n < 0:
+        _lib.check("pkv_attend_workspace_bytes", n)
+    return n
+
+
+def new_workspace(cache: PagedKVCache, num_q_heads: int, num_segments: int, max_q_len: int, max_kv: int,
+                  num_splits: int = 0, flags: int = 0) -> Optional[torch.Tensor]:
+    """A zero-filled workspace for these bounds on the cache's device, or None if none is needed."""
+    n = attend_workspace_bytes(cache, num_q_heads, num_segments, max_q_len, max_kv, num_splits, flags)
+    return torch.zeros(n, dtype=torch.uint8, device=cache.k[0].device) if n > 0 else None
 
 
 def seqinfo_from_seqused(cu_seqlens_q: torch.Tensor, seqused_k: torch.Tensor, out: torch.Tensor,

@@ -49,7 +49,36 @@ int check_layer(const pkv_cache *c, int layer) {
 struct Plan {
     AttnKernel k;
     int G, rows_max, row_tiles, units, ncta;
+    bool gm;  // decode kernel merging its splits through a global workspace (no cluster)
 };
+
+constexpr int kMaxSplitsGm = 64;  // splits per key range when merging through global memory
+
+// SMs of the current device (GB300's count when no device answers).
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return kDefaultSms;
+    }
+    return n > 0 ? n : kDefaultSms;
+}
+
+// Workspace layout of the global merge: partial rows, (max, sum), flags,
+// counters, each region 256-byte aligned.
+struct WsLayout {
+    size_t part, stat, flag, count, total;
+};
+WsLayout ws_layout(long long units, int ncta, int dp) {
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    WsLayout w;
+    w.part = 0;
+    w.stat = al(w.part + (size_t)units * ncta * 8 * dp * 4);
+    w.flag = al(w.stat + (size_t)units * ncta * 8 * 8);
+    w.count = al(w.flag + (size_t)units * ncta * 4);
+    w.total = al(w.count + (size_t)units * 4);
+    return w;
+}
 
 AttnKernel pick(int variant, int dp, int rc) {
     switch (variant * 1000 + dp) {
@@ -110,11 +139,11 @@ int schedulable_cluster(const AttnKernel &k, int want) {
 }
 
 int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv, int num_splits,
-              unsigned flags, Plan *pl) {
+              unsigned flags, bool want_gm, Plan *pl) {
     int st = check_cache(c);
     if (st) return st;
     if (Hq <= 0 || Hq % c->kv_heads != 0) return PKV_EINVAL;
-    if (S < 0 || S > 65535 || max_q_len <= 0 || max_kv <= 0 || num_splits < 0 || num_splits > kMaxCluster)
+    if (S < 0 || S > 65535 || max_q_len <= 0 || max_kv <= 0 || num_splits < 0 || num_splits > kMaxSplitsGm)
         return PKV_EINVAL;
     const int D = c->head_dim;
     const int dp = D <= 64 ? 64 : D <= 128 ? 128 : 256;
@@ -128,12 +157,22 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
                    : rows_max <= 16 ? 0 : rows_max <= 32 ? 1 : rows_max <= 64 ? 2 : 3;
     pl->k = pick(variant, dp, rc);
     if (!pl->k.fn) return PKV_EUNSUPPORTED;
+    pl->gm = want_gm && rc == 4;
+    if (!pl->gm && num_splits > kMaxCluster) return PKV_EINVAL;
     pl->row_tiles = (int)((rows_max + pl->k.rows - 1) / pl->k.rows);
     if ((long long)c->kv_heads * pl->row_tiles > 65535) return PKV_EINVAL;
     const long long units = (long long)std::max(S, 1) * c->kv_heads * pl->row_tiles;
     pl->units = (int)units;
     const long long max_pages = (max_kv + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE + 1;
     long long n = num_splits;
+    if (pl->gm) {
+        // independent CTAs: one per SM across the launch (the next layer's
+        // CTAs take the second slot of each SM), at least 4 pages each
+        if (n == 0) n = std::min<long long>({(device_sms() + units - 1) / units, std::max<long long>(1, max_pages / 4),
+                                             (long long)kMaxSplitsGm});
+        pl->ncta = (int)std::max<long long>(1, std::min<long long>(n, max_pages));
+        return PKV_OK;
+    }
     if (n == 0) {
         const long long want = (kTargetCtas + units - 1) / units;
         n = 1;
@@ -242,10 +281,11 @@ int encode_pool_pages(CUtensorMap *map, const void *pool, const pkv_cache *c) {
 int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_new, const void *v_new,
                   int Hq, int total_rows, const int *seq_info, int S, int max_q_len, long long max_kv,
                   int num_splits, float scale, int causal, int window, float *out, float *lse,
-                  unsigned *err, unsigned flags, void *stream) {
+                  void *workspace, long long workspace_bytes, unsigned *err, unsigned flags, void *stream) {
     Plan pl;
-    int st = make_plan(c, Hq, S, max_q_len, max_kv, num_splits, flags, &pl);
+    int st = make_plan(c, Hq, S, max_q_len, max_kv, num_splits, flags, workspace != nullptr, &pl);
     if (st) return st;
+    if (workspace && (!aligned16(workspace) || workspace_bytes < 0)) return PKV_EINVAL;
     if ((st = check_layer(c, layer))) return st;
     if (total_rows < 0 || window < 0 || (causal != 0 && causal != 1)) return PKV_EINVAL;
     if (!err || !out || (total_rows > 0 && (!q || !aligned16(q)))) return PKV_EINVAL;
@@ -254,8 +294,11 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
         return PKV_EINVAL;
     if (k_new && (!v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
     if (S == 0 && total_rows == 0) return PKV_OK;
+    const bool gm = pl.gm && S > 0 && pl.ncta > 1;
+    const WsLayout wl = ws_layout((long long)S * c->kv_heads * pl.row_tiles, pl.ncta, pl.k.dp);
+    if (gm && workspace_bytes < (long long)wl.total) return PKV_EINVAL;
     if ((st = prepare_kernel(pl.k))) return st;
-    const int ncta = S == 0 ? 1 : schedulable_cluster(pl.k, pl.ncta);
+    const int ncta = S == 0 ? 1 : pl.gm ? pl.ncta : schedulable_cluster(pl.k, pl.ncta);
 
     AttendParams p;
     // The decode kernel takes a page tile in one box when head_dim fills its
@@ -291,6 +334,17 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     p.causal = causal;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.ws_part = nullptr;
+    p.ws_stat = nullptr;
+    p.ws_flag = nullptr;
+    p.ws_count = nullptr;
+    if (gm) {
+        char *base = reinterpret_cast<char *>(workspace);
+        p.ws_part = reinterpret_cast<float *>(base + wl.part);
+        p.ws_stat = reinterpret_cast<float2 *>(base + wl.stat);
+        p.ws_flag = reinterpret_cast<int *>(base + wl.flag);
+        p.ws_count = reinterpret_cast<int *>(base + wl.count);
+    }
     p.k_next = p.v_next = nullptr;
     p.pf_next = 0;
     if ((flags & PKV_FLAG_PREFETCH_NEXT) && layer + 1 < c->num_layers && S > 0 && !check_layer(c, layer + 1)) {
@@ -311,7 +365,7 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (ncta > 1) {
+    if (ncta > 1 && !gm) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = (unsigned)ncta;
         attr[na].val.clusterDim.y = 1;
@@ -399,20 +453,31 @@ int pkv_append(const pkv_cache *c, int32_t layer, const void *k_new, const void 
 
 int pkv_attend_varlen(const pkv_cache *c, int32_t layer, const void *q, int32_t Hq, int32_t total_rows,
                       const int32_t *seq_info, int32_t S, int32_t max_q_len, int64_t max_kv, int32_t num_splits,
-                      float scale, int32_t causal, int32_t window, float *out, float *lse, uint32_t *err,
-                      uint32_t flags, void *stream) {
+                      float scale, int32_t causal, int32_t window, float *out, float *lse, void *workspace,
+                      int64_t workspace_bytes, uint32_t *err, uint32_t flags, void *stream) {
     return attend_common(c, layer, q, nullptr, nullptr, Hq, total_rows, seq_info, S, max_q_len, max_kv,
-                         num_splits, scale, causal, window, out, lse, err, flags, stream);
+                         num_splits, scale, causal, window, out, lse, workspace, workspace_bytes, err, flags,
+                         stream);
 }
 
 int pkv_append_attend(const pkv_cache *c, int32_t layer, const void *q, const void *k_new, const void *v_new,
                       int32_t Hq, int32_t total_rows, const int32_t *seq_info, int32_t S, int32_t max_q_len,
                       int64_t max_kv, int32_t num_splits, float scale, int32_t causal, int32_t window,
-                      float *out, float *lse, uint32_t *err, uint32_t flags, void *stream) {
+                      float *out, float *lse, void *workspace, int64_t workspace_bytes, uint32_t *err,
+                      uint32_t flags, void *stream) {
     if (total_rows > 0 && (!k_new || !v_new)) return PKV_EINVAL;
     return attend_common(c, layer, q, total_rows > 0 ? k_new : nullptr, total_rows > 0 ? v_new : nullptr, Hq,
                          total_rows, seq_info, S, max_q_len, max_kv, num_splits, scale, causal, window, out, lse,
-                         err, flags, stream);
+                         workspace, workspace_bytes, err, flags, stream);
+}
+
+int64_t pkv_attend_workspace_bytes(const pkv_cache *c, int32_t Hq, int32_t S, int32_t max_q_len, int64_t max_kv,
+                                   int32_t num_splits, uint32_t flags) {
+    Plan pl;
+    const int st = make_plan(c, Hq, S, max_q_len, max_kv, num_splits, flags, true, &pl);
+    if (st) return st;
+    if (!pl.gm || S == 0 || pl.ncta <= 1) return 0;
+    return (int64_t)ws_layout((long long)S * c->kv_heads * pl.row_tiles, pl.ncta, pl.k.dp).total;
 }
 
 int pkv_seqinfo_from_seqused(const int32_t *cu, const int32_t *used, int32_t n, int32_t *out, void *stream) {

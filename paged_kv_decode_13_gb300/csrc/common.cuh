@@ -188,6 +188,13 @@ struct AttendParams {
     const void *k_next;
     const void *v_next;
     int pf_next;
+    // Split-K merge through global memory instead of the cluster (decode
+    // kernel with a workspace): per (segment, kv head) unit the partial rows,
+    // their (max, sum), flags and an arrival counter; all null = cluster merge.
+    float *ws_part;         // [units][ncta][8][DP]
+    float2 *ws_stat;        // [units][ncta][8]
+    int *ws_flag;           // [units][ncta]
+    int *ws_count;          // [units], zero between calls
 };
 
 struct AppendParams {

@@ -169,13 +169,15 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     // the cluster's merge is skipped (uniformly: it depends on kv_end only).
     const bool solo = nblk <= kSoloPages * KW;
     const int ncl = solo ? 1 : ncta;  // CTAs that share the range
+    const bool gm = p.ws_count != nullptr;  // partials merged through global memory, no cluster
     const int bps = solo ? nblk : (nblk + ncta - 1) / ncta;
     const int active = bps > 0 ? (nblk + bps - 1) / bps : 0;
     const int cb0 = pb_begin + rank * bps;
     const int nb = rank < active ? min(cb0 + bps, pb_end) - cb0 : 0;
     const int n_mine = nb > kw ? (nb - kw + KW - 1) / KW : 0;
     if (solo && rank > 0 && !first_cta) return;  // nothing to read or write
-    if (ncl > 1)  // announce this CTA to the cluster; waited on before any remote store
+    if (gm && rank >= active && !first_cta) return;  // no pages; only the active CTAs take part in the merge
+    if (ncl > 1 && !gm)  // announce this CTA to the cluster; waited on before any remote store
         asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
 
     const T *knew = reinterpret_cast<const T *>(p.k_new);
@@ -569,7 +571,8 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     int lg = 0;
     while ((1 << lg) * ncl < DP) ++lg;
     const int per = 1 << lg;
-    if (ncl > 1) {
+    const int unit = blockIdx.z * gridDim.y + blockIdx.y;
+    if (ncl > 1 && !gm) {
         // Every CTA of the cluster has started (the arrive at the top), so
         // peers' shared memory may be written from here on.
         asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
@@ -616,6 +619,12 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
                 for (int e = 0; e < CB; ++e)
                     if (d0 + e < p.D) p.out[orow * p.D + d0 + e] = zero ? 0.f : o[e] * inv;  // o may be NaN when poisoned
                 if (cq == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
+            } else if (gm) {
+                float *dst = p.ws_part + (((size_t)unit * ncta + rank) * C::kRows + n) * DP + d0;
+#pragma unroll
+                for (int e = 0; e < CB; e += 4)
+                    *reinterpret_cast<float4 *>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                if (cq == 0) p.ws_stat[((size_t)unit * ncta + rank) * C::kRows + n] = make_float2(M, L);
             } else {
                 float *dst = cluster.map_shared_rank(sRecv + ((rank * C::kRows + n) << lg) + (d0 & (per - 1)), d0 >> lg);
 #pragma unroll
@@ -626,6 +635,99 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         }
     }
     if (ncl == 1) return;
+
+    if (gm) {
+        // ---- the last of the range's CTAs to arrive merges every partial
+        if (tid == 0) p.ws_flag[(size_t)unit * ncta + rank] = flags;
+        __threadfence();  // this CTA's partial is visible before its arrival is counted
+        __syncthreads();
+        if (tid == 0) sFlag[20] = atomicAdd(p.ws_count + unit, 1) == active - 1;
+        __syncthreads();
+        if (!sFlag[20]) return;
+        __threadfence();
+        const float *wp = p.ws_part + (size_t)unit * ncta * C::kRows * DP;
+        const float2 *wst = p.ws_stat + (size_t)unit * ncta * C::kRows;
+        const int poison = __syncthreads_or(tid < active && __ldcg(p.ws_flag + (size_t)unit * ncta + tid) != 0);
+        float *sWg = sRecv;  // [8][64] normalised weights (the cluster's receive buffer is unused here)
+        {   // thread = (row n, sources c16, c16 + 16, ...): max and sum by 16-lane shuffles
+            const int n = tid >> 4, c16 = tid & 15;
+            float mc[4], lc[4], M = -CUDART_INF_F;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = c16 + 16 * i;
+                const float2 st = (c < active && n < rows_unit) ? __ldcg(wst + (size_t)c * C::kRows + n)
+                                                                : make_float2(-CUDART_INF_F, 0.f);
+                mc[i] = st.x;
+                lc[i] = st.y;
+                M = fmaxf(M, st.x);
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float w[4], W = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                // A zero weight must not touch its partial: a poisoned one may hold NaN.
+                w[i] = (M == -CUDART_INF_F || mc[i] == -CUDART_INF_F) ? 0.f : exp2f(mc[i] - M);
+                W = fmaf(w[i], lc[i], W);
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+            const bool zero = poison || !(W > 0.f);
+            const float inv = zero ? 0.f : 1.f / W;
+            if (n < C::kRows)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sWg[n * 64 + c16 + 16 * i] = zero ? 0.f : w[i] * inv;  // w may be NaN when poisoned
+            if (c16 == 0 && n < rows_unit && p.lse) p.lse[out_row(n)] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+        }
+        // The partials' rows are staged in shared memory (the idle stages) with
+        // 16-byte async copies, all in flight together, as many partials per
+        // batch as fit; each thread then sums its elements from there.
+        constexpr int EPT = C::kRows * DP / NT;  // elements per thread at most
+        float acc[EPT];
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) acc[i] = 0.f;
+        float *stg = reinterpret_cast<float *>(pipe);
+        const int q4 = DP / 4, per_c = rows_unit * q4;  // 16-byte chunks per partial
+        const int cap = (int)(C::kPipeBytes / ((size_t)rows_unit * DP * 4));
+        #pragma unroll 1
+        for (int c0 = 0; c0 < active; c0 += cap) {
+            const int nc = min(cap, active - c0);
+            __syncthreads();  // weights written / previous batch consumed
+            #pragma unroll 1
+            for (int x = tid; x < nc * per_c; x += NT) {
+                const int c = x / per_c, r = x - c * per_c, n = r / q4, ch = r - n * q4;
+                const unsigned dst = smem_u32(stg + ((size_t)c * rows_unit + n) * DP + ch * 4);
+                const float *src = wp + ((size_t)(c0 + c) * C::kRows + n) * DP + ch * 4;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+            }
+            asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                const int e = tid + i * NT;
+                if (e < rows_unit * DP) {
+                    const int n = e / DP, d = e - n * DP;
+                    float o = acc[i];
+                    #pragma unroll 4
+                    for (int c = 0; c < nc; ++c) {
+                        const float w = sWg[n * 64 + c0 + c];
+                        o += w != 0.f ? w * stg[((size_t)c * rows_unit + n) * DP + d] : 0.f;
+                    }
+                    acc[i] = o;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+            const int e = tid + i * NT;
+            if (e < rows_unit * DP) {
+                const int n = e / DP, d = e - n * DP;
+                if (d < p.D) p.out[out_row(n) * p.D + d] = acc[i];
+            }
+        }
+        if (tid == 0) p.ws_count[unit] = 0;  // ready for the next call
+        return;
+    }
 
     // ---- merge the cluster's partials of this CTA's columns
     cluster.sync();  // publishes every CTA's pushed partials

@@ -18,7 +18,7 @@ from typing import Dict, Optional, Tuple
 import torch
 
 from . import _lib
-from .api import PagedKVCache, append, append_attend, attend_varlen, new_err_flags
+from .api import PagedKVCache, append, append_attend, attend_varlen, new_err_flags, new_workspace
 
 _SHARED_POOL = None
 
@@ -36,7 +36,8 @@ class DecodeStep:
     def __init__(self, cache: PagedKVCache, num_q_heads: int, rows: int = 1, num_segments: int = 1,
                  max_q_len: int = 1, max_kv: Optional[int] = None, scale: Optional[float] = None,
                  causal: bool = False, window: int = 0, fused: bool = True, pdl: bool = True,
-                 flags: int = 0, num_splits: int = 0, with_lse: bool = False, prefetch_next: bool = True):
+                 flags: int = 0, num_splits: int = 0, with_lse: bool = False, prefetch_next: bool = True,
+                 workspace: bool = False):
         dev = cache.k[0].device
         L, Hkv, D = cache.num_layers, cache.kv_heads, cache.head_dim
         self.cache = cache
@@ -55,6 +56,16 @@ class DecodeStep:
             if with_lse else [None] * L
         self.seq_info = torch.zeros(num_segments, 4, dtype=torch.int32, device=dev)
         self.err = new_err_flags(dev)
+        self.use_workspace = workspace
+        self.ws = None
+        self.size_workspace()
+
+    def size_workspace(self) -> None:
+        """(Re)allocate the split-merge workspace for the current cache and bounds (None when not needed)."""
+        self.ws = None
+        if self.use_workspace:
+            self.ws = new_workspace(self.cache, self.num_q_heads, int(self.seq_info.shape[0]), self.max_q_len,
+                                    self.max_kv, self.num_splits, self.flags)
 
     def launch_count(self) -> int:
         return self.cache.num_layers * (1 if self.fused else 2)
@@ -72,13 +83,13 @@ class DecodeStep:
                 append_attend(c, layer, self.q[layer], self.k_new[layer], self.v_new[layer], self.seq_info,
                               self.out[layer], self.err, self.max_q_len, self.max_kv, self.scale, self.causal,
                               self.window, lse=self.lse[layer], num_splits=self.num_splits, flags=flags,
-                              stream=stream)
+                              stream=stream, workspace=self.ws)
             else:
                 append(c, layer, self.k_new[layer], self.v_new[layer], self.seq_info, self.err,
                        window=self.window, stream=stream)
                 attend_varlen(c, layer, self.q[layer], self.seq_info, self.out[layer], self.err, self.max_q_len,
                               self.max_kv, self.scale, self.causal, self.window, lse=self.lse[layer],
-                              num_splits=self.num_splits, flags=flags, stream=stream)
+                              num_splits=self.num_splits, flags=flags, stream=stream, workspace=self.ws)
 
 
 class DecodeGraphRunner:
@@ -108,6 +119,7 @@ class DecodeGraphRunner:
         st = self.step_bufs
         st.cache = cache
         st.max_kv = cache.bucket
+        st.size_workspace()
         self._graphs = {k: g for k, g in self._graphs.items() if k == (cache.bucket, cache.generation)}
 
     def graph_for(self) -> torch.cuda.CUDAGraph:

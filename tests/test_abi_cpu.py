@@ -88,7 +88,7 @@ def test_bad_cache_rejected_before_launch(lib, field, value, status):
     d, keep = _desc(lib, **{field: value})
     L = lib.lib
     st = L.pkv_attend_varlen(ctypes.byref(d), 0, 0x4000, 8, 1, 0x5000, 1, 1, 512, 0, 0.125, 0, 0,
-                             0x6000, None, 0x7000, 0, None)
+                             0x6000, None, None, 0, 0x7000, 0, None)
     assert st == status
     st = L.pkv_append(ctypes.byref(d), 0, 0x4000, 0x4000, 1, 0x5000, 1, 0, 0x7000, None)
     assert st == status
@@ -101,11 +101,11 @@ def test_bad_call_arguments_rejected(lib):
 
     def attend(**kw):
         a = dict(layer=0, q=0x4000, hq=8, rows=1, si=0x5000, S=1, mq=1, mk=512, ns=0, scale=1.0, causal=0,
-                 window=0, out=0x6000, lse=None, err=0x7000, flags=0)
+                 window=0, out=0x6000, lse=None, ws=None, wsb=0, err=0x7000, flags=0)
         a.update(kw)
         return L.pkv_attend_varlen(ref, a["layer"], a["q"], a["hq"], a["rows"], a["si"], a["S"], a["mq"], a["mk"],
-                                   a["ns"], a["scale"], a["causal"], a["window"], a["out"], a["lse"], a["err"],
-                                   a["flags"], None)
+                                   a["ns"], a["scale"], a["causal"], a["window"], a["out"], a["lse"], a["ws"],
+                                   a["wsb"], a["err"], a["flags"], None)
 
     assert attend(hq=3) == -1              # q heads not a multiple of kv heads
     assert attend(layer=1) == -1           # layer out of range
@@ -115,15 +115,36 @@ def test_bad_call_arguments_rejected(lib):
     assert attend(causal=2) == -1
     assert attend(window=-1) == -1
     assert attend(ns=17) == -1             # more splits than a cluster can hold
+    assert attend(ns=65, ws=0x8000, wsb=1 << 30) == -1   # more than the workspace mode allows
+    assert attend(ns=17, ws=0x8000, wsb=16) == -1        # workspace smaller than the split merge needs
+    assert attend(ws=0x8004, wsb=1 << 30) == -1          # misaligned workspace
     assert attend(ns=-1) == -1
     assert attend(mq=0) == -1
     assert attend(mk=0) == -1
     assert attend(S=-1) == -1
     # fused call without k_new / v_new
     assert L.pkv_append_attend(ref, 0, 0x4000, None, None, 8, 1, 0x5000, 1, 1, 512, 0, 1.0, 0, 0, 0x6000,
-                               None, 0x7000, 0, None) == -1
+                               None, None, 0, 0x7000, 0, None) == -1
     # nothing to do: no rows and no segments
     assert attend(rows=0, S=0) == 0
+
+
+def test_workspace_size_query(lib):
+    L = lib.lib
+    d, keep = _desc(lib)   # bf16, 2 kv heads, head_dim 64, 512 tokens
+    ref = ctypes.byref(d)
+    # decode kernel (8 q heads over 2 kv heads, one row each): splits merge through the workspace
+    n = L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 0, 0)
+    assert n > 0 and n % 256 == 0
+    # more segments need more
+    assert L.pkv_attend_workspace_bytes(ref, 8, 4, 1, 512, 0, 0) > n
+    # one split: nothing to merge
+    assert L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 1, 0) == 0
+    # 16 query rows per kv head: the wide kernel, which merges in the cluster
+    assert L.pkv_attend_workspace_bytes(ref, 8, 1, 4, 512, 0, 0) == 0
+    # the CUDA-core path never uses one
+    assert L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 0, 1) == 0
+    assert L.pkv_attend_workspace_bytes(ref, 3, 1, 1, 512, 0, 0) == -1
 
 
 def test_resize_and_prefix_host_rules(lib):

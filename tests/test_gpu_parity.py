@@ -25,8 +25,10 @@ def pkv():
     return m
 
 
-def run(pkv, w, layer=0, fused=True, flags=0, num_splits=0, max_q_len=None, max_kv=None, canary=True):
-    """Append + attend layer `layer` of w on the GPU.  Returns (out, lse, err, cache)."""
+def run(pkv, w, layer=0, fused=True, flags=0, num_splits=0, max_q_len=None, max_kv=None, canary=True,
+        workspace=False):
+    """Append + attend layer `layer` of w on the GPU.  Returns (out, lse, err, cache).  With
+    workspace=True the split merge goes through a workspace (decode kernel) instead of the cluster."""
     cache = U.device_cache(pkv, w, canary=canary)
     dev = torch.device("cuda")
     q = w.q[layer].to(dev)
@@ -38,16 +40,26 @@ def run(pkv, w, layer=0, fused=True, flags=0, num_splits=0, max_q_len=None, max_
     obuf, out = U.guarded_out(w.total_rows, w.q_heads, w.head_dim)
     lse = torch.full((max(w.total_rows, 1), w.q_heads), 3.0, device=dev)[:w.total_rows]
     err = pkv.new_err_flags()
+    ws = None
+    if workspace:
+        ws = pkv.new_workspace(cache, w.q_heads, w.num_segments, mq, mk, num_splits, flags)
+        if ws is not None:  # guard margin: the call must not write past the size it asked for
+            n = ws.numel()
+            ws_buf = torch.full((n + 1024,), 0x5A, dtype=torch.uint8, device=dev)
+            ws_buf[:n].zero_()
+            ws = ws_buf[:n]
     if fused:
         pkv.append_attend(cache, layer, q, kn, vn, si, out, err, mq, mk, w.scale, w.causal, w.window, lse=lse,
-                          num_splits=num_splits, flags=flags)
+                          num_splits=num_splits, flags=flags, workspace=ws)
     else:
         pkv.append(cache, layer, kn, vn, si, err, window=w.window)
         pkv.attend_varlen(cache, layer, q, si, out, err, mq, mk, w.scale, w.causal, w.window, lse=lse,
-                          num_splits=num_splits, flags=flags)
+                          num_splits=num_splits, flags=flags, workspace=ws)
     torch.cuda.synchronize()
     U.check_guarded(obuf)
     U.check_canaries(cache)
+    if ws is not None:
+        assert bool((ws_buf[ws.numel():] == 0x5A).all()), "write past the workspace"
     return out, lse, int(err.item()), cache
 
 
@@ -198,6 +210,58 @@ def test_decode_windows_edge_pages(pkv, window):
     out, lse, err, cache = run(pkv, w, max_kv=3000)
     assert err == 0
     check_against_oracle(w, 0, out, lse, cache)
+
+
+def _ws_workload(kind):
+    if kind == "single_8192":
+        return U.nan_tails(workloads.sensenova(8190, 8192, num_layers=1, seed=21))
+    if kind == "single_1000":
+        return U.nan_tails(workloads.sensenova(1000, 1024, num_layers=1, seed=22))
+    if kind == "batched":
+        return U.nan_tails(workloads.batched(S=32, max_len=4000, seed=23, num_layers=1))
+    if kind == "narrow_rows":
+        return U.nan_tails(workloads.spec_verify(S=6, max_q=2, len_lo=1, len_hi=3000, causal=True, seed=24,
+                                                 q_heads=32))
+    return U.nan_tails(workloads.long_context(S=3, kv_len=20000, window=1000, ring_rows=1024, seed=25, num_layers=1,
+                                              q_heads=32, kv_heads=4, head_dim=256))
+
+
+@pytest.mark.parametrize("kind", ["single_8192", "single_1000", "batched", "narrow_rows", "ring_d256"])
+@pytest.mark.parametrize("num_splits", [0, 3, 19, 64])
+def test_workspace_merge_matches_oracle(pkv, kind, num_splits):
+    # independent CTAs merging through the workspace, any split count up to 64
+    w = _ws_workload(kind)
+    mk = int(w.seq_info[:, 3].max())
+    out, lse, err, cache = run(pkv, w, max_kv=mk, num_splits=num_splits, workspace=True)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+def test_workspace_is_reusable_and_poison_zeroes(pkv):
+    w = U.nan_tails(workloads.sensenova(3000, 4096, num_layers=1, seed=26))
+    dev = torch.device("cuda")
+    cache = U.device_cache(pkv, w)
+    ws = pkv.new_workspace(cache, w.q_heads, 1, 1, 4096, 0)
+    assert ws is not None
+    outs = []
+    for _ in range(3):  # the counters return to zero: every call merges the same way
+        out = torch.zeros(1, w.q_heads, w.head_dim, device=dev)
+        err = pkv.new_err_flags()
+        pkv.attend_varlen(cache, 0, w.q[0].to(dev), w.seq_info.to(dev), out, err, 1, 4096, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(out.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    # a bad block id in one split's range: the merged rows are zero, the flag is set
+    bt = cache.block_table
+    bt[0, 100] = w.num_blocks + 5
+    out = torch.full((1, w.q_heads, w.head_dim), 9.0, device=dev)
+    err = pkv.new_err_flags()
+    pkv.attend_varlen(cache, 0, w.q[0].to(dev), w.seq_info.to(dev), out, err, 1, 4096, w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.ERR_BLOCK
+    assert not out.abs().sum().item()
 
 
 @pytest.mark.parametrize("window,ring", [(0, 0), (1000, 0), (1024, 1024), (300, 320)])
