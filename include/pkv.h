@@ -226,14 +226,37 @@ int pkv_append_attend(const pkv_cache *cache, int32_t layer,
  * merges them.  Without one (NULL), the splits form a thread-block cluster
  * and merge through distributed shared memory (num_splits 0..16).  The
  * workspace is device memory the caller owns, 16-byte aligned, zero-filled
- * before its first use and not touched by the caller between calls (each
- * call leaves its counters at zero); calls that may run concurrently need
- * their own.  A workspace smaller than this size is rejected with
+ * before its first use and not touched by the caller between calls: its
+ * first bytes are per-range arrival counters that every call leaves at zero,
+ * the rest is scratch.  Used with larger launch bounds (more segments or kv
+ * heads) than before, it must be zero-filled again.  Calls that may run
+ * concurrently need their own.  A workspace smaller than this size is rejected with
  * PKV_EINVAL.  Returns a negative pkv_status for invalid bounds.
  */
 int64_t pkv_attend_workspace_bytes(const pkv_cache *cache, int32_t num_q_heads,
                                    int32_t num_segments, int32_t max_q_len,
                                    int64_t max_kv, int32_t num_splits, uint32_t flags);
+
+/*
+ * pkv_append_attend with the split-merge workspace taken from a fixed 8 MiB
+ * scratch array in the library's device memory instead of the caller: no
+ * allocation, no workspace argument.  The pages have no counterpart of this
+ * call; it exists for callers that may not allocate (the scratch is a
+ * file-scope device array, zero at load, left zeroed by every call).  A
+ * launch whose merge would need more than 8 MiB (see
+ * pkv_attend_workspace_bytes) or more than 4096 (segment, kv head) ranges is
+ * rejected with PKV_ECAPACITY before anything runs.  The scratch is shared by every call on a device, so calls must not
+ * run concurrently (one stream, or serialised).  Otherwise the same
+ * arguments, results and errors as pkv_append_attend.
+ */
+int pkv_append_attend_noalloc(const pkv_cache *cache, int32_t layer,
+                              const void *q, const void *k_new, const void *v_new,
+                              int32_t num_q_heads, int32_t total_rows,
+                              const int32_t *seq_info, int32_t num_segments,
+                              int32_t max_q_len, int64_t max_kv, int32_t num_splits,
+                              float softmax_scale, int32_t causal, int32_t window,
+                              float *out, float *lse,
+                              uint32_t *err_flags, uint32_t flags, void *stream);
 
 /*
  * Build a segment table from the flash-attention argument form

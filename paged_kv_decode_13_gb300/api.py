@@ -153,6 +153,20 @@ def append_attend(cache: PagedKVCache, layer: int, q: torch.Tensor, k_new: torch
             causal, window, num_splits, flags, stream, workspace)
 
 
+def append_attend_noalloc(cache: PagedKVCache, layer: int, q: torch.Tensor, k_new: torch.Tensor,
+                          v_new: torch.Tensor, seq_info: torch.Tensor, out: torch.Tensor, err: torch.Tensor,
+                          max_q_len: int, max_kv: int, scale: float, causal: bool = False, window: int = 0,
+                          lse: Optional[torch.Tensor] = None, num_splits: int = 0, flags: int = 0,
+                          stream=None) -> None:
+    """pkv_append_attend_noalloc: append_attend merging its splits in the library's fixed scratch."""
+    rows, hq = int(q.shape[0]), int(q.shape[1])
+    _lib.check("pkv_append_attend_noalloc", lib.pkv_append_attend_noalloc(
+        cache.ref(), layer, _ptr(_contig(q, "q")), _ptr(_contig(k_new, "k_new")), _ptr(_contig(v_new, "v_new")),
+        hq, rows, _ptr(_contig(seq_info, "seq_info")), int(seq_info.shape[0]), int(max_q_len), int(max_kv),
+        int(num_splits), float(scale), int(bool(causal)), int(window), _ptr(_contig(out, "out")), _ptr(lse),
+        _ptr(err), int(flags), _stream(stream)))
+
+
 def attend_workspace_bytes(cache: PagedKVCache, num_q_heads: int, num_segments: int, max_q_len: int, max_kv: int,
                            num_splits: int = 0, flags: int = 0) -> int:
     """pkv_attend_workspace_bytes: workspace the attention calls need for these bounds (0: none)."""

@@ -69,14 +69,15 @@ int device_sms() {
 struct WsLayout {
     size_t part, stat, flag, count, total;
 };
+// The counters come first, at a place that depends only on the unit count.
 WsLayout ws_layout(long long units, int ncta, int dp) {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
     WsLayout w;
-    w.part = 0;
+    w.count = 0;
+    w.part = al((size_t)units * 4);
     w.stat = al(w.part + (size_t)units * ncta * 8 * dp * 4);
     w.flag = al(w.stat + (size_t)units * ncta * 8 * 8);
-    w.count = al(w.flag + (size_t)units * ncta * 4);
-    w.total = al(w.count + (size_t)units * 4);
+    w.total = al(w.flag + (size_t)units * ncta * 4);
     return w;
 }
 
@@ -281,7 +282,8 @@ int encode_pool_pages(CUtensorMap *map, const void *pool, const pkv_cache *c) {
 int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_new, const void *v_new,
                   int Hq, int total_rows, const int *seq_info, int S, int max_q_len, long long max_kv,
                   int num_splits, float scale, int causal, int window, float *out, float *lse,
-                  void *workspace, long long workspace_bytes, unsigned *err, unsigned flags, void *stream) {
+                  void *workspace, long long workspace_bytes, unsigned *err, unsigned flags, void *stream,
+                  int *counters = nullptr) {
     Plan pl;
     int st = make_plan(c, Hq, S, max_q_len, max_kv, num_splits, flags, workspace != nullptr, &pl);
     if (st) return st;
@@ -343,7 +345,7 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
         p.ws_part = reinterpret_cast<float *>(base + wl.part);
         p.ws_stat = reinterpret_cast<float2 *>(base + wl.stat);
         p.ws_flag = reinterpret_cast<int *>(base + wl.flag);
-        p.ws_count = reinterpret_cast<int *>(base + wl.count);
+        p.ws_count = counters ? counters : reinterpret_cast<int *>(base + wl.count);
     }
     p.k_next = p.v_next = nullptr;
     p.pf_next = 0;
@@ -393,6 +395,42 @@ int copy_rows(const void *s0, const void *s1, void *d0, void *d1, long long n, i
     const long long blocks = std::min<long long>((total + 255) / 256, (long long)kDefaultSms * 8);
     strided_copy_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     return launch_status(cudaSuccess);
+}
+
+// Fixed split-merge scratch of pkv_append_attend_noalloc: file-scope device
+// memory (zero at module load; every call leaves its counters at zero), so
+// that entry point never allocates.
+// The arrival counters live in an array of their own, so they are zero at
+// every call whatever shape the previous call had.
+constexpr long long kStaticScratchBytes = 8ll << 20;
+constexpr int kStaticUnits = 4096;
+static __device__ __align__(256) unsigned char g_split_scratch[kStaticScratchBytes];
+static __device__ __align__(256) int g_split_counters[kStaticUnits];
+
+// Device addresses of g_split_scratch and g_split_counters on the current
+// device (looked up once per device).
+bool static_scratch(void **scratch, int **counters) {
+    static std::mutex mu;
+    static void *addr[64][2] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev][0]) {
+        void *a = nullptr, *b = nullptr;
+        if (cudaGetSymbolAddress(&a, g_split_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress(&b, g_split_counters) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        addr[dev][0] = a;
+        addr[dev][1] = b;
+    }
+    *scratch = addr[dev][0];
+    *counters = reinterpret_cast<int *>(addr[dev][1]);
+    return true;
 }
 
 }  // namespace
@@ -469,6 +507,23 @@ int pkv_append_attend(const pkv_cache *c, int32_t layer, const void *q, const vo
     return attend_common(c, layer, q, total_rows > 0 ? k_new : nullptr, total_rows > 0 ? v_new : nullptr, Hq,
                          total_rows, seq_info, S, max_q_len, max_kv, num_splits, scale, causal, window, out, lse,
                          workspace, workspace_bytes, err, flags, stream);
+}
+
+int pkv_append_attend_noalloc(const pkv_cache *c, int32_t layer, const void *q, const void *k_new,
+                              const void *v_new, int32_t Hq, int32_t total_rows, const int32_t *seq_info, int32_t S,
+                              int32_t max_q_len, int64_t max_kv, int32_t num_splits, float scale, int32_t causal,
+                              int32_t window, float *out, float *lse, uint32_t *err, uint32_t flags, void *stream) {
+    const int64_t need = pkv_attend_workspace_bytes(c, Hq, S, max_q_len, max_kv, num_splits, flags);
+    if (need < 0) return (int)need;
+    if (need > kStaticScratchBytes || (need > 0 && (long long)S * c->kv_heads > kStaticUnits))
+        return PKV_ECAPACITY;  // rejected before any launch
+    void *ws = nullptr;
+    int *counters = nullptr;
+    if (need > 0 && !static_scratch(&ws, &counters)) return PKV_ECUDA;
+    if (total_rows > 0 && (!k_new || !v_new)) return PKV_EINVAL;
+    return attend_common(c, layer, q, total_rows > 0 ? k_new : nullptr, total_rows > 0 ? v_new : nullptr, Hq,
+                         total_rows, seq_info, S, max_q_len, max_kv, num_splits, scale, causal, window, out, lse, ws,
+                         need > 0 ? kStaticScratchBytes : 0, err, flags, stream, counters);
 }
 
 int64_t pkv_attend_workspace_bytes(const pkv_cache *c, int32_t Hq, int32_t S, int32_t max_q_len, int64_t max_kv,
