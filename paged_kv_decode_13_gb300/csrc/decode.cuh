@@ -647,28 +647,47 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         __threadfence();
         const float *wp = p.ws_part + (size_t)unit * ncta * C::kRows * DP;
         const float2 *wst = p.ws_stat + (size_t)unit * ncta * C::kRows;
-        const int poison = __syncthreads_or(tid < active && __ldcg(p.ws_flag + (size_t)unit * ncta + tid) != 0);
-        float *sWg = sRecv;  // [8][64] normalised weights (the cluster's receive buffer is unused here)
-        {   // thread = (row n, sources c16, c16 + 16, ...): max and sum by 16-lane shuffles
-            const int n = tid >> 4, c16 = tid & 15;
-            float mc[4], lc[4], M = -CUDART_INF_F;
+        // Issue every global read at once: the statistics, the flags and the
+        // async copies staging the partials' rows in shared memory (the idle
+        // stages, as many partials per batch as fit).
+        const int n = tid >> 4, c16 = tid & 15;  // thread = (row n, sources c16, c16 + 16, ...)
+        float2 st[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = c16 + 16 * i;
-                const float2 st = (c < active && n < rows_unit) ? __ldcg(wst + (size_t)c * C::kRows + n)
-                                                                : make_float2(-CUDART_INF_F, 0.f);
-                mc[i] = st.x;
-                lc[i] = st.y;
-                M = fmaxf(M, st.x);
+        for (int i = 0; i < 4; ++i) {
+            const int c = c16 + 16 * i;
+            st[i] = (c < active && n < rows_unit) ? __ldcg(wst + (size_t)c * C::kRows + n)
+                                                  : make_float2(-CUDART_INF_F, 0.f);
+        }
+        const int fl = tid < active ? __ldcg(p.ws_flag + (size_t)unit * ncta + tid) : 0;
+        float *stg = reinterpret_cast<float *>(pipe);
+        const int q4 = DP / 4, per_c = rows_unit * q4;  // 16-byte chunks per partial
+        const int cap = (int)(C::kPipeBytes / ((size_t)rows_unit * DP * 4));
+        auto stage_batch = [&](int c0, int nc) {
+            #pragma unroll 1
+            for (int x = tid; x < nc * per_c; x += NT) {
+                const int c = x / per_c, r = x - c * per_c, nn = r / q4, ch = r - nn * q4;
+                const unsigned dst = smem_u32(stg + ((size_t)c * rows_unit + nn) * DP + ch * 4);
+                const float *src = wp + ((size_t)(c0 + c) * C::kRows + nn) * DP + ch * 4;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
             }
+            asm volatile("cp.async.commit_group;\n" ::: "memory");
+        };
+        int c0 = 0, nc = min(cap, active);
+        stage_batch(0, nc);
+        const int poison = __syncthreads_or(fl != 0);
+        float *sWg = sRecv;  // [8][64] normalised weights (the cluster's receive buffer is unused here)
+        {   // max and sum by 16-lane shuffles
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) M = fmaxf(M, st[i].x);
 #pragma unroll
             for (int o = 1; o < 16; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             float w[4], W = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 // A zero weight must not touch its partial: a poisoned one may hold NaN.
-                w[i] = (M == -CUDART_INF_F || mc[i] == -CUDART_INF_F) ? 0.f : exp2f(mc[i] - M);
-                W = fmaf(w[i], lc[i], W);
+                w[i] = (M == -CUDART_INF_F || st[i].x == -CUDART_INF_F) ? 0.f : exp2f(st[i].x - M);
+                W = fmaf(w[i], st[i].y, W);
             }
 #pragma unroll
             for (int o = 1; o < 16; o <<= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
@@ -679,50 +698,40 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
                 for (int i = 0; i < 4; ++i) sWg[n * 64 + c16 + 16 * i] = zero ? 0.f : w[i] * inv;  // w may be NaN when poisoned
             if (c16 == 0 && n < rows_unit && p.lse) p.lse[out_row(n)] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
         }
-        // The partials' rows are staged in shared memory (the idle stages) with
-        // 16-byte async copies, all in flight together, as many partials per
-        // batch as fit; each thread then sums its elements from there.
         constexpr int EPT = C::kRows * DP / NT;  // elements per thread at most
         float acc[EPT];
 #pragma unroll
         for (int i = 0; i < EPT; ++i) acc[i] = 0.f;
-        float *stg = reinterpret_cast<float *>(pipe);
-        const int q4 = DP / 4, per_c = rows_unit * q4;  // 16-byte chunks per partial
-        const int cap = (int)(C::kPipeBytes / ((size_t)rows_unit * DP * 4));
         #pragma unroll 1
-        for (int c0 = 0; c0 < active; c0 += cap) {
-            const int nc = min(cap, active - c0);
-            __syncthreads();  // weights written / previous batch consumed
-            #pragma unroll 1
-            for (int x = tid; x < nc * per_c; x += NT) {
-                const int c = x / per_c, r = x - c * per_c, n = r / q4, ch = r - n * q4;
-                const unsigned dst = smem_u32(stg + ((size_t)c * rows_unit + n) * DP + ch * 4);
-                const float *src = wp + ((size_t)(c0 + c) * C::kRows + n) * DP + ch * 4;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-            }
-            asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
-            __syncthreads();
+        for (;;) {
+            asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+            __syncthreads();  // the batch and the weights are in shared memory
 #pragma unroll
             for (int i = 0; i < EPT; ++i) {
                 const int e = tid + i * NT;
                 if (e < rows_unit * DP) {
-                    const int n = e / DP, d = e - n * DP;
+                    const int nn = e / DP, d = e - nn * DP;
                     float o = acc[i];
                     #pragma unroll 4
                     for (int c = 0; c < nc; ++c) {
-                        const float w = sWg[n * 64 + c0 + c];
-                        o += w != 0.f ? w * stg[((size_t)c * rows_unit + n) * DP + d] : 0.f;
+                        const float w = sWg[nn * 64 + c0 + c];
+                        o += w != 0.f ? w * stg[((size_t)c * rows_unit + nn) * DP + d] : 0.f;
                     }
                     acc[i] = o;
                 }
             }
+            c0 += nc;
+            if (c0 >= active) break;
+            nc = min(cap, active - c0);
+            __syncthreads();  // the batch is consumed
+            stage_batch(c0, nc);
         }
 #pragma unroll
         for (int i = 0; i < EPT; ++i) {
             const int e = tid + i * NT;
             if (e < rows_unit * DP) {
-                const int n = e / DP, d = e - n * DP;
-                if (d < p.D) p.out[out_row(n) * p.D + d] = acc[i];
+                const int nn = e / DP, d = e - nn * DP;
+                if (d < p.D) p.out[out_row(nn) * p.D + d] = acc[i];
             }
         }
         if (tid == 0) p.ws_count[unit] = 0;  // ready for the next call
