@@ -310,12 +310,15 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
             (long long)bid < p.num_blocks)
             prefetch_page(bid);
     }
-    // The next layer's pages of the same range (same table and segments), so
-    // its HBM traffic runs under this layer's compute: whole pages, warmed by
-    // the CTAs of the same cluster rank in turn (page li by kv head li % Hkv).
+    // The next layer's first pages of the same range (same table and
+    // segments: the pages its CTAs copy into their stages as they start), so
+    // a CTA of the next layer that starts late finds them in L2; its later
+    // pages it warms itself.  Whole pages, warmed by the CTAs of the same
+    // cluster rank in turn (page li by kv head li % Hkv).
     if (p.pf_next > 0) {
         const int li = kw + lane * KW, bid = id_reg;
-        if (li < min(nb, p.pf_next) && li % p.Hkv == g && bid >= 0 && (long long)bid < p.num_blocks) warm_next(bid);
+        if (li < min(min(nb, p.pf_next), KW * NST) && li % p.Hkv == g && bid >= 0 && (long long)bid < p.num_blocks)
+            warm_next(bid);
     }
     // The step's rows in the CTA's last page (decode: the one new row) are
     // handled by the warp that computes that page.
