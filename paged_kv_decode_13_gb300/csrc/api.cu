@@ -154,11 +154,13 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
     if (rows_max > (1 << 20)) return PKV_EINVAL;
     pl->rows_max = (int)rows_max;
     // Groups of at most 8 rows take the decode kernel (rows as the MMA's N side).
-    const int rc = (variant == kMmaBf16 && rows_max <= 8) ? 4
+    // Long buckets take the decode configuration with more warps (class 5).
+    const long long max_pages0 = (max_kv + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE + 1;
+    const int rc = (variant == kMmaBf16 && rows_max <= 8) ? (max_pages0 > 256 ? 5 : 4)
                    : rows_max <= 16 ? 0 : rows_max <= 32 ? 1 : rows_max <= 64 ? 2 : 3;
     pl->k = pick(variant, dp, rc);
     if (!pl->k.fn) return PKV_EUNSUPPORTED;
-    pl->gm = want_gm && rc == 4;
+    pl->gm = want_gm && rc >= 4;
     if (!pl->gm && num_splits > kMaxCluster) return PKV_EINVAL;
     pl->row_tiles = (int)((rows_max + pl->k.rows - 1) / pl->k.rows);
     if ((long long)c->kv_heads * pl->row_tiles > 65535) return PKV_EINVAL;
@@ -179,10 +181,10 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
         n = 1;
         while (n < want && n < kMaxCluster) n *= 2;
     }
-    if (rc == 4 && num_splits == 0) {
-        // decode kernel: no more CTAs than keep each of their 4 warps a page
+    if (rc >= 4 && num_splits == 0) {
+        // decode kernel: no more CTAs than keep each of their warps two pages
         long long cap = 1;
-        while (cap * 2 <= max_pages / 4 && cap * 2 <= kMaxCluster) cap *= 2;
+        while (cap * 2 <= max_pages / 8 && cap * 2 <= kMaxCluster) cap *= 2;
         n = std::min(n, cap);
     }
     n = std::max<long long>(1, std::min<long long>(n, max_pages));

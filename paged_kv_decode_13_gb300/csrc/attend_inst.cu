@@ -26,7 +26,8 @@ static AttnKernel info() {
                       C::kRows, C::DP, C::MMA};
 }
 
-// Decode kernel for groups of at most 8 query rows (row class 4).
+// Decode kernel for groups of at most 8 query rows (row class 4; class 5 for
+// long buckets, with more warps where head_dim 128 allows).
 template <class C>
 static AttnKernel dinfo() {
     static_assert(C::kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
@@ -44,7 +45,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
 #if PKV_INST_VARIANT == 0
 #if PKV_INST_DP == 64
     {
-        if (rc == 4) return dinfo<DecCfg<64, 4, 6>>();
+        if (rc >= 4) return dinfo<DecCfg<64, 4, 6>>();
         if (rc == 0) return CFG(B16, 1, 4, 4, true);
         if (rc == 1) return CFG(B16, 2, 2, 4, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);
@@ -52,6 +53,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #elif PKV_INST_DP == 128
     {
+        if (rc == 5) return dinfo<DecCfg<128, 6, 2>>();
         if (rc == 4) return dinfo<DecCfg<128, 4, 3>>();
         if (rc == 0) return CFG(B16, 1, 4, 3, true);
         if (rc == 1) return CFG(B16, 2, 2, 4, true);
@@ -60,7 +62,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #else
     {
-        if (rc == 4) return dinfo<DecCfg<256, 4, 2>>();
+        if (rc >= 4) return dinfo<DecCfg<256, 4, 2>>();
         if (rc == 0) return CFG(B16, 1, 4, 2, true);
         if (rc == 1) return CFG(B16, 2, 2, 3, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);

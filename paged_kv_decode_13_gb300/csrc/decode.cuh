@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
                 for (int i = 0; i < 4; ++i) sWg[n * 64 + c16 + 16 * i] = zero ? 0.f : w[i] * inv;  // w may be NaN when poisoned
             if (c16 == 0 && n < rows_unit && p.lse) p.lse[out_row(n)] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
         }
-        constexpr int EPT = C::kRows * DP / NT;  // elements per thread at most
+        constexpr int EPT = (C::kRows * DP + NT - 1) / NT;  // elements per thread at most
         float acc[EPT];
 #pragma unroll
         for (int i = 0; i < EPT; ++i) acc[i] = 0.f;
