@@ -334,7 +334,7 @@ def gpu_arm(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (STREAM-style copy)",
-                         "kernel": "decode_kernel (fused append + split-K attention, 16-CTA clusters), one launch per layer",
+                         "kernel": "decode_kernel (fused append + split-K attention, 16-CTA clusters; 6 warps x 2 stages at this bucket), one launch per layer",
                          "algorithmic_bytes_per_launch": bytes_layer,
                          "launch_ms": round(per_launch_ms, 6)},
             "by_kv_len": by_len,
