@@ -52,6 +52,10 @@ def _lib():
             lib.oracle_attend.argtypes = [p, i32, i32, p, p, i64, i32, i32, p, i32, i32, i32, p, i32,
                                           ctypes.c_double, i32, i32, p, p, p]
             lib.oracle_attend.restype = i32
+            lib.oracle_seq_clone.argtypes = [p, p, i32, i64, i32, i32, p, i32, i32, i32, i32, i32, i64]
+            lib.oracle_seq_clone.restype = i32
+            lib.oracle_rewind.argtypes = [p, i32, p, i32, i32]
+            lib.oracle_rewind.restype = i32
             _LIB = lib
     return _LIB
 
@@ -112,3 +116,25 @@ def attend(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, block_table: n
                                 float(scale), int(bool(causal)), int(window), _ptr(out), _ptr(lse),
                                 _ptr(work))
     return out, lse, int(errs)
+
+
+def seq_clone(k_pool: np.ndarray, v_pool: np.ndarray, block_table: np.ndarray, src_col: int, dst_col: int,
+              n: int, ring_rows: int = 0) -> int:
+    """Copy positions 0..n-1 of sequence src_col to dst_col in place (one layer; ring: the last
+    min(n, ring_rows) positions).  Returns 0 or the failure bit (all or nothing)."""
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    nb, blk, hkv, d = k_pool.shape
+    assert blk == 16
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    return int(_lib().oracle_seq_clone(_ptr(k_pool), _ptr(v_pool), k_pool.itemsize, nb, hkv, d, _ptr(bt),
+                                       bt.shape[0], bt.shape[1], int(ring_rows), int(src_col), int(dst_col),
+                                       int(n)))
+
+
+def rewind(seq_info: np.ndarray, amount: np.ndarray, ring_rows: int = 0, window: int = 0):
+    """kv_end -= amount per segment where allowed.  Returns (new seq_info, failed-segment bitmask)."""
+    si = np.ascontiguousarray(seq_info, dtype=np.int32).reshape(-1, 4).copy()
+    am = np.ascontiguousarray(amount, dtype=np.int32).reshape(-1)
+    assert am.shape[0] == si.shape[0]
+    errs = _lib().oracle_rewind(_ptr(si), si.shape[0], _ptr(am), int(ring_rows), int(window))
+    return si, int(errs)

@@ -22,7 +22,9 @@
  *       kv_end), causal / non-causal, sliding window, ring storage, GQA,
  *       rows no segment covers are zeroed.
  *   [ExecuTorch #24074]  ring slot = position % rows.
- *   [ExecuTorch #24073]  ring layers hold window + max_write - 1 rows.
+ *   [ExecuTorch #24073]  ring layers hold window + max_write - 1 rows;
+ *       CudaBatchedSequenceCache's BatchControl: seq_clone (device copy of
+ *       the source prefix), rewind (bounded by the ring floor).
  *
  * Readings where the pages leave a step open (each also listed in the design
  * notes): q head h uses kv head h / (Hq / Hkv); the window covers W keys
@@ -225,6 +227,60 @@ int oracle_attend(const double *q, int q_heads, int total_rows,
                 lse[t * q_heads + h] = m + log(sum);
             }
         }
+    }
+    return errs;
+}
+
+/* seq_clone: positions 0 .. n-1 of sequence src_col are copied bit for bit to
+ * the same positions of dst_col (one layer's pools).  With ring storage of R
+ * rows only the last min(n, R) positions exist and are copied.  All or
+ * nothing: if any slot either side needs maps outside the table or the pool,
+ * nothing is written.  Returns 0 or 1 << status. */
+int oracle_seq_clone(uint8_t *k_pool, uint8_t *v_pool, int elem_size,
+                     int64_t num_blocks, int kv_heads, int head_dim,
+                     const int32_t *block_table, int max_seqs, int max_blocks_per_seq,
+                     int ring_rows, int src_col, int dst_col, int64_t n)
+{
+    oracle_pool P = {num_blocks, kv_heads, head_dim, block_table, max_seqs,
+                     max_blocks_per_seq, ring_rows};
+    if (src_col < 0 || src_col >= max_seqs || dst_col < 0 || dst_col >= max_seqs || n < 0)
+        return 1 << OR_BAD_SEGMENT;
+    if (!ring_rows && n > (int64_t)max_blocks_per_seq * ORACLE_BLOCK) return 1 << OR_CAPACITY;
+    int64_t lo = (ring_rows && n > ring_rows) ? n - ring_rows : 0;
+    for (int64_t p = lo; p < n; ++p) {
+        int64_t b; int o;
+        int st = locate(&P, src_col, p, &b, &o);
+        if (!st) st = locate(&P, dst_col, p, &b, &o);
+        if (st) return 1 << st;
+    }
+    int64_t row_bytes = (int64_t)kv_heads * head_dim * elem_size;
+    for (int64_t p = lo; p < n; ++p) {
+        int64_t bs, bd; int os, od;
+        locate(&P, src_col, p, &bs, &os);
+        locate(&P, dst_col, p, &bd, &od);
+        memmove(k_pool + (bd * ORACLE_BLOCK + od) * row_bytes, k_pool + (bs * ORACLE_BLOCK + os) * row_bytes,
+                (size_t)row_bytes);
+        memmove(v_pool + (bd * ORACLE_BLOCK + od) * row_bytes, v_pool + (bs * ORACLE_BLOCK + os) * row_bytes,
+                (size_t)row_bytes);
+    }
+    return 0;
+}
+
+/* rewind: segment s moves back amount[s] positions (kv_end -= amount[s]),
+ * e.g. draft tokens a verify step rejected.  Allowed when
+ * 0 <= amount <= kv_end and, with ring storage of R rows and window W, when
+ * amount <= R - W + 1: the positions the next window reads (from the new
+ * kv_end - W + 1 on) must still be held by the ring, which keeps the last R.
+ * A segment that breaks a rule keeps its kv_end.  Returns a bitmask of
+ * (1 << status) over such segments. */
+int oracle_rewind(int32_t *seq_info, int num_segments, const int32_t *amount, int ring_rows, int window)
+{
+    int errs = 0;
+    for (int s = 0; s < num_segments; ++s) {
+        int64_t kend = seq_info[4 * s + 3], a = amount[s];
+        if (a < 0 || a > kend) { errs |= 1 << OR_BAD_SEGMENT; continue; }
+        if (ring_rows && (window <= 0 || a > (int64_t)ring_rows - window + 1)) { errs |= 1 << OR_RING; continue; }
+        seq_info[4 * s + 3] = (int32_t)(kend - a);
     }
     return errs;
 }

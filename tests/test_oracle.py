@@ -451,3 +451,121 @@ def test_append_gated_only_by_written_slots():
     kn = np.full((1, 1, 4), 3.0)
     assert O.append(kp, vp, bt, si, kn, kn) == 0
     assert np.array_equal(kp.reshape(-1, 1, 4)[99], kn[0])
+
+
+# ---------------------------------------------------------------- batched-sequence cache operations
+# (ExecuTorch #24073, CudaBatchedSequenceCache: seq_clone copies the source
+# prefix on the device; rewind is bounded by the ring floor)
+
+def _two_seq_pool(rng, n_src, ring_rows=0, Hkv=2, D=8):
+    span = ring_rows if ring_rows else max(n_src, 1)
+    need = (span + PAGE - 1) // PAGE
+    nb = 2 * need + 3
+    perm = rng.permutation(nb).astype(np.int32)
+    bt = np.full((2, need + 1), -1, dtype=np.int32)
+    bt[0, :need] = perm[:need]
+    bt[1, :need] = perm[need:2 * need]
+    kp = rng.standard_normal((nb, PAGE, Hkv, D))
+    vp = rng.standard_normal((nb, PAGE, Hkv, D))
+    return kp, vp, bt
+
+
+def _slot(bt, col, pos, ring_rows=0):
+    r = pos % ring_rows if ring_rows else pos
+    return int(bt[col, r // PAGE]), r % PAGE
+
+
+@pytest.mark.parametrize("n", [0, 1, 15, 16, 40])
+def test_seq_clone_copies_the_prefix_bit_exact(n):
+    rng = np.random.default_rng(n + 1)
+    kp, vp, bt = _two_seq_pool(rng, 48)
+    k0, v0 = kp.copy(), vp.copy()
+    assert O.seq_clone(kp, vp, bt, 0, 1, n) == 0
+    for pos in range(48):
+        bs, os_ = _slot(bt, 0, pos)
+        bd, od = _slot(bt, 1, pos)
+        if pos < n:   # the destination's slot now holds the source's row
+            assert np.array_equal(kp[bd, od], k0[bs, os_]) and np.array_equal(vp[bd, od], v0[bs, os_])
+        else:         # untouched past n
+            assert np.array_equal(kp[bd, od], k0[bd, od]) and np.array_equal(vp[bd, od], v0[bd, od])
+    # the source never changes
+    for pos in range(48):
+        bs, os_ = _slot(bt, 0, pos)
+        assert np.array_equal(kp[bs, os_], k0[bs, os_])
+
+
+def test_seq_clone_then_attention_matches_the_source():
+    rng = np.random.default_rng(7)
+    kp, vp, bt = _two_seq_pool(rng, 37, Hkv=2, D=16)
+    assert O.seq_clone(kp, vp, bt, 0, 1, 37) == 0
+    q = rng.standard_normal((2, 4, 16))
+    si = np.array([[0, 1, 0, 37], [1, 1, 1, 37]], np.int32)
+    q[1] = q[0]
+    out, lse, err = O.attend(q, kp, vp, bt, si, 0.25)
+    assert err == 0
+    assert np.array_equal(out[0], out[1]) and np.array_equal(lse[0], lse[1])
+
+
+def test_seq_clone_ring_copies_only_the_last_rows():
+    rng = np.random.default_rng(9)
+    R = 32
+    kp, vp, bt = _two_seq_pool(rng, 0, ring_rows=R)
+    k0 = kp.copy()
+    assert O.seq_clone(kp, vp, bt, 0, 1, 75, ring_rows=R) == 0
+    # positions 43..74 live in the ring; each one's slot holds the source row of the same slot
+    for pos in range(75 - R, 75):
+        bs, os_ = _slot(bt, 0, pos, R)
+        bd, od = _slot(bt, 1, pos, R)
+        assert np.array_equal(kp[bd, od], k0[bs, os_])
+    # and a windowed attention on the clone equals the source's
+    q = rng.standard_normal((1, 4, 8))
+    for col in (0, 1):
+        si = np.array([[0, 1, col, 75]], np.int32)
+        o, l, e = O.attend(q, kp, vp, bt, si, 0.3, causal=True, window=20, ring_rows=R)
+        assert e == 0
+        if col == 0:
+            ref = o
+        else:
+            assert np.array_equal(o, ref)
+
+
+def test_seq_clone_all_or_nothing_on_bad_pages():
+    rng = np.random.default_rng(11)
+    kp, vp, bt = _two_seq_pool(rng, 40)
+    bt[1, 2] = -1     # the destination's third page is missing
+    k0, v0 = kp.copy(), vp.copy()
+    assert O.seq_clone(kp, vp, bt, 0, 1, 40) == 1 << 4
+    assert np.array_equal(kp, k0) and np.array_equal(vp, v0)
+    assert O.seq_clone(kp, vp, bt, 0, 5, 4) == 1 << 1      # no such sequence
+    assert O.seq_clone(kp, vp, bt, 0, 1, 10_000) == 1 << 2  # beyond the table's capacity
+
+
+def test_rewind_arithmetic_and_ring_floor():
+    si = np.array([[0, 1, 0, 100], [1, 1, 1, 5], [2, 1, 2, 50], [3, 1, 3, 8]], np.int32)
+    new, err = O.rewind(si, np.array([10, 6, 0, -1]))
+    assert new[:, 3].tolist() == [90, 5, 50, 8] and err == 1 << 1
+    # ring of 64 rows with a window of 40: at most 64 - 40 + 1 = 25 positions back
+    new, err = O.rewind(si[:1], np.array([25]), ring_rows=64, window=40)
+    assert new[0, 3] == 75 and err == 0
+    new, err = O.rewind(si[:1], np.array([26]), ring_rows=64, window=40)
+    assert new[0, 3] == 100 and err == 1 << 3
+
+
+def test_rewind_then_rewrite_restores_the_state():
+    # a verify step appends 4 draft rows and rejects 3 of them: attending over
+    # the accepted length equals having appended the one accepted row alone
+    rng = np.random.default_rng(5)
+    kp, vp, bt = _two_seq_pool(rng, 64, Hkv=2, D=8)
+    kn = rng.standard_normal((4, 2, 8))
+    vn = rng.standard_normal((4, 2, 8))
+    a_k, a_v = kp.copy(), vp.copy()
+    assert O.append(a_k, a_v, bt, np.array([[0, 4, 0, 24]], np.int32), kn, vn) == 0
+    si, err = O.rewind(np.array([[0, 4, 0, 24]], np.int32), np.array([3]))
+    assert err == 0 and si[0, 3] == 21
+    b_k, b_v = kp.copy(), vp.copy()
+    assert O.append(b_k, b_v, bt, np.array([[0, 1, 0, 21]], np.int32), kn[:1], vn[:1]) == 0
+    q = rng.standard_normal((1, 4, 8))
+    one = np.array([[0, 1, 0, 21]], np.int32)
+    oa, _, _ = O.attend(q, a_k, a_v, bt, one, 0.5)
+    ob, _, _ = O.attend(q, b_k, b_v, bt, one, 0.5)
+    assert np.array_equal(oa, ob)
