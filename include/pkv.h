@@ -268,6 +268,39 @@ int pkv_seqinfo_from_seqused(const int32_t *cu_seqlens_q, const int32_t *seqused
                              int32_t num_seqs, int32_t *seq_info_out, void *stream);
 
 /*
+ * seq_clone of the batched-sequence cache ([ExecuTorch #24073]
+ * CudaBatchedSequenceCache: a device copy of the source prefix), over the
+ * paged layout: in every layer, positions 0 .. n-1 of the sequence in
+ * block-table row src_col are copied bit for bit (all kv heads) to the same
+ * positions of row dst_col, each side mapped through its own table row.
+ * With ring storage only the last min(n, ring_rows) positions exist and are
+ * copied (slot position % ring_rows on both sides).  Typical use: admit a
+ * request that shares a prefix, then set its segment's kv_end to n.
+ * All or nothing per layer: if any page either side needs is outside
+ * [0, num_blocks), that layer is not written and PKV_ERR_BLOCK is set.  The
+ * two rows' pages must not overlap (other than being identical).  Host
+ * errors: a column outside [0, max_seqs), n < 0, or (flat layout) n beyond
+ * the table's capacity (PKV_ECAPACITY).  Launches one kernel per layer.
+ */
+int pkv_seq_clone(const pkv_cache *cache, int32_t src_col, int32_t dst_col, int64_t n,
+                  uint32_t *err_flags, void *stream);
+
+/*
+ * rewind of the batched-sequence cache ([ExecuTorch #24073], bounded by the
+ * ring floor), on the device: kv_end -= amount[s] for every segment s
+ * (amount: device int32[num_segments]), e.g. the draft tokens a verify step
+ * rejected; their slots are simply rewritten by the next append.  A segment
+ * keeps its kv_end and sets PKV_ERR_SEGMENT when amount < 0 or
+ * amount > kv_end, and PKV_ERR_RING when the cache is a ring of R rows and
+ * amount > R - window + 1 (the next step's window would need positions the
+ * ring no longer holds; window must be > 0 with rings).  The block table is
+ * untouched: removing a sequence (seq_rm) is the caller releasing its table
+ * row's pages, which needs no device work.
+ */
+int pkv_rewind(const pkv_cache *cache, int32_t *seq_info, int32_t num_segments,
+               const int32_t *amount, int32_t window, uint32_t *err_flags, void *stream);
+
+/*
  * Advance every segment to the next step on the device: kv_end += q_len
  * ([tiny-llm kv_cache.py] SlotKVCache.end_step does the same for slot
  * lengths inside a captured graph, so a replay needs no host write).

@@ -9,5 +9,5 @@ from ._lib import (BF16, BLOCK_SIZE, ERR_BLOCK, ERR_CAPACITY, ERR_OVERLAP, ERR_Q
                    PkvError)
 from .api import (PagedKVCache, advance, append, append_attend, append_attend_noalloc,  # noqa: F401
                   attend_varlen, attend_workspace_bytes,
-                  bucket_for, load_prefix, new_err_flags, new_workspace, resize_bucket, seqinfo_from_seqused,
-                  to_contiguous)
+                  bucket_for, load_prefix, new_err_flags, new_workspace, resize_bucket, rewind, seq_clone,
+                  seqinfo_from_seqused, to_contiguous)

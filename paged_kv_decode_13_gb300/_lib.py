@@ -60,6 +60,8 @@ def _declare(lib):
         "pkv_append_attend_noalloc": (ctypes.c_int, [cp, i32, p, p, p, i32, i32, p, i32, i32, i64, i32, f32, i32,
                                                      i32, p, p, p, u32, p]),
         "pkv_seqinfo_from_seqused": (ctypes.c_int, [p, p, i32, p, p]),
+        "pkv_seq_clone": (ctypes.c_int, [cp, i32, i32, i64, p, p]),
+        "pkv_rewind": (ctypes.c_int, [cp, p, i32, p, i32, p, p]),
         "pkv_advance": (ctypes.c_int, [p, i32, p]),
         "pkv_resize_bucket": (ctypes.c_int, [cp, cp, i64, p]),
         "pkv_load_prefix": (ctypes.c_int, [cp, p, p, i64, i64, i64, p]),

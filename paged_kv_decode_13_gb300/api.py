@@ -184,6 +184,20 @@ def new_workspace(cache: PagedKVCache, num_q_heads: int, num_segments: int, max_
     return torch.zeros(n, dtype=torch.uint8, device=cache.k[0].device) if n > 0 else None
 
 
+def seq_clone(cache: PagedKVCache, src_col: int, dst_col: int, n: int, err: torch.Tensor, stream=None) -> None:
+    """pkv_seq_clone: copy positions 0..n-1 of block-table row src_col to dst_col in every layer."""
+    _lib.check("pkv_seq_clone", lib.pkv_seq_clone(cache.ref(), int(src_col), int(dst_col), int(n), _ptr(err),
+                                                  _stream(stream)))
+
+
+def rewind(cache: PagedKVCache, seq_info: torch.Tensor, amount: torch.Tensor, err: torch.Tensor, window: int = 0,
+           stream=None) -> None:
+    """pkv_rewind: kv_end -= amount per segment on the device, bounded by the ring floor."""
+    _lib.check("pkv_rewind", lib.pkv_rewind(cache.ref(), _ptr(_contig(seq_info, "seq_info")), int(seq_info.shape[0]),
+                                            _ptr(_contig(amount, "amount")), int(window), _ptr(err),
+                                            _stream(stream)))
+
+
 def seqinfo_from_seqused(cu_seqlens_q: torch.Tensor, seqused_k: torch.Tensor, out: torch.Tensor,
                          stream=None) -> None:
     n = int(seqused_k.shape[0])

@@ -537,6 +537,42 @@ int64_t pkv_attend_workspace_bytes(const pkv_cache *c, int32_t Hq, int32_t S, in
     return (int64_t)ws_layout((long long)S * c->kv_heads * pl.row_tiles, pl.ncta, pl.k.dp).total;
 }
 
+int pkv_seq_clone(const pkv_cache *c, int32_t src_col, int32_t dst_col, int64_t n, uint32_t *err, void *stream) {
+    int st = check_cache(c);
+    if (st) return st;
+    if (!err || n < 0 || src_col < 0 || src_col >= c->max_seqs || dst_col < 0 || dst_col >= c->max_seqs)
+        return PKV_EINVAL;
+    if (!c->ring_rows && n > (long long)c->max_blocks_per_seq * PKV_BLOCK_SIZE) return PKV_ECAPACITY;
+    if (n > INT32_MAX - PKV_BLOCK_SIZE) return PKV_EINVAL;
+    for (int l = 0; l < c->num_layers; ++l)
+        if ((st = check_layer(c, l))) return st;
+    if (n == 0 || src_col == dst_col) return PKV_OK;
+    const long long lo = (c->ring_rows && n > c->ring_rows) ? n - c->ring_rows : 0;
+    const int row_chunks = c->kv_heads * c->head_dim * elem_bytes(c->dtype) / 16;
+    const long long total = 2 * (n - lo) * row_chunks;
+    const long long blocks = std::max<long long>(1, std::min<long long>((total + 255) / 256, (long long)kDefaultSms * 8));
+    for (int l = 0; l < c->num_layers; ++l) {
+        CloneParams p{reinterpret_cast<const char *>(c->k[l]), reinterpret_cast<const char *>(c->v[l]),
+                      reinterpret_cast<char *>(c->k[l]), reinterpret_cast<char *>(c->v[l]), c->block_table, err,
+                      c->num_blocks, lo, n, row_chunks, c->max_blocks_per_seq, c->ring_rows, src_col, dst_col};
+        seq_clone_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+        if ((st = launch_status(cudaSuccess))) return st;
+    }
+    return PKV_OK;
+}
+
+int pkv_rewind(const pkv_cache *c, int32_t *seq_info, int32_t n, const int32_t *amount, int32_t window,
+               uint32_t *err, void *stream) {
+    int st = check_cache(c);
+    if (st) return st;
+    if (n < 0 || window < 0 || !err) return PKV_EINVAL;
+    if (n == 0) return PKV_OK;
+    if (!seq_info || !aligned16(seq_info) || !amount || (reinterpret_cast<uintptr_t>(amount) & 3u)) return PKV_EINVAL;
+    rewind_kernel<<<(unsigned)((n + 127) / 128), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<int4 *>(seq_info), amount, n, c->ring_rows, window, err);
+    return launch_status(cudaSuccess);
+}
+
 int pkv_seqinfo_from_seqused(const int32_t *cu, const int32_t *used, int32_t n, int32_t *out, void *stream) {
     if (n < 0) return PKV_EINVAL;
     if (n == 0) return PKV_OK;

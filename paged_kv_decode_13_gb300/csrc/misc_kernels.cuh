@@ -93,4 +93,78 @@ static __global__ void advance_kernel(int4 *seq_info, int n) {
     }
 }
 
+// ---------------------------------------------------------------- batched-sequence cache operations
+
+// seq_clone of ExecuTorch #24073 (CudaBatchedSequenceCache: a device copy of
+// the source prefix) over the paged layout: positions lo .. n-1 of sequence
+// `src` are copied row by row (all kv heads) to the same positions of `dst`,
+// each side mapped through its block-table row (ring: position % rows).  One
+// layer per launch.  Every CTA first checks every page either side touches,
+// so the copy is all or nothing; a bad page id sets PKV_ERR_BLOCK.
+struct CloneParams {
+    const char *k, *v;          // this layer's pools (read)
+    char *kw, *vw;              // the same pools (written)
+    const int *block_table;
+    unsigned *err;
+    long long num_blocks;
+    long long lo, n;            // positions lo .. n-1
+    int row_chunks;             // 16-byte chunks per token row (Hkv * D * elem / 16)
+    int mbps, ring_rows, src, dst;
+};
+
+static __global__ void __launch_bounds__(256) seq_clone_kernel(const __grid_constant__ CloneParams p) {
+    const int *bs = p.block_table + (long long)p.src * p.mbps;
+    const int *bd = p.block_table + (long long)p.dst * p.mbps;
+    const long long pb0 = p.lo / kPage, pb1 = (p.n + kPage - 1) / kPage;
+    bool ok = true;
+    for (long long pb = pb0 + threadIdx.x; pb < pb1; pb += blockDim.x) {
+        const int tp = table_page((int)pb, p.ring_rows);
+        const int a = bs[tp], b = bd[tp];
+        ok &= a >= 0 && (long long)a < p.num_blocks && b >= 0 && (long long)b < p.num_blocks;
+    }
+    if (!__syncthreads_and(ok)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PKV_ERR_BLOCK);
+        return;
+    }
+    const long long rows = p.n - p.lo, per_tensor = rows * p.row_chunks;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < 2 * per_tensor; c += stride) {
+        const int kv = c >= per_tensor;
+        const long long rem = c - kv * per_tensor;
+        const long long i = rem / p.row_chunks;
+        const int ch = (int)(rem - i * p.row_chunks);
+        const long long pos = p.lo + i;
+        const long long r = p.ring_rows ? pos % p.ring_rows : pos;
+        const int tp = table_page((int)(pos / kPage), p.ring_rows);
+        const long long s_slot = (long long)bs[tp] * kPage + r % kPage;
+        const long long d_slot = (long long)bd[tp] * kPage + r % kPage;
+        const uint4 *src = reinterpret_cast<const uint4 *>(kv ? p.v : p.k) + s_slot * p.row_chunks + ch;
+        uint4 *dst = reinterpret_cast<uint4 *>(kv ? p.vw : p.kw) + d_slot * p.row_chunks + ch;
+        *dst = *src;
+    }
+}
+
+// rewind of ExecuTorch #24073 (bounded by the ring floor): kv_end -= amount
+// per segment when 0 <= amount <= kv_end and, with ring storage of R rows
+// and window W, amount <= R - W + 1 (the next window's keys are still in the
+// ring).  A segment that breaks a rule keeps its kv_end and sets
+// PKV_ERR_SEGMENT (amount out of range) or PKV_ERR_RING (ring floor).
+static __global__ void rewind_kernel(int4 *seq_info, const int *amount, int n, int ring_rows, int window,
+                                     unsigned *err) {
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= n) return;
+    int4 v = seq_info[s];
+    const int a = amount[s];
+    if (a < 0 || a > v.w) {
+        atomicOr(err, PKV_ERR_SEGMENT);
+        return;
+    }
+    if (ring_rows && (window <= 0 || (long long)a > (long long)ring_rows - window + 1)) {
+        atomicOr(err, PKV_ERR_RING);
+        return;
+    }
+    v.w -= a;
+    seq_info[s] = v;
+}
+
 }  // namespace pkv

@@ -129,6 +129,22 @@ def test_bad_call_arguments_rejected(lib):
     assert attend(rows=0, S=0) == 0
 
 
+def test_batch_ops_host_rules(lib):
+    L = lib.lib
+    d, keep = _desc(lib)       # one sequence row, 32 pages of 16
+    ref = ctypes.byref(d)
+    assert L.pkv_seq_clone(ref, 0, 1, 4, 0x7000, None) == -1      # no row 1
+    assert L.pkv_seq_clone(ref, -1, 0, 4, 0x7000, None) == -1
+    assert L.pkv_seq_clone(ref, 0, 0, -1, 0x7000, None) == -1
+    assert L.pkv_seq_clone(ref, 0, 0, 4, None, None) == -1        # no error word
+    assert L.pkv_seq_clone(ref, 0, 0, 513, 0x7000, None) == -4    # beyond 32 pages
+    assert L.pkv_seq_clone(ref, 0, 0, 100, 0x7000, None) == 0     # same row: nothing to copy, no launch
+    assert L.pkv_rewind(ref, 0x5000, -1, 0x6000, 0, 0x7000, None) == -1
+    assert L.pkv_rewind(ref, 0x5004, 1, 0x6000, 0, 0x7000, None) == -1   # misaligned segment table
+    assert L.pkv_rewind(ref, 0x5000, 1, 0x6002, 0, 0x7000, None) == -1   # misaligned amounts
+    assert L.pkv_rewind(ref, 0x5000, 0, None, 0, 0x7000, None) == 0      # nothing to do
+
+
 def test_workspace_size_query(lib):
     L = lib.lib
     d, keep = _desc(lib)   # bf16, 2 kv heads, head_dim 64, 512 tokens
