@@ -170,6 +170,38 @@ def time_steps(runner, steps: int, warmup: int, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def time_clone(pkv, device, flush, stream, reps: int = 10, warmup: int = 3):
+    """pkv_seq_clone of an 8192-token prefix in all 42 layers (the admission of
+    a request that shares it): ms per clone and the bytes it moves."""
+    import torch
+    pages = HEADLINE_LEN // 16
+    k = [torch.zeros(2 * pages, 16, HKV, D, dtype=torch.bfloat16, device=device) for _ in range(LAYERS)]
+    v = [torch.zeros(2 * pages, 16, HKV, D, dtype=torch.bfloat16, device=device) for _ in range(LAYERS)]
+    for t in k + v:
+        t.normal_()
+    bt = torch.arange(2 * pages, dtype=torch.int32, device=device).view(2, pages)
+    cache = pkv.PagedKVCache(k, v, bt, bucket=HEADLINE_LEN)
+    err = pkv.new_err_flags(device)
+    for _ in range(warmup):
+        pkv.seq_clone(cache, 0, 1, HEADLINE_LEN, err, stream=stream)
+    ts = []
+    for _ in range(reps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pkv.seq_clone(cache, 0, 1, HEADLINE_LEN, err, stream=stream)
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError(f"seq_clone error flags {int(err.item()):#x}")
+    ms = statistics.median([a.elapsed_time(b) for a, b in ts])
+    moved = 2 * 2 * LAYERS * HEADLINE_LEN * HKV * D * 2  # K and V, read and written
+    del k, v, cache
+    return ms, moved
+
+
 def time_e2e(runner, steps: int, warmup: int, flush, stream):
     """Per step: pinned host -> device copy of the step's inputs, graph replay,
     device -> host copy of the outputs, all inside the timed events."""
@@ -305,6 +337,16 @@ def gpu_arm(args):
             del r
             torch.cuda.empty_cache()
 
+    clone = None
+    if not args.no_sweep:
+        cms, moved = time_clone(pkv, device, flush, stream)
+        cms = reduce_max(cms, world, device)
+        cgbs = moved / (cms * 1e-3) / 1e9
+        clone = {"what": f"pkv_seq_clone of a {HEADLINE_LEN}-token prefix in all {LAYERS} layers (K and V read and "
+                         f"written)", "ms": round(cms, 4), "bytes": moved, "gbs": round(cgbs, 1),
+                 "frac_of_peak": round(cgbs / peak, 4)}
+        torch.cuda.empty_cache()
+
     traffic = None
     if os.path.exists(PROFILE):
         with open(PROFILE) as f:
@@ -338,6 +380,7 @@ def gpu_arm(args):
                          "algorithmic_bytes_per_launch": bytes_layer,
                          "launch_ms": round(per_launch_ms, 6)},
             "by_kv_len": by_len,
+            "seq_clone": clone,
             "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "µs/step", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,

@@ -549,12 +549,25 @@ int pkv_seq_clone(const pkv_cache *c, int32_t src_col, int32_t dst_col, int64_t 
     if (n == 0 || src_col == dst_col) return PKV_OK;
     const long long lo = (c->ring_rows && n > c->ring_rows) ? n - c->ring_rows : 0;
     const int row_chunks = c->kv_heads * c->head_dim * elem_bytes(c->dtype) / 16;
-    const long long total = 2 * (n - lo) * row_chunks;
-    const long long blocks = std::max<long long>(1, std::min<long long>((total + 255) / 256, (long long)kDefaultSms * 8));
-    for (int l = 0; l < c->num_layers; ++l) {
-        CloneParams p{reinterpret_cast<const char *>(c->k[l]), reinterpret_cast<const char *>(c->v[l]),
-                      reinterpret_cast<char *>(c->k[l]), reinterpret_cast<char *>(c->v[l]), c->block_table, err,
-                      c->num_blocks, lo, n, row_chunks, c->max_blocks_per_seq, c->ring_rows, src_col, dst_col};
+    for (int l0 = 0; l0 < c->num_layers; l0 += kCloneLayers) {
+        CloneParams p = {};
+        p.layers = std::min(kCloneLayers, c->num_layers - l0);
+        for (int i = 0; i < p.layers; ++i) {
+            p.k[i] = reinterpret_cast<char *>(c->k[l0 + i]);
+            p.v[i] = reinterpret_cast<char *>(c->v[l0 + i]);
+        }
+        p.block_table = c->block_table;
+        p.err = err;
+        p.num_blocks = c->num_blocks;
+        p.lo = lo;
+        p.n = n;
+        p.row_chunks = row_chunks;
+        p.mbps = c->max_blocks_per_seq;
+        p.ring_rows = c->ring_rows;
+        p.src = src_col;
+        p.dst = dst_col;
+        const long long total = 2LL * p.layers * (n - lo) * row_chunks;
+        const long long blocks = std::max<long long>(1, std::min<long long>((total + 255) / 256, (long long)device_sms() * 8));
         seq_clone_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
         if ((st = launch_status(cudaSuccess))) return st;
     }

@@ -98,12 +98,15 @@ static __global__ void advance_kernel(int4 *seq_info, int n) {
 // seq_clone of ExecuTorch #24073 (CudaBatchedSequenceCache: a device copy of
 // the source prefix) over the paged layout: positions lo .. n-1 of sequence
 // `src` are copied row by row (all kv heads) to the same positions of `dst`,
-// each side mapped through its block-table row (ring: position % rows).  One
-// layer per launch.  Every CTA first checks every page either side touches,
-// so the copy is all or nothing; a bad page id sets PKV_ERR_BLOCK.
+// each side mapped through its block-table row (ring: position % rows), in
+// up to kCloneLayers layers per launch.  Every CTA first checks every page
+// either side touches, so the copy is all or nothing; a bad page id sets
+// PKV_ERR_BLOCK.
+constexpr int kCloneLayers = 64;
 struct CloneParams {
-    const char *k, *v;          // this layer's pools (read)
-    char *kw, *vw;              // the same pools (written)
+    char *k[kCloneLayers];      // the layers' pools (read and written)
+    char *v[kCloneLayers];
+    int layers;
     const int *block_table;
     unsigned *err;
     long long num_blocks;
@@ -126,21 +129,20 @@ static __global__ void __launch_bounds__(256) seq_clone_kernel(const __grid_cons
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PKV_ERR_BLOCK);
         return;
     }
-    const long long rows = p.n - p.lo, per_tensor = rows * p.row_chunks;
+    // work items: (position, layer, K or V) rows, each row_chunks 16-byte chunks
+    const long long rows = p.n - p.lo, per_pos = 2LL * p.layers * p.row_chunks;
     const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < 2 * per_tensor; c += stride) {
-        const int kv = c >= per_tensor;
-        const long long rem = c - kv * per_tensor;
-        const long long i = rem / p.row_chunks;
-        const int ch = (int)(rem - i * p.row_chunks);
+    for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < rows * per_pos; c += stride) {
+        const long long i = c / per_pos;
+        const int rem = (int)(c - i * per_pos);
+        const int t = rem / p.row_chunks, ch = rem - t * p.row_chunks;  // t = 2 * layer + (V ? 1 : 0)
         const long long pos = p.lo + i;
         const long long r = p.ring_rows ? pos % p.ring_rows : pos;
         const int tp = table_page((int)(pos / kPage), p.ring_rows);
         const long long s_slot = (long long)bs[tp] * kPage + r % kPage;
         const long long d_slot = (long long)bd[tp] * kPage + r % kPage;
-        const uint4 *src = reinterpret_cast<const uint4 *>(kv ? p.v : p.k) + s_slot * p.row_chunks + ch;
-        uint4 *dst = reinterpret_cast<uint4 *>(kv ? p.vw : p.kw) + d_slot * p.row_chunks + ch;
-        *dst = *src;
+        uint4 *base = reinterpret_cast<uint4 *>((t & 1) ? p.v[t >> 1] : p.k[t >> 1]);
+        base[d_slot * p.row_chunks + ch] = base[s_slot * p.row_chunks + ch];
     }
 }
 
