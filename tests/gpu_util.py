@@ -65,8 +65,12 @@ def compact(w, layer: int, segs, k_pool: torch.Tensor, v_pool: torch.Tensor):
         npg = (span + PAGE - 1) // PAGE
         row = []
         for pg in range(npg):
-            row.append(len(ids))
-            ids.append(int(bt[col, pg]))
+            b = int(bt[col, pg])
+            if 0 <= b < k_pool.shape[0]:
+                row.append(len(ids))
+                ids.append(b)
+            else:          # a page the table does not list (e.g. a ring not yet grown to it)
+                row.append(-1)
         rows.append(row)
     mb = max(len(r) for r in rows) if rows else 1
     new_bt = np.full((len(segs), max(mb, 1)), -1, np.int32)

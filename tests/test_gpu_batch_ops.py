@@ -165,3 +165,22 @@ def test_verify_then_rewind_then_decode_matches_oracle(pkv):
     ref, _, e = O.attend(q1.double().numpy(), kpf, vpf, bt, np.array([[0, 1, 0, 502]], np.int32), w.scale)
     assert e == 0
     assert float(np.abs(U.f64(out1) - ref).max()) <= U.TOL[torch.bfloat16]
+
+
+def test_growable_ring_table_lists_only_filled_pages(pkv):
+    # before a ring layer wraps, its table may list only the pages filled so far
+    w = workloads.long_context(S=3, kv_len=70, window=100, ring_rows=128, num_layers=1, seed=31, q_heads=16,
+                               kv_heads=2, head_dim=128)
+    w.block_table[:, (70 + 15) // 16:] = -1
+    w = U.nan_tails(w)
+    dev = torch.device("cuda")
+    cache = U.device_cache(pkv, w)
+    out = torch.zeros(w.total_rows, w.q_heads, w.head_dim, device=dev)
+    lse = torch.zeros(w.total_rows, w.q_heads, device=dev)
+    err = pkv.new_err_flags()
+    pkv.append_attend(cache, 0, w.q[0].to(dev), w.k_new[0].to(dev), w.v_new[0].to(dev), w.seq_info.to(dev), out,
+                      err, 1, 128, w.scale, True, 100, lse=lse)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, ref_lse = U.oracle_attend(w, 0)
+    assert float(np.abs(U.f64(out) - ref).max()) <= U.TOL[w.dtype]

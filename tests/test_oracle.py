@@ -569,3 +569,18 @@ def test_rewind_then_rewrite_restores_the_state():
     oa, _, _ = O.attend(q, a_k, a_v, bt, one, 0.5)
     ob, _, _ = O.attend(q, b_k, b_v, bt, one, 0.5)
     assert np.array_equal(oa, ob)
+
+
+def test_growable_ring_reads_only_filled_pages():
+    # ExecuTorch #24076: a ring layer grows with the flat layers until it holds
+    # all its rows, so before the first wrap its table may list only the pages
+    # filled so far; the result equals the flat layout with the same window
+    rng = np.random.default_rng(21)
+    R, W, kend = 128, 100, 70            # 70 < R: no wrap yet, 5 of 8 pages filled
+    q, kp, vp, bt, si = random_paged(rng, [kend], [1], 4, 2, 8, ring_rows=R)
+    bt[0, (kend + PAGE - 1) // PAGE:] = -1
+    out_r, lse_r, err = O.attend(q, kp, vp, bt, si, 0.3, causal=True, window=W, ring_rows=R)
+    assert err == 0
+    out_f, lse_f, err = O.attend(q, kp, vp, bt, si, 0.3, causal=True, window=W)
+    assert err == 0
+    assert np.array_equal(out_r, out_f) and np.array_equal(lse_r, lse_f)
