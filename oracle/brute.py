@@ -12,9 +12,14 @@ import math
 PAGE = 16
 
 
-def _visible(j: int, pos: int, kend: int, causal: bool, window: int) -> bool:
-    """Is key position j visible to the query row sitting at position pos?"""
+def _visible(j: int, pos: int, kend: int, causal: bool, window: int, first: int = 0) -> bool:
+    """Is key position j visible to the query row sitting at position pos?
+    Keys before `first` (left padding) are hidden, except the row's own key."""
     if j >= kend:
+        return False
+    if j == pos and pos < first:
+        return True
+    if j < first or pos < first:
         return False
     if causal and j > pos:
         return False
@@ -30,7 +35,7 @@ def _slot(block_table, col: int, j: int, ring_rows: int):
     return int(block_table[col][page]), off
 
 
-def attend(q, k_pool, v_pool, block_table, seq_info, scale, causal=False, window=0, ring_rows=0):
+def attend(q, k_pool, v_pool, block_table, seq_info, scale, causal=False, window=0, ring_rows=0, first_valid=None):
     """Same contract as oracle.attend for valid inputs; returns (out, lse) as nested lists."""
     rows, hq, d = len(q), len(q[0]), len(q[0][0])
     hkv = len(k_pool[0][0])
@@ -42,7 +47,8 @@ def attend(q, k_pool, v_pool, block_table, seq_info, scale, causal=False, window
             t, pos = q0 + i, kend - ql + i
             for h in range(hq):
                 g = h // group
-                keys = [j for j in range(kend) if _visible(j, pos, kend, causal, window)]
+                first = max(0, int(first_valid[col])) if first_valid is not None else 0
+                keys = [j for j in range(kend) if _visible(j, pos, kend, causal, window, first)]
                 if not keys:
                     continue
                 scores = []

@@ -50,7 +50,7 @@ def _lib():
                                           p, p, i32, p, i32]
             lib.oracle_append.restype = i32
             lib.oracle_attend.argtypes = [p, i32, i32, p, p, i64, i32, i32, p, i32, i32, i32, p, i32,
-                                          ctypes.c_double, i32, i32, p, p, p]
+                                          ctypes.c_double, i32, i32, p, p, p, p]
             lib.oracle_attend.restype = i32
             lib.oracle_seq_clone.argtypes = [p, p, i32, i64, i32, i32, p, i32, i32, i32, i32, i32, i64]
             lib.oracle_seq_clone.restype = i32
@@ -93,8 +93,12 @@ def append(k_pool: np.ndarray, v_pool: np.ndarray, block_table: np.ndarray, seq_
 
 def attend(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, block_table: np.ndarray,
            seq_info: np.ndarray, scale: float, causal: bool = False, window: int = 0,
-           ring_rows: int = 0):
+           ring_rows: int = 0, first_valid=None):
     """fp64 paged attention.  Returns (out, lse, failed-segment bitmask).
+
+    first_valid (optional, int32 [max_seqs]): each sequence's first valid
+    position (left padding): earlier keys are hidden, and a row sitting before
+    it sees only its own key.
 
     q: (rows, Hq, D); k_pool / v_pool: (num_blocks, 16, Hkv, D); all widened
     to float64 here.  out: (rows, Hq, D); lse: (rows, Hq), natural log.
@@ -111,10 +115,12 @@ def attend(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, block_table: n
     lse = np.zeros((rows, hq), dtype=np.float64)
     max_keys = int(max([int(s[3]) for s in si] + [1]))
     work = np.zeros(max_keys + 1, dtype=np.float64)
+    fv = None if first_valid is None else np.ascontiguousarray(first_valid, dtype=np.int32).reshape(-1)
+    assert fv is None or fv.shape[0] == bt.shape[0]
     errs = _lib().oracle_attend(_ptr(q), hq, rows, _ptr(kp), _ptr(vp), nb, hkv, d, _ptr(bt),
                                 bt.shape[0], bt.shape[1], int(ring_rows), _ptr(si), si.shape[0],
-                                float(scale), int(bool(causal)), int(window), _ptr(out), _ptr(lse),
-                                _ptr(work))
+                                float(scale), int(bool(causal)), int(window),
+                                None if fv is None else _ptr(fv), _ptr(out), _ptr(lse), _ptr(work))
     return out, lse, int(errs)
 
 

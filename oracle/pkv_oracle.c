@@ -87,8 +87,12 @@ static int locate(const oracle_pool *P, int col, int64_t pos, int64_t *blk, int 
     return OR_OK;
 }
 
-/* Key range [lo, hi) that query row i of a segment sees. */
-static void key_range(int64_t kend, int64_t qlen, int64_t i, int causal, int window,
+/* Key range [lo, hi) that query row i of a segment sees.  `first` is the
+ * sequence's first valid position (left padding of a batched prefill,
+ * [tiny-llm kv_cache.py] SlotKVCache / padded_causal_mask): keys before it
+ * are hidden, and a row that itself sits before it sees only its own key
+ * (the diagonal is always kept). */
+static void key_range(int64_t kend, int64_t qlen, int64_t i, int causal, int window, int64_t first,
                       int64_t *lo, int64_t *hi)
 {
     int64_t p = kend - qlen + i;          /* this row's own position */
@@ -96,6 +100,12 @@ static void key_range(int64_t kend, int64_t qlen, int64_t i, int causal, int win
     int64_t last = causal ? p : kend - 1;
     *lo = 0;
     if (window > 0 && last - window + 1 > 0) *lo = last - window + 1;
+    if (p < first) {
+        *lo = p;
+        *hi = p + 1;
+    } else if (*lo < first) {
+        *lo = first;
+    }
 }
 
 /* Segment validity.  The attention needs every key any row of the segment
@@ -103,7 +113,7 @@ static void key_range(int64_t kend, int64_t qlen, int64_t i, int causal, int win
  * (positions kv_end - q_len .. kv_end - 1), so `written_only` narrows the
  * block check to those. */
 static int check_segment(const oracle_pool *P, const int32_t *seg, int total_rows,
-                         int causal, int window, int written_only)
+                         int causal, int window, int64_t first, int written_only)
 {
     int64_t q0 = seg[0], ql = seg[1], col = seg[2], kend = seg[3];
     if (q0 < 0 || ql < 0 || q0 + ql > total_rows) return OR_BAD_SEGMENT;
@@ -119,8 +129,8 @@ static int check_segment(const oracle_pool *P, const int32_t *seg, int total_row
      * to a valid block.  Rows' ranges are nested at the top (all end at or
      * before kv_end) and the first row starts lowest. */
     int64_t lo0, hi0, lo_last, hi_last;
-    key_range(kend, ql, 0, causal, window, &lo0, &hi0);
-    key_range(kend, ql, ql - 1, causal, window, &lo_last, &hi_last);
+    key_range(kend, ql, 0, causal, window, first, &lo0, &hi0);
+    key_range(kend, ql, ql - 1, causal, window, first, &lo_last, &hi_last);
     int64_t lo = lo0 < lo_last ? lo0 : lo_last;
     if (written_only) lo = kend - ql;
     for (int64_t j = lo; j < kend; ++j) {
@@ -148,7 +158,7 @@ int oracle_append(uint8_t *k_pool, uint8_t *v_pool, int elem_size,
     int errs = 0;
     for (int s = 0; s < num_segments; ++s) {
         const int32_t *seg = seq_info + 4 * s;
-        int st = check_segment(&P, seg, total_rows, causal, window, 1);
+        int st = check_segment(&P, seg, total_rows, causal, window, 0, 1);
         if (st) { errs |= 1 << st; continue; }
         for (int64_t i = 0; i < seg[1]; ++i) {
             int64_t t = seg[0] + i;
@@ -174,7 +184,7 @@ int oracle_attend(const double *q, int q_heads, int total_rows,
                   int64_t num_blocks, int kv_heads, int head_dim,
                   const int32_t *block_table, int max_seqs, int max_blocks_per_seq,
                   int ring_rows, const int32_t *seq_info, int num_segments,
-                  double scale, int causal, int window,
+                  double scale, int causal, int window, const int32_t *first_valid,
                   double *out, double *lse, double *work)
 {
     oracle_pool P = {num_blocks, kv_heads, head_dim, block_table, max_seqs,
@@ -189,13 +199,16 @@ int oracle_attend(const double *q, int q_heads, int total_rows,
 
     for (int s = 0; s < num_segments; ++s) {
         const int32_t *seg = seq_info + 4 * s;
-        int st = check_segment(&P, seg, total_rows, causal, window, 0);
+        /* first valid position of the sequence (0 without left padding) */
+        int64_t first = 0;
+        if (first_valid && seg[2] >= 0 && seg[2] < max_seqs && first_valid[seg[2]] > 0) first = first_valid[seg[2]];
+        int st = check_segment(&P, seg, total_rows, causal, window, first, 0);
         if (st) { errs |= 1 << st; continue; }
         int64_t q0 = seg[0], ql = seg[1], col = seg[2], kend = seg[3];
         for (int64_t i = 0; i < ql; ++i) {
             int64_t t = q0 + i;
             int64_t lo, hi;
-            key_range(kend, ql, i, causal, window, &lo, &hi);
+            key_range(kend, ql, i, causal, window, first, &lo, &hi);
             for (int h = 0; h < q_heads; ++h) {
                 int g = h / group;
                 const double *qv = q + (t * q_heads + h) * D;

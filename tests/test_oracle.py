@@ -584,3 +584,78 @@ def test_growable_ring_reads_only_filled_pages():
     out_f, lse_f, err = O.attend(q, kp, vp, bt, si, 0.3, causal=True, window=W)
     assert err == 0
     assert np.array_equal(out_r, out_f) and np.array_equal(lse_r, lse_f)
+
+
+# ---------------------------------------------------------------- left padding (tiny-llm kv_cache.py, SlotKVCache:
+# slot b holds keys at positions first[b] .. lens[b]-1; padded_causal_mask hides keys before first_valid[b] and
+# always keeps the diagonal)
+
+def test_first_valid_zero_is_no_padding():
+    rng = np.random.default_rng(40)
+    q, kp, vp, bt, si = random_paged(rng, [37, 90], [3, 1], 4, 2, 8)
+    a = O.attend(q, kp, vp, bt, si, 0.3, causal=True)
+    b = O.attend(q, kp, vp, bt, si, 0.3, causal=True, first_valid=np.zeros(2, np.int32))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2] == b[2] == 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_left_padding_decode_equals_dense_over_valid_keys(causal):
+    rng = np.random.default_rng(41)
+    kend, first = 70, 23
+    q, kp, vp, bt = identity_case(rng, kend, Hq=4, Hkv=2, D=16)
+    si = np.array([[0, 1, 0, kend]], np.int32)
+    out, lse, err = O.attend(q, kp, vp, bt, si, 0.25, causal=causal, first_valid=np.array([first], np.int32))
+    assert err == 0
+    for h in range(4):
+        g = h // 2
+        ref = sdpa_dense(q[0, h][None], flat_keys(kp, kend, g)[first:], flat_keys(vp, kend, g)[first:], 0.25)
+        assert np.abs(out[0, h] - ref[0]).max() < 1e-12
+
+
+def test_padded_rows_see_only_themselves():
+    # rows at positions before first_valid read exactly their own value
+    rng = np.random.default_rng(42)
+    kend, ql, first = 40, 6, 37          # rows at 34..39: 34, 35, 36 are padding
+    q, kp, vp, bt = identity_case(rng, kend, Hq=2, Hkv=1, D=8, rows=ql)
+    si = np.array([[0, ql, 0, kend]], np.int32)
+    out, lse, err = O.attend(q, kp, vp, bt, si, 0.5, causal=True, first_valid=np.array([first], np.int32))
+    assert err == 0
+    for i in range(3):
+        pos = kend - ql + i
+        for h in range(2):
+            assert np.array_equal(out[i, h], flat_keys(vp, kend, 0)[pos])
+            assert lse[i, h] == pytest.approx(0.5 * float(q[i, h] @ flat_keys(kp, kend, 0)[pos]), abs=1e-12)
+
+
+def test_left_padding_matches_tinyllm_mask_dense():
+    # multi-row causal step with padding: SDPA with the page's padded_causal_mask rule
+    rng = np.random.default_rng(43)
+    kend, ql, first = 30, 8, 25
+    q, kp, vp, bt = identity_case(rng, kend, Hq=2, Hkv=2, D=8, rows=ql)
+    si = np.array([[0, ql, 0, kend]], np.int32)
+    out, _, err = O.attend(q, kp, vp, bt, si, 0.35, causal=True, first_valid=np.array([first], np.int32))
+    assert err == 0
+    start = kend - ql
+    qpos = np.arange(start, kend)[:, None]
+    kpos = np.arange(kend)[None, :]
+    mask = (kpos <= qpos) & ((kpos >= first) | (kpos == qpos))
+    for h in range(2):
+        ref = sdpa_dense(q[:, h], flat_keys(kp, kend, h), flat_keys(vp, kend, h), 0.35, mask=mask)
+        assert np.abs(out[:, h] - ref).max() < 1e-12
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_left_padding_matches_brute_force_twin(seed):
+    rng = np.random.default_rng(100 + seed)
+    lens, qlens = [33, 20, 47], [2, 1, 3]
+    q, kp, vp, bt, si = random_paged(rng, lens, qlens, 4, 2, 8)
+    fv = np.array([rng.integers(0, L + 2) for L in lens], np.int32)
+    for causal in (True, False):
+        out, lse, err = O.attend(q, kp, vp, bt, si, 0.37, causal=causal, window=9, first_valid=fv)
+        assert err == 0
+        bo, bl = brute.attend(q.tolist(), kp.tolist(), vp.tolist(), bt.tolist(), si.tolist(), 0.37, causal=causal,
+                              window=9, first_valid=fv.tolist())
+        assert np.abs(out - np.array(bo)).max() < 1e-12
+        fin = np.isfinite(lse)
+        assert np.array_equal(fin, np.isfinite(np.array(bl)))
+        assert np.abs(lse[fin] - np.array(bl)[fin]).max() < 1e-12
