@@ -90,6 +90,16 @@ typedef enum pkv_dtype { PKV_BF16 = 0, PKV_F32 = 1 } pkv_dtype;
  * capacity the buffers were sized for and generation counts reallocations
  * ([vllm-omni paged_decode.py] PagedDecodeCache.generation); the library
  * reads both and writes generation only in pkv_resize_bucket.
+ *
+ * first_valid (optional, NULL = no padding) is a device int32 array with one
+ * entry per table row: the sequence's first valid position, for batches of
+ * left-padded sequences ([tiny-llm kv_cache.py] SlotKVCache,
+ * padded_causal_mask).  Every query row of that sequence then ignores the
+ * keys before it, and a query row whose own position lies before it (a
+ * padding row) attends to its own key alone, so no row is empty.  A
+ * negative entry counts as 0.  Only the attention calls read it, before the
+ * dependency wait like the block table, so the kernel launched just before
+ * a PDL attention call must not write it.
  */
 typedef struct pkv_cache {
     int32_t num_layers;
@@ -106,6 +116,7 @@ typedef struct pkv_cache {
     const int32_t *block_table; /* device [max_seqs][max_blocks_per_seq] */
     int64_t bucket;
     int64_t generation;
+    const int32_t *first_valid; /* device [max_seqs] or NULL; see above */
 } pkv_cache;
 
 /*

@@ -41,6 +41,7 @@ class CacheDesc(ctypes.Structure):
         ("block_table", ctypes.c_void_p),
         ("bucket", ctypes.c_int64),
         ("generation", ctypes.c_int64),
+        ("first_valid", ctypes.c_void_p),
     ]
 
 

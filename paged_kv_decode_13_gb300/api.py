@@ -39,12 +39,16 @@ class PagedKVCache:
 
     Pools are (num_blocks, 16, kv_heads, head_dim) tensors of bf16 or fp32
     (the layout of vLLM-Omni's SenseNova-U1 PagedDecodeCache); the block
-    table is int32 (max_seqs, max_blocks_per_seq).  The tensors are owned by
-    this object; the descriptor only points at them.
+    table is int32 (max_seqs, max_blocks_per_seq).  first_valid, optional
+    int32 (max_seqs,), is each sequence's first non-padding position for
+    left-padded batches (tiny-llm kv_cache.py, SlotKVCache): the attention
+    calls hide earlier keys and let a padding row see only its own key.  The
+    tensors are owned by this object; the descriptor only points at them.
     """
 
     def __init__(self, k: Sequence[torch.Tensor], v: Sequence[torch.Tensor], block_table: torch.Tensor,
-                 ring_rows: int = 0, bucket: Optional[int] = None, generation: int = 0):
+                 ring_rows: int = 0, bucket: Optional[int] = None, generation: int = 0,
+                 first_valid: Optional[torch.Tensor] = None):
         if len(k) != len(v) or not k:
             raise ValueError("k and v need one tensor per layer")
         shape, dtype = k[0].shape, k[0].dtype
@@ -60,6 +64,10 @@ class PagedKVCache:
         self.k: List[torch.Tensor] = list(k)
         self.v: List[torch.Tensor] = list(v)
         self.block_table = _contig(block_table, "block_table")
+        if first_valid is not None and (first_valid.dtype != torch.int32 or first_valid.dim() != 1
+                                        or first_valid.shape[0] != block_table.shape[0]):
+            raise ValueError("first_valid is int32 (max_seqs,)")
+        self.first_valid = None if first_valid is None else _contig(first_valid, "first_valid")
         self.ring_rows = int(ring_rows)
         self.generation = int(generation)
         nb = shape[0]
@@ -70,7 +78,8 @@ class PagedKVCache:
             num_layers=len(k), kv_heads=shape[2], head_dim=shape[3], dtype=_DTYPES[dtype], num_blocks=nb,
             max_seqs=block_table.shape[0], max_blocks_per_seq=block_table.shape[1], ring_rows=self.ring_rows,
             reserved0=0, k=ctypes.cast(self._kp, ctypes.c_void_p), v=ctypes.cast(self._vp, ctypes.c_void_p),
-            block_table=block_table.data_ptr(), bucket=self.bucket, generation=self.generation)
+            block_table=block_table.data_ptr(), bucket=self.bucket, generation=self.generation,
+            first_valid=_ptr(self.first_valid))
 
     @classmethod
     def allocate(cls, num_layers: int, kv_heads: int, head_dim: int, bucket: int, dtype=torch.bfloat16,

@@ -34,6 +34,7 @@ int check_cache(const pkv_cache *c) {
     if (c->max_seqs <= 0 || c->max_blocks_per_seq <= 0) return PKV_EINVAL;
     if (!c->k || !c->v || !c->block_table) return PKV_EINVAL;
     if ((reinterpret_cast<uintptr_t>(c->block_table) & 3u) != 0) return PKV_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(c->first_valid) & 3u) != 0) return PKV_EINVAL;
     if (c->ring_rows < 0 || c->ring_rows % PKV_BLOCK_SIZE != 0) return PKV_EINVAL;
     if ((long long)c->ring_rows > (long long)c->max_blocks_per_seq * PKV_BLOCK_SIZE) return PKV_EINVAL;
     return PKV_OK;
@@ -320,6 +321,7 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     p.v_pool_w = c->v[layer];
     p.block_table = c->block_table;
     p.seq_info = reinterpret_cast<const int4 *>(seq_info);
+    p.first_valid = c->first_valid;
     p.out = out;
     p.lse = lse;
     p.err = err;

@@ -546,8 +546,8 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     // Positions fit in 32 bits: kv_end <= 2^31 - 33 is part of segment validity.
     const int kend = sg.kend;
     const int new_start = kend - sg.ql;  // first position appended this step
-    int lo_u = 0;
-    if (p.window > 0) lo_u = max(0, (p.causal ? new_start : kend - 1) - p.window + 1);
+    const int first = first_valid_of(p.first_valid, sg.col);
+    const int lo_u = segment_key_lo(new_start, kend, p.causal, p.window, first);
     const int pb_begin = lo_u / kPage;
     const int pb_end = (kend + kPage - 1) / kPage;
     const int nblk = pb_end - pb_begin;
@@ -751,12 +751,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     for (int r = tid; r < R; r += NT) {
         const int ur = row0 + r;
         int lo = 0, hi = 0;
-        if (ur < rows_unit) {
-            const int pos = new_start + ur / p.G;
-            const int newest = p.causal ? pos : kend - 1;
-            hi = p.causal ? pos + 1 : kend;
-            lo = p.window > 0 ? max(0, newest - p.window + 1) : 0;
-        }
+        if (ur < rows_unit) row_key_bounds(new_start + ur / p.G, kend, p.causal, p.window, first, lo, hi);
         sLo[r] = lo;
         sHi[r] = hi;
     }

@@ -167,6 +167,7 @@ struct AttendParams {
     void *v_pool_w;
     const int *block_table; // [max_seqs][mbps]
     const int4 *seq_info;   // [S]
+    const int *first_valid; // [max_seqs] first non-padding position, or null (no padding)
     float *out;             // [rows][Hq][D]
     float *lse;             // [rows][Hq] or null
     unsigned *err;
@@ -234,6 +235,42 @@ __device__ __forceinline__ int table_page(int pb, int ring_rows) {
 __device__ __forceinline__ Segment load_segment(const int4 *seq_info, int s) {
     int4 v = seq_info[s];
     return Segment{v.x, v.y, v.z, v.w};
+}
+
+// ---------------------------------------------------------------- key ranges
+
+// Left padding ([tiny-llm kv_cache.py] SlotKVCache, padded_causal_mask):
+// keys before a sequence's first valid position are hidden from every row,
+// and a row that is itself padding sees only its own key (the diagonal is
+// always kept, so no row is fully masked).
+__device__ __forceinline__ int first_valid_of(const int *first_valid, int col) {
+    return first_valid ? max(first_valid[col], 0) : 0;
+}
+
+// Keys [lo, hi) of the row at position `pos` of a segment ending at kv_end:
+// causal rows end at their own position, a window of W keeps the last W keys
+// up to the row's newest key, padding as above.
+__device__ __forceinline__ void row_key_bounds(int pos, int kend, int causal, int window, int first,
+                                               int &lo, int &hi) {
+    const int newest = causal ? pos : kend - 1;
+    hi = causal ? pos + 1 : kend;
+    lo = window > 0 ? max(0, newest - window + 1) : 0;
+    if (pos < first) {
+        lo = pos;
+        hi = pos + 1;
+    } else {
+        lo = max(lo, first);
+    }
+}
+
+// Lowest key any row of the segment reads.  Bounds are non-decreasing in
+// the row's position, so it is the first row's: with padded rows that is
+// the step's first position (a padded row reads its own key; the others
+// start at `first`, which is past it).
+__device__ __forceinline__ int segment_key_lo(int new_start, int kend, int causal, int window, int first) {
+    int lo, hi;
+    row_key_bounds(new_start, kend, causal, window, first, lo, hi);
+    return lo;
 }
 
 }  // namespace pkv

@@ -159,8 +159,8 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     }
     const int kend = sg.kend;
     const int new_start = kend - sg.ql;
-    int lo_u = 0;
-    if (p.window > 0) lo_u = max(0, (p.causal ? new_start : kend - 1) - p.window + 1);
+    const int first = first_valid_of(p.first_valid, sg.col);
+    const int lo_u = segment_key_lo(new_start, kend, p.causal, p.window, first);
     const int pb_begin = lo_u / kPage;
     const int pb_end = (kend + kPage - 1) / kPage;
     const int nblk = pb_end - pb_begin;
@@ -405,12 +405,8 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         const int n = 2 * tq + e;
         lo_r[e] = 0;
         hi_r[e] = 0;
-        if (n < rows_unit) {
-            const int pos = new_start + n / p.G;
-            const int newest = p.causal ? pos : kend - 1;
-            hi_r[e] = p.causal ? pos + 1 : kend;
-            lo_r[e] = p.window > 0 ? max(0, newest - p.window + 1) : 0;
-        }
+        if (n < rows_unit)
+            row_key_bounds(new_start + n / p.G, kend, p.causal, p.window, first, lo_r[e], hi_r[e]);
     }
     if (first_cta) apply_coverage(p, sCov, cov_any, NT);
     #pragma unroll 1

@@ -12,7 +12,7 @@ PAGE = 16
 TOL = {torch.bfloat16: 2e-3, torch.float32: 1e-5}
 
 
-def device_cache(pkv, w, canary: bool = False):
+def device_cache(pkv, w, canary: bool = False, first_valid=None):
     """PagedKVCache over copies of w's pools on cuda.  With canary=True each
     pool is a slice of a larger buffer whose margins hold a sentinel, so an
     out-of-range write shows up in check_canaries()."""
@@ -28,7 +28,9 @@ def device_cache(pkv, w, canary: bool = False):
         else:
             view = t.to(dev).contiguous()
         (ks if len(ks) < len(w.k) else vs).append(view)
-    cache = pkv.PagedKVCache(ks, vs, w.block_table.to(dev), ring_rows=w.ring_rows, bucket=w.bucket)
+    fv = None if first_valid is None else torch.as_tensor(first_valid, dtype=torch.int32).to(dev)
+    cache = pkv.PagedKVCache(ks, vs, w.block_table.to(dev), ring_rows=w.ring_rows, bucket=w.bucket,
+                             first_valid=fv)
     cache._guards = guards
     return cache
 
@@ -97,17 +99,21 @@ def oracle_pools(w, layer: int):
     return kt, vt
 
 
-def oracle_attend(w, layer: int, segs=None, causal=None, window=None):
+def oracle_attend(w, layer: int, segs=None, causal=None, window=None, first_valid=None):
     """fp64 oracle on layer `layer` for the segments `segs` (all by default),
     over the oracle-appended pools.  Returns (out, lse) over all rows; rows of
-    other segments are zero."""
+    other segments are zero.  first_valid is indexed by the table row."""
     si = w.seq_info.cpu().numpy()
     segs = list(range(si.shape[0])) if segs is None else list(segs)
     k_pool, v_pool = oracle_pools(w, layer)
     kp, vp, bt, sub = compact(w, layer, segs, k_pool, v_pool)
+    fv = None
+    if first_valid is not None:   # compact() renumbers the table rows 0..len(segs)-1
+        fv = np.array([int(first_valid[int(si[s, 2])]) for s in segs], np.int32)
     out, lse, err = O.attend(f64(w.q[layer]), f64(kp), f64(vp), bt, sub, w.scale,
                              causal=w.causal if causal is None else causal,
-                             window=w.window if window is None else window, ring_rows=w.ring_rows)
+                             window=w.window if window is None else window, ring_rows=w.ring_rows,
+                             first_valid=fv)
     assert err == 0, f"oracle rejected the workload: {err:#x}"
     return out, lse
 

@@ -4,6 +4,7 @@ launching anything."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -40,9 +41,10 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_layout_matches_header(lib):
-    # int32 x4, int64, int32 x4, three pointers, int64 x2 on LP64.
-    assert ctypes.sizeof(lib.CacheDesc) == 4 * 4 + 8 + 4 * 4 + 3 * 8 + 2 * 8
+    # int32 x4, int64, int32 x4, three pointers, int64 x2, one pointer on LP64.
+    assert ctypes.sizeof(lib.CacheDesc) == 4 * 4 + 8 + 4 * 4 + 3 * 8 + 2 * 8 + 8
     assert lib.CacheDesc.k.offset == 40 and lib.CacheDesc.bucket.offset == 64
+    assert lib.CacheDesc.first_valid.offset == 80
 
 
 def test_bucket_for_matches_golden(lib):
@@ -192,3 +194,17 @@ def test_binding_fails_loudly_without_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import paged_kv_decode_13_gb300"], cwd=tmp_path,
                        capture_output=True, text=True)
     assert r.returncode != 0 and "libpkv.so not found" in r.stderr
+
+
+def test_struct_layout_matches_compiled_header(lib, tmp_path):
+    # the C compiler's own offsets for include/pkv.h against the ctypes mirror
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "pkv.h"\n'
+                   'int main(void) { printf("%zu", sizeof(pkv_cache));\n'
+                   + "".join(f'  printf(" %zu", offsetof(pkv_cache, {n}));\n' for n, _ in lib.CacheDesc._fields_)
+                   + "  return 0; }\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(lib.CacheDesc)
+    assert got[1:] == [getattr(lib.CacheDesc, n).offset for n, _ in lib.CacheDesc._fields_]

@@ -26,10 +26,10 @@ def pkv():
 
 
 def run(pkv, w, layer=0, fused=True, flags=0, num_splits=0, max_q_len=None, max_kv=None, canary=True,
-        workspace=False):
+        workspace=False, first_valid=None):
     """Append + attend layer `layer` of w on the GPU.  Returns (out, lse, err, cache).  With
     workspace=True the split merge goes through a workspace (decode kernel) instead of the cluster."""
-    cache = U.device_cache(pkv, w, canary=canary)
+    cache = U.device_cache(pkv, w, canary=canary, first_valid=first_valid)
     dev = torch.device("cuda")
     q = w.q[layer].to(dev)
     kn = w.k_new[layer].to(dev)
@@ -63,9 +63,9 @@ def run(pkv, w, layer=0, fused=True, flags=0, num_splits=0, max_q_len=None, max_
     return out, lse, int(err.item()), cache
 
 
-def check_against_oracle(w, layer, out, lse, cache, segs=None, tol=None):
+def check_against_oracle(w, layer, out, lse, cache, segs=None, tol=None, first_valid=None):
     tol = tol or U.TOL[w.dtype]
-    ref, ref_lse = U.oracle_attend(w, layer, segs=segs)
+    ref, ref_lse = U.oracle_attend(w, layer, segs=segs, first_valid=first_valid)
     rows = U.rows_of(w, segs) if segs is not None else list(range(w.total_rows))
     got = U.f64(out)[rows]
     exp = ref[rows]

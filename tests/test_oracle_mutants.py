@@ -30,6 +30,8 @@ MUTANTS = {
     "tail_step_floor": ("int64_t steps = (over + kTailStep - 1) / kTailStep;",
                         "int64_t steps = over / kTailStep + 1;"),
     "v_from_k": ("const double *vv = v_pool +", "const double *vv = k_pool +"),
+    "padding_keys_not_hidden": ("} else if (*lo < first) {", "} else if (0) {"),
+    "padding_row_sees_prefix": ("*lo = p;\n", "*lo = 0;\n"),
 }
 
 
