@@ -202,6 +202,88 @@ def time_clone(pkv, device, flush, stream, reps: int = 10, warmup: int = 3):
     return ms, moved
 
 
+def workload_bytes_flops(w):
+    """Algorithmic bytes and flops of one fused append + attention launch over
+    workload w: K and V of every key some row of a segment reads (per kv
+    head), q, the appended rows, the fp32 output, the touched table entries
+    and the segment entries; flops 4 * D per (query head, row, visible key)."""
+    eb = w.k[0].element_size()
+    kv = q = app = out = table = flops = 0
+    for q0, ql, col, kend in w.seq_info.tolist():
+        first = kend - ql
+        newest0 = first if w.causal else kend - 1
+        lo = max(0, newest0 - w.window + 1) if w.window > 0 else 0
+        kv += (kend - lo) * w.kv_heads * w.head_dim * 2 * eb
+        table += 4 * ((kend + 15) // 16 - lo // 16)
+        for i in range(ql):
+            p = first + i
+            hi = p + 1 if w.causal else kend
+            rlo = max(0, (p if w.causal else kend - 1) - w.window + 1) if w.window > 0 else 0
+            flops += 4 * w.q_heads * w.head_dim * (hi - rlo)
+        q += ql * w.q_heads * w.head_dim * eb
+        app += 2 * ql * w.kv_heads * w.head_dim * eb
+        out += ql * w.q_heads * w.head_dim * 4
+    return kv + q + app + out + table + 16 * w.num_segments, flops
+
+
+CONFIGS = (
+    ("batched varlen: S=32, lengths U[1,16384], shuffled shared-pool tables, GQA 32:8, D 128, bf16, q_len 1",
+     "batched", dict(S=32, max_len=16384)),
+    ("spec verify, causal: S=16, q_len U[1,16] aligned to kv_end, GQA 64:8, D 128, bf16, KV U[256,8192]",
+     "spec_verify", dict(S=16, max_q=16, len_lo=256, len_hi=8192, causal=True)),
+    ("spec verify, non-causal draft blocks: same shapes, causal off",
+     "spec_verify", dict(S=16, max_q=16, len_lo=256, len_hi=8192, causal=False)),
+    ("long context, full causal: S=4, KV 131072 flat, GQA 32:4, D 256, bf16, q_len 1",
+     "long_context", dict(S=4, kv_len=131072)),
+    ("long context, window 4096 over a 4096-row ring: S=4, KV 131072, GQA 32:4, D 256, bf16, q_len 1",
+     "long_context", dict(S=4, kv_len=131072, window=4096, ring_rows=4096)),
+)
+
+
+def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int = 50, warmup: int = 5):
+    """The other workloads of the scope table, one fused append + attention
+    call each (one launch), L2 flushed before every timed call: median µs,
+    algorithmic GB/s and its fraction of the copy peak."""
+    import torch
+
+    import workloads
+    res = []
+    for name, gen, kw in CONFIGS:
+        w = getattr(workloads, gen)(seed=seed, device=device, **kw)
+        cache = pkv.PagedKVCache(w.k, w.v, w.block_table, ring_rows=w.ring_rows, bucket=w.bucket)
+        q, kn, vn, si = w.q[0], w.k_new[0], w.v_new[0], w.seq_info
+        out = torch.empty(w.total_rows, w.q_heads, w.head_dim, device=device)
+        err = pkv.new_err_flags(device)
+        max_kv = int(si[:, 3].max().item())
+
+        def call():
+            pkv.append_attend(cache, 0, q, kn, vn, si, out, err, w.max_q_len, max_kv, w.scale, w.causal,
+                              w.window, stream=stream)
+
+        for _ in range(warmup):
+            flush()
+            call()
+        evs = []
+        for _ in range(reps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        if int(err.item()):
+            raise RuntimeError(f"{name}: device error flags {int(err.item()):#x}")
+        ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+        nbytes, flops = workload_bytes_flops(w)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res.append({"workload": name, "us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                    "frac_of_peak": round(gbs / peak, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2)})
+        del w, cache, q, kn, vn, si, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def time_e2e(runner, steps: int, warmup: int, flush, stream):
     """Per step: pinned host -> device copy of the step's inputs, graph replay,
     device -> host copy of the outputs, all inside the timed events."""
@@ -347,6 +429,10 @@ def gpu_arm(args):
                  "frac_of_peak": round(cgbs / peak, 4)}
         torch.cuda.empty_cache()
 
+    by_config = None
+    if not args.no_sweep:
+        by_config = time_configs(pkv, device, flush, stream, peak, seed=rank)
+
     traffic = None
     if os.path.exists(PROFILE):
         with open(PROFILE) as f:
@@ -381,6 +467,7 @@ def gpu_arm(args):
                          "launch_ms": round(per_launch_ms, 6)},
             "by_kv_len": by_len,
             "seq_clone": clone,
+            "by_config": by_config,
             "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "µs/step", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,

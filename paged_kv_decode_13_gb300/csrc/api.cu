@@ -17,7 +17,7 @@ using namespace pkv;
 namespace {
 
 constexpr int kDefaultSms = 152;       // GB300, used when no device is visible
-constexpr int kTargetCtas = 4 * 152;   // aim for a few CTAs per SM when choosing the split count
+constexpr int kTargetWaves = 3;        // split count: about this many waves of resident CTAs
 constexpr int kMaxCluster = 16;        // largest thread-block cluster (non-portable size)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -178,7 +178,10 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
         return PKV_OK;
     }
     if (n == 0) {
-        const long long want = (kTargetCtas + units - 1) / units;
+        // CTAs of this kernel that fit on one SM by shared memory
+        const long long per_sm = std::max<long long>(1, 232448 / ((long long)pl->k.smem + 1024));
+        const long long target = (long long)kTargetWaves * device_sms() * per_sm;
+        const long long want = (target + units - 1) / units;
         n = 1;
         while (n < want && n < kMaxCluster) n *= 2;
     }
@@ -306,9 +309,9 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     const int ncta = S == 0 ? 1 : pl.gm ? pl.ncta : schedulable_cluster(pl.k, pl.ncta);
 
     AttendParams p;
-    // The decode kernel takes a page tile in one box when head_dim fills its
-    // padded width exactly (128 or 256; the other kernels use the 4-D view).
-    const bool page_box = pl.k.rows == 8 && c->dtype == PKV_BF16 && c->head_dim == pl.k.dp && c->head_dim > 64;
+    // bf16 page tiles come in one box when head_dim fills its padded width
+    // exactly (128 or 256); otherwise, and for fp32, the 4-D view.
+    const bool page_box = c->dtype == PKV_BF16 && c->head_dim == pl.k.dp && c->head_dim > 64;
     auto encode = [&](CUtensorMap *m, const void *pool) {
         return page_box ? encode_pool_pages(m, pool, c) : encode_pool(m, pool, c);
     };

@@ -68,6 +68,12 @@ struct AttnCfg {
     static constexpr size_t kRecvNeed = ((size_t)kRows * DP + 16) * 4;
     static constexpr bool kPush = kBaseBytes + kRecvNeed <= 232448;
     static constexpr size_t kSmemBytes = kBaseBytes + (kPush ? kRecvNeed : 0);
+    // L2 warm-up before the dependency wait: each key group prefetches up to
+    // kL2Pages pages past its stages, about 512 KB per SM over the CTAs that
+    // fit on one (at most 32 pages: the page-id window of a warp).
+    static constexpr int kCtasPerSm = (int)(232448 / (kSmemBytes + 1024)) > 0 ? (int)(232448 / (kSmemBytes + 1024)) : 1;
+    static constexpr int kL2PagesRaw = (int)(524288 / ((size_t)kCtasPerSm * KW * kStageBytes));
+    static constexpr int kL2Pages = kL2PagesRaw < 1 ? 1 : kL2PagesRaw > 32 - NST ? 32 - NST : kL2PagesRaw;
     static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
     static_assert(kQBytes % 16 == 0, "smem sections stay 16-byte aligned");
     static_assert(!MMA || sizeof(T) == 2, "tensor-core path is bf16");
@@ -469,6 +475,10 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     constexpr int DP = C::DP, MT = C::MT, KW = C::KW, NST = C::NST;
     constexpr int EPC = C::kEpc, R = C::kRows, NT = C::kThreads;
     constexpr int GT = MT * 32;  // threads per key group
+    // Each key group's last warp issues its copies: a tile with fewer rows
+    // than the CTA holds leaves its last warps without rows to compute, and
+    // the copies then cost the computing warps nothing.
+    constexpr int kIssuer = MT - 1;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *body = reinterpret_cast<unsigned char *>(
@@ -592,8 +602,8 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         app_ok = __syncthreads_and(ok);
     }
 
-    // Page ids of this group's pages, 32 at a time, held by the group's first
-    // warp: lane l holds the id of the group's page (window + l).
+    // Page ids of this group's pages, 32 at a time, held by the group's
+    // issuing warp: lane l holds the id of the group's page (window + l).
     int id_reg = -1, id_window = -1;
     bool bad = false, timed_out = false;
     auto load_ids = [&](int j) {
@@ -602,7 +612,21 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         id_reg = -1;
         if (li < nb) id_reg = bt_row[table_page(cb0 + li, p.ring_rows)];
     };
-    // Issue the TMA copies of the group's j-th page (called by the group's first warp).
+    // Warm L2 with page `bid` of this kv head (K and V).
+    auto prefetch_page = [&](int bid) {
+        if (p.page_box) {
+            tma_prefetch_l2_5d(&p.tmap_k, 0, 0, 0, g, bid);
+            tma_prefetch_l2_5d(&p.tmap_v, 0, 0, 0, g, bid);
+        } else {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
+            }
+        }
+    };
+    // Issue the TMA copies of the group's j-th page (called by the group's
+    // issuing warp).
     auto issue = [&](int j) {
         if ((j & ~31) != id_window) load_ids(j);
         const int bid = __shfl_sync(0xffffffffu, id_reg, j & 31);
@@ -614,10 +638,15 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             if (ok) {
                 fence_proxy_async();
                 mbar_expect_tx(bar, C::kStageBytes);
+                if (p.page_box) {
+                    tma_load_5d(st, &p.tmap_k, bar, 0, 0, 0, g, bid);
+                    tma_load_5d(st + C::kTileBytes, &p.tmap_v, bar, 0, 0, 0, g, bid);
+                } else {
 #pragma unroll
-                for (int b = 0; b < C::kBoxes; ++b) {
-                    tma_load_4d(st + b * 2048, &p.tmap_k, bar, b * C::kBoxEl, g, 0, bid);
-                    tma_load_4d(st + C::kTileBytes + b * 2048, &p.tmap_v, bar, b * C::kBoxEl, g, 0, bid);
+                    for (int b = 0; b < C::kBoxes; ++b) {
+                        tma_load_4d(st + b * 2048, &p.tmap_k, bar, b * C::kBoxEl, g, 0, bid);
+                        tma_load_4d(st + C::kTileBytes + b * 2048, &p.tmap_v, bar, b * C::kBoxEl, g, 0, bid);
+                    }
                 }
             } else {
                 mbar_arrive(bar);  // nothing to fetch: complete the phase, the result is discarded
@@ -666,7 +695,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
 
     // ---- prologue: start the first stages before waiting on the previous kernel
     int issued = 0;
-    if (mt == 0) {
+    if (mt == kIssuer) {
         load_ids(0);
         #pragma unroll 1
         for (; issued < NST && issued < n_mine; ++issued) {
@@ -674,21 +703,13 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             issue(issued);
         }
     }
-    // Pages past the shared-memory stages (up to ~128 KB per key group) are
-    // prefetched into L2 now, so their HBM traffic overlaps the previous
-    // kernel's tail and the later TMA copies hit L2.  Lane l of the group's
-    // first warp holds page l's id.
-    if (mt == 0) {
-        constexpr int kL2Pages = (131072 / (int)C::kStageBytes) > 0 ? 131072 / (int)C::kStageBytes : 1;
-        const int pf_end = min(min(n_mine, 32), NST + kL2Pages);
+    // Pages past the shared-memory stages are prefetched into L2 now, so
+    // their HBM traffic overlaps the previous kernel's tail and the later TMA
+    // copies hit L2.  Lane l of the issuing warp holds page l's id.
+    if (mt == kIssuer) {
         const int bid = id_reg;
-        if (lane >= issued && lane < pf_end && bid >= 0 && (long long)bid < p.num_blocks) {
-#pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b) {
-                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
-                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
-            }
-        }
+        if (lane >= issued && lane < min(n_mine, NST + C::kL2Pages) && bid >= 0 && (long long)bid < p.num_blocks)
+            prefetch_page(bid);
     }
     pdl_wait();
     pdl_trigger();
@@ -755,7 +776,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         sLo[r] = lo;
         sHi[r] = hi;
     }
-    if (mt == 0) {
+    if (mt == kIssuer) {
         #pragma unroll 1
         for (; issued < NST && issued < n_mine; ++issued) issue(issued);
     }
@@ -822,30 +843,42 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         group_sync();
     };
 
-    // Two pages per pass where the ring holds them (independent MMA chains).
-    constexpr int kPair = C::MMA && NST >= 2 ? 2 : 1;
+    // Several pages per pass where the ring holds them (independent MMA
+    // chains): four with eight stages, else two.
+    constexpr int kPair = C::MMA && NST >= 8 ? 4 : C::MMA && NST >= 2 ? 2 : 1;
 #pragma unroll 1
     for (int j = 0; j < n_mine; j += kPair) {
         const int np = min(kPair, n_mine - j);
-        unsigned char *st[2];
-        int pos0[2];
+        unsigned char *st[4];
+        int pos0[4];
 #pragma unroll
         for (int u = 0; u < kPair; ++u) {
             const int jj = j + min(u, np - 1);
             st[u] = gstage + (size_t)(jj % NST) * C::kStageBytes;
             pos0[u] = (cb0 + kw + jj * KW) * kPage;
         }
-        wait_page(j);
-        fix_page(j, st[0], pos0[0]);
-        if (np > 1) {
-            wait_page(j + 1);
-            fix_page(j + 1, st[1], pos0[1]);
+#pragma unroll
+        for (int u = 0; u < kPair; ++u) {
+            if (u < np) {
+                wait_page(j + u);
+                fix_page(j + u, st[u], pos0[u]);
+            }
         }
         if (nrw > 0) {
             if constexpr (C::MMA) {
-                const unsigned char *ks[2] = {st[0], st[kPair - 1]};
-                const unsigned char *vs[2] = {st[0] + C::kTileBytes, st[kPair - 1] + C::kTileBytes};
-                if (np == 2)
+                const unsigned char *ks[4], *vs[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    ks[u] = st[min(u, kPair - 1)];
+                    vs[u] = st[min(u, kPair - 1)] + C::kTileBytes;
+                }
+                if (np == 4)
+                    mw.template consume<4>(reinterpret_cast<const T *>(qarea), ks, vs, pos0, sLo, sHi, mt, lane,
+                                           p.scale_log2);
+                else if (np == 3)
+                    mw.template consume<3>(reinterpret_cast<const T *>(qarea), ks, vs, pos0, sLo, sHi, mt, lane,
+                                           p.scale_log2);
+                else if (np == 2)
                     mw.template consume<2>(reinterpret_cast<const T *>(qarea), ks, vs, pos0, sLo, sHi, mt, lane,
                                            p.scale_log2);
                 else
@@ -857,12 +890,13 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             }
         }
         group_sync();  // every warp of the group is done with these stages
-        if (mt == 0) {
-            if (j + NST < n_mine) issue(j + NST);
-            if (np > 1 && j + 1 + NST < n_mine) issue(j + 1 + NST);
+        if (mt == kIssuer) {
+#pragma unroll
+            for (int u = 0; u < kPair; ++u)
+                if (u < np && j + u + NST < n_mine) issue(j + u + NST);
         }
     }
-    if (timed_out && lane == 0 && mt == 0) {
+    if (timed_out && lane == 0 && mt == kIssuer) {
         // Give the copies still in flight a bounded chance to land before the
         // stage memory is reused.
         #pragma unroll 1

@@ -5,7 +5,9 @@
 // Per row class the tuple is (row tiles MT, key groups KW, stages NST): stage
 // counts keep a CTA near 100-135 KB of shared memory where the page size
 // allows (two CTAs per SM), and fp32 / wide heads drop to fewer key groups or
-// a 64-row cap to stay inside the 227 KB limit.
+// a 64-row cap to stay inside the 227 KB limit.  The 128-row tensor-core
+// class takes eight stages: its ring aliases the key-group merge buffer,
+// which is at least as large, so the deeper ring costs no shared memory.
 #include "attend.cuh"
 #include "decode.cuh"
 #include "launch.h"
@@ -49,7 +51,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
         if (rc == 0) return CFG(B16, 1, 4, 4, true);
         if (rc == 1) return CFG(B16, 2, 2, 4, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);
-        return CFG(B16, 8, 1, 4, true);
+        return CFG(B16, 8, 1, 8, true);
     }
 #elif PKV_INST_DP == 128
     {
@@ -58,7 +60,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
         if (rc == 0) return CFG(B16, 1, 4, 3, true);
         if (rc == 1) return CFG(B16, 2, 2, 4, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);
-        return CFG(B16, 8, 1, 4, true);
+        return CFG(B16, 8, 1, 8, true);
     }
 #else
     {
@@ -66,7 +68,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
         if (rc == 0) return CFG(B16, 1, 4, 2, true);
         if (rc == 1) return CFG(B16, 2, 2, 3, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);
-        return CFG(B16, 8, 1, 4, true);
+        return CFG(B16, 8, 1, 8, true);
     }
 #endif
 #elif PKV_INST_VARIANT == 1

@@ -65,6 +65,12 @@ struct DecCfg {
     static constexpr size_t kCovBytes = (size_t)kThreads * 4;
     static constexpr size_t kSmemBytes =
         1024 + kPipeBytes + kRecvBytes + kStatBytes + kBarBytes + kFlagBytes + kCovBytes + kWnBytes;
+    // L2 warm-up before the dependency wait: each warp prefetches up to
+    // kL2Pages pages past its stages, about 512 KB per SM over the CTAs that
+    // fit on one (at most 32 pages: the page-id window of a warp).
+    static constexpr int kCtasPerSm = (int)(232448 / (kSmemBytes + 1024)) > 0 ? (int)(232448 / (kSmemBytes + 1024)) : 1;
+    static constexpr int kL2PagesRaw = (int)(524288 / ((size_t)kCtasPerSm * KW * kStageBytes));
+    static constexpr int kL2Pages = kL2PagesRaw < 1 ? 1 : kL2PagesRaw > 32 - NST ? 32 - NST : kL2PagesRaw;
     static_assert(kThreads >= 128, "the merges map 8 rows x 16 onto the first 128 threads");
     static_assert(kPartBytes <= NST * kStageBytes, "a warp's partial fits over its own stages");
     static_assert(DP % kBoxEl == 0, "page rows are whole 128-byte boxes");
@@ -207,6 +213,20 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         id_reg = -1;
         if (li < nb) id_reg = bt_row[table_page(cb0 + li, p.ring_rows)];
     };
+    // Warm L2 with page `bid` of this kv head (K and V).
+    auto prefetch_page = [&](int bid) {
+        if (p.page_box) {
+            tma_prefetch_l2_5d(&p.tmap_k, 0, 0, 0, g, bid);
+            tma_prefetch_l2_5d(&p.tmap_v, 0, 0, 0, g, bid);
+        } else {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
+                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
+            }
+        }
+    };
+    // Issue the TMA copies of the warp's j-th page.
     auto issue = [&](int j) {
         if ((j & ~31) != id_window) load_ids(j);
         const int bid = __shfl_sync(0xffffffffu, id_reg, j & 31);
@@ -246,19 +266,6 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         if (!__all_sync(0xffffffffu, done)) timed_out = true;
     };
 
-    // Warm L2 with page `bid` of this kv head (K and V).
-    auto prefetch_page = [&](int bid) {
-        if (p.page_box) {
-            tma_prefetch_l2_5d(&p.tmap_k, 0, 0, 0, g, bid);
-            tma_prefetch_l2_5d(&p.tmap_v, 0, 0, 0, g, bid);
-        } else {
-#pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b) {
-                tma_prefetch_l2_4d(&p.tmap_k, b * C::kBoxEl, g, 0, bid);
-                tma_prefetch_l2_4d(&p.tmap_v, b * C::kBoxEl, g, 0, bid);
-            }
-        }
-    };
     // A whole page of the next layer (every kv head, K and V: one contiguous
     // block each), one bulk prefetch per tensor.
     const unsigned page_bytes = (unsigned)(kPage * p.Hkv * p.D * (int)sizeof(T));
@@ -300,14 +307,12 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
             }
         }
     }
-    // The warp's pages past its stages go to L2 now (up to ~128 KB per warp),
-    // so their HBM traffic overlaps the previous kernel's tail.  Lane l holds
-    // the id of the warp's page kw + l * KW.
+    // The warp's pages past its stages go to L2 now, so their HBM traffic
+    // overlaps the previous kernel's tail.  Lane l holds the id of the warp's
+    // page kw + l * KW.
     {
-        constexpr int kL2Pages = (131072 / (int)C::kStageBytes) > 0 ? 131072 / (int)C::kStageBytes : 1;
         const int bid = id_reg;
-        if (lane >= issued && lane < min(min(n_mine, 32), NST + kL2Pages) && bid >= 0 &&
-            (long long)bid < p.num_blocks)
+        if (lane >= issued && lane < min(n_mine, NST + C::kL2Pages) && bid >= 0 && (long long)bid < p.num_blocks)
             prefetch_page(bid);
     }
     // The next layer's first pages of the same range (same table and

@@ -46,7 +46,7 @@ def _rank_main(rank, world, port, results):
 
 def test_max_over_ranks_gloo_world2():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_rank_main, args=(2, port, results), nprocs=2, join=True)
         assert dict(results) == {0: 2.5, 1: 2.5}

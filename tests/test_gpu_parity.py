@@ -294,6 +294,21 @@ def test_split_count_does_not_change_result(pkv, num_splits):
     check_against_oracle(w, 0, out, lse, cache)
 
 
+@pytest.mark.parametrize("q_heads,max_q,flags", [(64, 16, 0), (64, 8, 0), (32, 8, 0), (16, 8, 0), (64, 16, 1)])
+@pytest.mark.parametrize("num_splits", [1, 3])
+def test_long_ranges_per_cta_rolling_warm_up(pkv, q_heads, max_q, flags, num_splits):
+    # one or three CTAs per range of 2000..5000 keys: each key group copies
+    # far more pages than its stages and the warm-up distance hold, so the
+    # rolling L2 warm-up runs through several page-id windows (every row
+    # class of the general kernel; flags 1: the CUDA-core kernel)
+    w = U.nan_tails(workloads.spec_verify(S=4, max_q=max_q, len_lo=2000, len_hi=5000, seed=70 + q_heads + max_q,
+                                          q_heads=q_heads, kv_heads=8))
+    out, lse, err, cache = run(pkv, w, num_splits=num_splits, max_kv=5000, flags=flags)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
 def test_fused_equals_two_calls_bitwise(pkv):
     w = U.nan_tails(workloads.spec_verify(S=5, max_q=8, len_lo=100, len_hi=900, seed=11, q_heads=16))
     a, la, ea, ca = run(pkv, w, fused=True, max_kv=900)
