@@ -227,20 +227,20 @@ def workload_bytes_flops(w):
 
 
 CONFIGS = (
-    ("batched varlen: S=32, lengths U[1,16384], shuffled shared-pool tables, GQA 32:8, D 128, bf16, q_len 1",
-     "batched", dict(S=32, max_len=16384)),
-    ("spec verify, causal: S=16, q_len U[1,16] aligned to kv_end, GQA 64:8, D 128, bf16, KV U[256,8192]",
-     "spec_verify", dict(S=16, max_q=16, len_lo=256, len_hi=8192, causal=True)),
-    ("spec verify, non-causal draft blocks: same shapes, causal off",
+    ("batched", "batched varlen: S=32, lengths U[1,16384], shuffled shared-pool tables, GQA 32:8, D 128, bf16, "
+     "q_len 1", "batched", dict(S=32, max_len=16384)),
+    ("verify_causal", "spec verify, causal: S=16, q_len U[1,16] aligned to kv_end, GQA 64:8, D 128, bf16, "
+     "KV U[256,8192]", "spec_verify", dict(S=16, max_q=16, len_lo=256, len_hi=8192, causal=True)),
+    ("verify_noncausal", "spec verify, non-causal draft blocks: same shapes, causal off",
      "spec_verify", dict(S=16, max_q=16, len_lo=256, len_hi=8192, causal=False)),
-    ("long context, full causal: S=4, KV 131072 flat, GQA 32:4, D 256, bf16, q_len 1",
+    ("long_context", "long context, full causal: S=4, KV 131072 flat, GQA 32:4, D 256, bf16, q_len 1",
      "long_context", dict(S=4, kv_len=131072)),
-    ("long context, window 4096 over a 4096-row ring: S=4, KV 131072, GQA 32:4, D 256, bf16, q_len 1",
-     "long_context", dict(S=4, kv_len=131072, window=4096, ring_rows=4096)),
+    ("long_context_ring", "long context, window 4096 over a 4096-row ring: S=4, KV 131072, GQA 32:4, D 256, "
+     "bf16, q_len 1", "long_context", dict(S=4, kv_len=131072, window=4096, ring_rows=4096)),
 )
 
 
-def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int = 50, warmup: int = 5):
+def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int = 50, warmup: int = 5, only=None):
     """The other workloads of the scope table, one fused append + attention
     call each (one launch), L2 flushed before every timed call: median µs,
     algorithmic GB/s and its fraction of the copy peak."""
@@ -248,7 +248,9 @@ def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int =
 
     import workloads
     res = []
-    for name, gen, kw in CONFIGS:
+    for key, name, gen, kw in CONFIGS:
+        if only is not None and key != only:
+            continue
         w = getattr(workloads, gen)(seed=seed, device=device, **kw)
         cache = pkv.PagedKVCache(w.k, w.v, w.block_table, ring_rows=w.ring_rows, bucket=w.bucket)
         q, kn, vn, si = w.q[0], w.k_new[0], w.v_new[0], w.seq_info
@@ -277,7 +279,7 @@ def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int =
         ms = statistics.median([a.elapsed_time(b) for a, b in evs])
         nbytes, flops = workload_bytes_flops(w)
         gbs = nbytes / (ms * 1e-3) / 1e9
-        res.append({"workload": name, "us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+        res.append({"key": key, "workload": name, "us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
                     "frac_of_peak": round(gbs / peak, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2)})
         del w, cache, q, kn, vn, si, out
         torch.cuda.empty_cache()
@@ -479,6 +481,22 @@ def gpu_arm(args):
         torch.distributed.destroy_process_group()
 
 
+def config_only(key: str):
+    """One workload of the scope table, 3 + 3 calls, one JSON line (no
+    headline): the command the profiler summaries capture."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_decode_13_gb300 as pkv
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    peak, _ = load_peaks()
+    res = time_configs(pkv, device, lambda: scratch.fill_(1), torch.cuda.current_stream(), peak, seed=0, reps=3,
+                       warmup=3, only=key)
+    print(json.dumps(res[0]), flush=True)
+
+
 # ---------------------------------------------------------------- reference arm (CPU oracle)
 
 def reference_arm(args):
@@ -525,11 +543,15 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--config-only", choices=[c[0] for c in CONFIGS],
+                    help="time only this workload's call (3 warm-up + 3 timed calls; for profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         reference_arm(args)
+    elif args.config_only:
+        config_only(args.config_only)
     else:
         gpu_arm(args)
 
