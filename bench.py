@@ -291,9 +291,11 @@ def time_e2e(runner, steps: int, warmup: int, flush, stream):
     device -> host copy of the outputs, all inside the timed events."""
     import torch
     st = runner.step_bufs
-    host_in = [t.cpu().pin_memory() for t in st.q + st.k_new + st.v_new + [st.seq_info]]
-    dev_in = st.q + st.k_new + st.v_new + [st.seq_info]
-    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in st.out]
+    # the step's inputs (every layer's q, k_new, v_new and the segment table)
+    # and outputs each sit in one device buffer: one copy each way
+    host_in = [st.inputs.cpu().pin_memory()]
+    dev_in = [st.inputs]
+    host_out = [torch.empty(st.outputs.shape, dtype=st.outputs.dtype).pin_memory()]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     graph = runner.graph_for()
@@ -302,7 +304,7 @@ def time_e2e(runner, steps: int, warmup: int, flush, stream):
         for d, h in zip(dev_in, host_in):
             d.copy_(h, non_blocking=True)
         graph.replay()
-        for h, o in zip(host_out, st.out):
+        for h, o in zip(host_out, [st.outputs]):
             h.copy_(o, non_blocking=True)
 
     for _ in range(warmup):

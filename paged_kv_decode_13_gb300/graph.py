@@ -13,7 +13,7 @@ per runner grew device memory without bound in the page's measurement.
 from __future__ import annotations
 
 import math
-from typing import Dict, Optional, Tuple
+from typing import Dict, List, Optional, Tuple
 
 import torch
 
@@ -30,8 +30,27 @@ def shared_pool():
     return _SHARED_POOL
 
 
+def _carve(spec, device) -> Tuple[torch.Tensor, List[torch.Tensor]]:
+    """One zeroed uint8 buffer holding tensors of the given (shape, dtype)
+    back to back, each at a 16-byte offset; returns it and the typed views."""
+    sizes = [math.prod(shape) * torch.empty((), dtype=dt).element_size() for shape, dt in spec]
+    offs, total = [], 0
+    for n in sizes:
+        offs.append(total)
+        total += (n + 15) // 16 * 16
+    buf = torch.zeros(max(total, 16), dtype=torch.uint8, device=device)
+    views = [buf[o:o + n].view(dt).view(shape) for (shape, dt), o, n in zip(spec, offs, sizes)]
+    return buf, views
+
+
 class DecodeStep:
-    """Static buffers and launches of one decode step over all layers."""
+    """Static buffers and launches of one decode step over all layers.
+
+    Every input a step varies (per layer q, k_new, v_new; then the segment
+    table) lives in one device buffer, `inputs`, and every output (per layer
+    out, then lse) in another, `outputs`; the per-layer tensors are views of
+    them, so a step's host round trip is one copy each way.
+    """
 
     def __init__(self, cache: PagedKVCache, num_q_heads: int, rows: int = 1, num_segments: int = 1,
                  max_q_len: int = 1, max_kv: Optional[int] = None, scale: Optional[float] = None,
@@ -48,13 +67,17 @@ class DecodeStep:
         self.causal, self.window = causal, window
         self.fused, self.pdl, self.flags, self.num_splits = fused, pdl, flags, num_splits
         self.prefetch_next = prefetch_next
-        self.q = [torch.zeros(rows, num_q_heads, D, dtype=cache.dtype, device=dev) for _ in range(L)]
-        self.k_new = [torch.zeros(rows, Hkv, D, dtype=cache.dtype, device=dev) for _ in range(L)]
-        self.v_new = [torch.zeros(rows, Hkv, D, dtype=cache.dtype, device=dev) for _ in range(L)]
-        self.out = [torch.zeros(rows, num_q_heads, D, dtype=torch.float32, device=dev) for _ in range(L)]
-        self.lse = [torch.zeros(rows, num_q_heads, dtype=torch.float32, device=dev) for _ in range(L)] \
-            if with_lse else [None] * L
-        self.seq_info = torch.zeros(num_segments, 4, dtype=torch.int32, device=dev)
+        spec_in = ([((rows, num_q_heads, D), cache.dtype)] * L + [((rows, Hkv, D), cache.dtype)] * (2 * L)
+                   + [((num_segments, 4), torch.int32)])
+        self.inputs, views = _carve(spec_in, dev)
+        self.q, self.k_new, self.v_new = views[:L], views[L:2 * L], views[2 * L:3 * L]
+        self.seq_info = views[3 * L]
+        spec_out = [((rows, num_q_heads, D), torch.float32)] * L
+        if with_lse:
+            spec_out += [((rows, num_q_heads), torch.float32)] * L
+        self.outputs, views = _carve(spec_out, dev)
+        self.out = views[:L]
+        self.lse = views[L:] if with_lse else [None] * L
         self.err = new_err_flags(dev)
         self.use_workspace = workspace
         self.ws = None
