@@ -387,6 +387,8 @@ def gpu_arm(args):
     if world > 1:
         torch.distributed.barrier()
     ms = statistics.mean(times)
+    qs = statistics.quantiles(times, n=10) if len(times) >= 2 else [times[0]] * 9
+    pct = {"p10": round(qs[0] * 1e3, 2), "p50": round(statistics.median(times) * 1e3, 2), "p90": round(qs[8] * 1e3, 2)}
     ms = reduce_max(ms, world, device)
     err = int(runner.step_bufs.err.item())
     if err:
@@ -453,6 +455,7 @@ def gpu_arm(args):
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": round(ms, 5),
+            "step_us_percentiles": pct,
             "higher_is_better": False,
             "scaling": "weak",
             "vs_baseline": None,
