@@ -159,3 +159,47 @@ def test_graph_pool_does_not_grow_across_requests(pkv):
         reserved.append(torch.cuda.memory_reserved())
     # After the first requests have warmed the allocator, memory stays level.
     assert reserved[-1] <= reserved[2], reserved
+
+
+def test_batched_left_padding_one_capture(pkv):
+    """A batched step over a left-padded batch: one capture, replayed while the
+    lengths grow and each sequence's first valid position changes (the graph
+    holds the descriptor's pointer, the values are read at run time)."""
+    from paged_kv_decode_13_gb300.graph import DecodeGraphRunner, DecodeStep
+    import workloads
+    S = 4
+    base = np.array([1500, 300, 1900, 40])
+    w = workloads.batched(S=S, max_len=2048, seed=5, lengths=base.tolist())
+    dev = torch.device("cuda")
+    fv = torch.zeros(S, dtype=torch.int32, device=dev)
+    cache = pkv.PagedKVCache([t.to(dev) for t in w.k], [t.to(dev) for t in w.v], w.block_table.to(dev),
+                             bucket=w.bucket, first_valid=fv)
+    step = DecodeStep(cache, w.q_heads, rows=S, num_segments=S, max_kv=w.bucket)
+    runner = DecodeGraphRunner(step)
+    kp = w.k[0].view(torch.int16).numpy().copy()
+    vp = w.v[0].view(torch.int16).numpy().copy()
+    bt = w.block_table.numpy()
+    gen = torch.Generator().manual_seed(3)
+    firsts = ([0, 0, 0, 0], [700, 299, 1950, 10], [1501, 0, 100, 41], [3, 150, 1901, 0])
+    for it, first in enumerate(firsts):
+        si = np.array([[s, 1, s, base[s] + it] for s in range(S)], np.int32)
+        q = torch.randn(S, w.q_heads, D, generator=gen).to(torch.bfloat16)
+        kn = (torch.randn(S, w.kv_heads, D, generator=gen) / math.sqrt(D)).to(torch.bfloat16)
+        vn = (torch.randn(S, w.kv_heads, D, generator=gen) / math.sqrt(D)).to(torch.bfloat16)
+        step.seq_info.copy_(torch.from_numpy(si))
+        step.q[0].copy_(q)
+        step.k_new[0].copy_(kn)
+        step.v_new[0].copy_(vn)
+        fv.copy_(torch.tensor(first, dtype=torch.int32))
+        runner.step()
+        torch.cuda.synchronize()
+        assert int(step.err.item()) == 0
+        assert O.append(kp, vp, bt, si, kn.view(torch.int16).numpy(), vn.view(torch.int16).numpy()) == 0
+        kpf = torch.from_numpy(kp).view(torch.bfloat16).double().numpy()
+        vpf = torch.from_numpy(vp).view(torch.bfloat16).double().numpy()
+        ref, _, e = O.attend(q.double().numpy(), kpf, vpf, bt, si, step.scale,
+                             first_valid=np.array(first, np.int32))
+        assert e == 0
+        diff = float(np.abs(U.f64(step.out[0]) - ref).max())
+        assert diff <= 2e-3, (it, diff)
+    assert runner.captures == 1
