@@ -169,7 +169,9 @@ int pkv_append(const pkv_cache *cache, int32_t layer,
  *   causal:     [lo, p + 1),        lo = max(0, p - window + 1) if window > 0 else 0
  *   non-causal: [lo, kv_end),       lo = max(0, kv_end - window) if window > 0 else 0
  * (bottom-right causal alignment, [tiny-llm kv_cache.py] causal_kwargs; for
- * q_len = 1 both are the same).  out[row][h][:] = softmax(softmax_scale *
+ * q_len = 1 both are the same).  With cache->first_valid set and
+ * f = max(first_valid[col], 0): a row with p < f sees key p alone, any other
+ * row has lo raised to at least f.  out[row][h][:] = softmax(softmax_scale *
  * q.k) weighted sum of V, in fp32; lse[row][h] = natural-log sum of
  * exp(softmax_scale * q.k) (may be NULL).  Rows no segment covers, and rows of
  * invalid segments, get out = 0 and lse = -inf.  Keys at or past kv_end and
