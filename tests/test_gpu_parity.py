@@ -296,11 +296,11 @@ def test_split_count_does_not_change_result(pkv, num_splits):
 
 @pytest.mark.parametrize("q_heads,max_q,flags", [(64, 16, 0), (64, 8, 0), (32, 8, 0), (16, 8, 0), (64, 16, 1)])
 @pytest.mark.parametrize("num_splits", [1, 3])
-def test_long_ranges_per_cta_rolling_warm_up(pkv, q_heads, max_q, flags, num_splits):
+def test_long_ranges_per_cta(pkv, q_heads, max_q, flags, num_splits):
     # one or three CTAs per range of 2000..5000 keys: each key group copies
-    # far more pages than its stages and the warm-up distance hold, so the
-    # rolling L2 warm-up runs through several page-id windows (every row
-    # class of the general kernel; flags 1: the CUDA-core kernel)
+    # far more pages than its stages and its L2 warm-up hold, through several
+    # page-id windows, and the last pass of a 4-page loop may hold 1..4 pages
+    # (every row class of the general kernel; flags 1: the CUDA-core kernel)
     w = U.nan_tails(workloads.spec_verify(S=4, max_q=max_q, len_lo=2000, len_hi=5000, seed=70 + q_heads + max_q,
                                           q_heads=q_heads, kv_heads=8))
     out, lse, err, cache = run(pkv, w, num_splits=num_splits, max_kv=5000, flags=flags)
