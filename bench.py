@@ -131,17 +131,25 @@ def reduce_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def bench_config(world: int) -> dict:
+    """The workload both arms report on."""
+    return {"workload": WORKLOAD, "kv_len": HEADLINE_LEN, "bucket": 8192, "layers": LAYERS, "q_heads": HQ,
+            "kv_heads": HKV, "head_dim": D,
+            "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+            "parallelism": f"replicas x{world} (one sequence per GPU)"}
+
+
 # ---------------------------------------------------------------- GPU arm
 
-def make_runner(pkv, L: int, seed: int, device):
+def make_runner(pkv, L: int, seed: int, device, advance: bool = False, bucket: int = 0):
     import torch
 
     import workloads
     from paged_kv_decode_13_gb300.graph import DecodeGraphRunner, DecodeStep
-    bucket = pkv.bucket_for(L)
+    bucket = bucket or pkv.bucket_for(L)
     w = workloads.sensenova(L, bucket, num_layers=LAYERS, seed=seed, device=device)
     cache = pkv.PagedKVCache(w.k, w.v, w.block_table, bucket=bucket)
-    step = DecodeStep(cache, HQ)
+    step = DecodeStep(cache, HQ, advance=advance)
     for layer in range(LAYERS):
         step.q[layer].copy_(w.q[layer])
         step.k_new[layer].copy_(w.k_new[layer])
@@ -286,26 +294,31 @@ def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int =
     return res
 
 
-def time_e2e(runner, steps: int, warmup: int, flush, stream):
-    """Per step: pinned host -> device copy of the step's inputs, graph replay,
-    device -> host copy of the outputs, all inside the timed events."""
+def time_e2e(pkv, steps: int, warmup: int, flush, stream, seed: int, device):
+    """End to end through the public API with host buffers.  Per step: one
+    pinned host -> device copy of the step's rows (every layer's q, k_new and
+    v_new), one replay of the captured step, which appends, attends and then
+    advances kv_end on the device (so the segment table is written by the
+    host once, before the first step), and one device -> host copy of every
+    layer's output, all inside the timed events.  The lengths start
+    warmup + steps - 1 below the headline length, so the last timed step
+    runs at it.  Returns the step times, the bytes copied each way per step
+    and the first and last KV length timed."""
     import torch
+    first = HEADLINE_LEN - (warmup + steps) + 1
+    runner, w = make_runner(pkv, first, seed, device, advance=True, bucket=pkv.bucket_for(HEADLINE_LEN))
+    del w
     st = runner.step_bufs
-    # the step's inputs (every layer's q, k_new, v_new and the segment table)
-    # and outputs each sit in one device buffer: one copy each way
-    host_in = [st.inputs.cpu().pin_memory()]
-    dev_in = [st.inputs]
-    host_out = [torch.empty(st.outputs.shape, dtype=st.outputs.dtype).pin_memory()]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    host_in = st.step_inputs.cpu().pin_memory()
+    host_out = torch.empty(st.outputs.shape, dtype=st.outputs.dtype).pin_memory()
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size()
     graph = runner.graph_for()
 
     def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
+        st.step_inputs.copy_(host_in, non_blocking=True)
         graph.replay()
-        for h, o in zip(host_out, [st.outputs]):
-            h.copy_(o, non_blocking=True)
+        host_out.copy_(st.outputs, non_blocking=True)
 
     for _ in range(warmup):
         flush()
@@ -318,7 +331,12 @@ def time_e2e(runner, steps: int, warmup: int, flush, stream):
         one()
         b.record(stream)
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in evs], h2d, d2h
+    if int(st.err.item()):
+        raise RuntimeError(f"e2e: device error flags {int(st.err.item()):#x}")
+    last = int(st.seq_info[0, 3].item()) - 1
+    assert last == HEADLINE_LEN, last
+    del runner
+    return [a.elapsed_time(b) for a, b in evs], h2d, d2h, first + warmup, last
 
 
 def oracle_layer_seconds(q, k, v, L: int, kv_heads: int = HKV) -> float:
@@ -438,7 +456,8 @@ def gpu_arm(args):
     achieved = bytes_layer / (per_launch_ms * 1e-3) / 1e9
     step_gbs = bytes_layer * LAYERS / (ms * 1e-3) / 1e9
 
-    e2e_times, h2d, d2h = time_e2e(runner, max(args.steps // 4, 10), args.warmup, flush, stream)
+    e2e_steps = min(max(args.steps // 4, 10), 200)
+    e2e_times, h2d, d2h, e2e_lo, e2e_hi = time_e2e(pkv, e2e_steps, args.warmup, flush, stream, rank, device)
     e2e_ms = reduce_max(statistics.mean(e2e_times), world, device)
 
     # CPU oracle baseline on a bounded sample of the same step's layers.
@@ -505,10 +524,7 @@ def gpu_arm(args):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic (seeded torch normal draws; q ~ N(0,1), K/V ~ N(0,1)/sqrt(128))",
-            "config": {"workload": WORKLOAD, "kv_len": HEADLINE_LEN, "bucket": pkv.bucket_for(HEADLINE_LEN),
-                       "layers": LAYERS, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
-                       "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
-                       "parallelism": f"replicas x{world} (one sequence per GPU)"},
+            "config": bench_config(world),
             "hbm_gbs": round(step_gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -520,7 +536,10 @@ def gpu_arm(args):
             "seq_clone": clone,
             "by_config": by_config,
             "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "µs/step", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "kv_len": f"{e2e_lo}..{e2e_hi}, advanced on the device by the captured step",
+                    "copies": "per step one pinned H2D of every layer's q, k_new, v_new and one D2H of every "
+                              "layer's output; the segment table is written once, before the first step"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -550,37 +569,70 @@ def config_only(key: str):
 # ---------------------------------------------------------------- reference arm (CPU oracle)
 
 def reference_arm(args):
+    """The oracle as it stands on whole steps of the headline workload: per
+    step, for each of the 42 layers, the oracle's append of the step's row
+    and its attention over all 8 kv heads at KV length 8192, on one host
+    thread.  Nothing is sampled or scaled; if the requested steps would take
+    more than a few minutes the step count is cut (never the work per step)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    import numpy as np
     import torch
 
     import workloads
     from oracle import oracle as orc
     orc.build()
-    bucket = 8192
-    w = workloads.sensenova(HEADLINE_LEN, bucket, num_layers=2, seed=0, device="cpu")
-    # Size each step's sample so the whole run stays within about two minutes.
-    budget = 120.0 / max(args.steps + args.warmup, 1)
-    m = 8 if budget >= 0.3 else 4 if budget >= 0.15 else 2 if budget >= 0.06 else 1
-    for i in range(args.warmup):
-        oracle_layer_seconds(w.q[i % 2], w.k[i % 2], w.v[i % 2], HEADLINE_LEN, m)
-    per = []
-    for i in range(args.steps):
-        t = oracle_layer_seconds(w.q[i % 2], w.k[i % 2], w.v[i % 2], HEADLINE_LEN, m)
-        per.append(t * (HKV / m) * LAYERS * 1e6)
+    torch.set_num_threads(max(1, min(8, os.cpu_count() or 1)))
+    w = workloads.sensenova(HEADLINE_LEN, HEADLINE_LEN, num_layers=LAYERS, seed=0, device="cpu")
+    si = w.seq_info.numpy()
+    bt = w.block_table.numpy()
+    scale = 1 / math.sqrt(D)
+    layers = []
+    for i in range(LAYERS):
+        kb = w.k[i].view(torch.int16).numpy().copy()
+        vb = w.v[i].view(torch.int16).numpy().copy()
+        kn = w.k_new[i].view(torch.int16).numpy()
+        vn = w.v_new[i].view(torch.int16).numpy()
+        assert orc.append(kb, vb, bt, si, kn, vn) == 0   # the pools the attention reads hold the step's row
+        layers.append((kb, vb, kn, vn, w.q[i].double().numpy(),
+                       torch.from_numpy(kb).view(torch.bfloat16).double().numpy(),
+                       torch.from_numpy(vb).view(torch.bfloat16).double().numpy()))
+    del w
+
+    def one_step() -> float:
+        t = 0.0
+        for kb, vb, kn, vn, q, kd, vd in layers:
+            t0 = time.perf_counter()
+            orc.append(kb, vb, bt, si, kn, vn)
+            orc.attend(q, kd, vd, bt, si, scale)
+            t += time.perf_counter() - t0
+        return t
+
+    budget_s = 240.0
+    start = time.perf_counter()
+    first = one_step()
+    for _ in range(args.warmup - 1):
+        one_step()
+    left = budget_s - (time.perf_counter() - start)
+    steps = max(1, min(args.steps, int(left / max(first, 1e-6))))
+    per = [one_step() * 1e6 for _ in range(steps)]
     us = statistics.mean(per)
-    sample = (f"each step: {m} of the 8 kv heads (with their query heads) of one layer at KV length "
-              f"{HEADLINE_LEN} through the fp64 C oracle (one thread), scaled to 8 kv heads x 42 layers")
+    sample = (f"whole steps: per step {LAYERS} layers x (the oracle's one-row append + its fp64 attention over all "
+              f"{HKV} kv heads at KV length {HEADLINE_LEN}), one host thread, C oracle built -O2; "
+              f"{steps} timed steps after {args.warmup} warm-up")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "µs/step", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "kv_len": HEADLINE_LEN, "bucket": bucket},
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch normal draws; "
+        "q ~ N(0,1), K/V ~ N(0,1)/sqrt(128))",
+        "config": bench_config(world),
         "cpu_baseline": {"value": round(us, 1), "unit": "µs/step", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(us, 1), "unit": "µs/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if steps != args.steps:
+        line["steps_requested"] = args.steps
     print(json.dumps(line), flush=True)
 
 

@@ -254,13 +254,22 @@ int64_t pkv_attend_workspace_bytes(const pkv_cache *cache, int32_t num_q_heads,
  * pkv_append_attend with the split-merge workspace taken from a fixed 8 MiB
  * scratch array in the library's device memory instead of the caller: no
  * allocation, no workspace argument.  The pages have no counterpart of this
- * call; it exists for callers that may not allocate (the scratch is a
- * file-scope device array, zero at load, left zeroed by every call).  A
- * launch whose merge would need more than 8 MiB (see
- * pkv_attend_workspace_bytes) or more than 4096 (segment, kv head) ranges is
- * rejected with PKV_ECAPACITY before anything runs.  The scratch is shared by every call on a device, so calls must not
- * run concurrently (one stream, or serialised).  Otherwise the same
- * arguments, results and errors as pkv_append_attend.
+ * call.  It serves callers that may not allocate device memory at the point
+ * of the call: an allocator-free runtime, a custom-op shim that owns no
+ * memory pool, or code running while an allocator must not be touched.  The
+ * scratch is a file-scope __device__ array (every device that loads the
+ * library holds it until the process exits), zero at load; the arrival
+ * counters live in an array of their own that every call leaves at zero.
+ * Its device address is looked up with cudaGetSymbolAddress on every call
+ * (a host-side query, so a new context after cudaDeviceReset is picked up);
+ * the first call on a device also loads the library's module there, so make
+ * it before any stream capture.  A launch whose merge would need more than
+ * 8 MiB (see pkv_attend_workspace_bytes) or more than 4096 (segment, kv
+ * head, row tile) ranges is rejected with PKV_ECAPACITY before anything
+ * runs; a failed lookup returns PKV_ECUDA.  The scratch is shared by every
+ * call on a device and keeps the last call's partials, so calls that overlap
+ * on the GPU race: issue them on one stream, or serialise them.  Otherwise
+ * the same arguments, results and errors as pkv_append_attend.
  */
 int pkv_append_attend_noalloc(const pkv_cache *cache, int32_t layer,
                               const void *q, const void *k_new, const void *v_new,

@@ -414,29 +414,19 @@ constexpr int kStaticUnits = 4096;
 static __device__ __align__(256) unsigned char g_split_scratch[kStaticScratchBytes];
 static __device__ __align__(256) int g_split_counters[kStaticUnits];
 
-// Device addresses of g_split_scratch and g_split_counters on the current
-// device (looked up once per device).
+// Device addresses of g_split_scratch and g_split_counters in the current
+// context.  Looked up on every call: the lookup is a host-side query, and an
+// address cached from an earlier context (before a cudaDeviceReset, say)
+// would be stale.  The first lookup on a device loads the library's module.
 bool static_scratch(void **scratch, int **counters) {
-    static std::mutex mu;
-    static void *addr[64][2] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    void *a = nullptr, *b = nullptr;
+    if (cudaGetSymbolAddress(&a, g_split_scratch) != cudaSuccess ||
+        cudaGetSymbolAddress(&b, g_split_counters) != cudaSuccess || !a || !b) {
         cudaGetLastError();
         return false;
     }
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev][0]) {
-        void *a = nullptr, *b = nullptr;
-        if (cudaGetSymbolAddress(&a, g_split_scratch) != cudaSuccess ||
-            cudaGetSymbolAddress(&b, g_split_counters) != cudaSuccess) {
-            cudaGetLastError();
-            return false;
-        }
-        addr[dev][0] = a;
-        addr[dev][1] = b;
-    }
-    *scratch = addr[dev][0];
-    *counters = reinterpret_cast<int *>(addr[dev][1]);
+    *scratch = a;
+    *counters = reinterpret_cast<int *>(b);
     return true;
 }
 
@@ -522,8 +512,15 @@ int pkv_append_attend_noalloc(const pkv_cache *c, int32_t layer, const void *q, 
                               int32_t window, float *out, float *lse, uint32_t *err, uint32_t flags, void *stream) {
     const int64_t need = pkv_attend_workspace_bytes(c, Hq, S, max_q_len, max_kv, num_splits, flags);
     if (need < 0) return (int)need;
-    if (need > kStaticScratchBytes || (need > 0 && (long long)S * c->kv_heads > kStaticUnits))
-        return PKV_ECAPACITY;  // rejected before any launch
+    if (need > 0) {
+        // One arrival counter per (segment, kv head, row tile) range: the
+        // same count the kernel indexes them by.
+        Plan pl;
+        const int st = make_plan(c, Hq, S, max_q_len, max_kv, num_splits, flags, true, &pl);
+        if (st) return st;
+        if (need > kStaticScratchBytes || (long long)S * c->kv_heads * pl.row_tiles > kStaticUnits)
+            return PKV_ECAPACITY;  // rejected before any launch
+    }
     void *ws = nullptr;
     int *counters = nullptr;
     if (need > 0 && !static_scratch(&ws, &counters)) return PKV_ECUDA;

@@ -389,38 +389,86 @@ struct SimtWarp {
 
 // ---------------------------------------------------------------- rows no segment covers
 
-// One CTA zeroes every output row that no segment covers and flags rows that
-// two segments claim.  Segments with a negative q_start or non-positive q_len
-// cover nothing.
-static __device__ __noinline__ void zero_uncovered(const AttendParams &p, int *sFlags, int nthreads, int first_row) {
+// Output rows are checked in slices of one CTA's thread count: slice k
+// belongs to the CTA of linear index k (and k + grid size, k + 2 * grid
+// size, ...), so the work spreads over the grid.  Segments with a negative
+// q_start or non-positive q_len cover nothing.
+__device__ __forceinline__ long long grid_cta_index() {
+    return (long long)blockIdx.x + (long long)gridDim.x * ((long long)blockIdx.y + (long long)gridDim.y * blockIdx.z);
+}
+__device__ __forceinline__ long long grid_cta_count() {
+    return (long long)gridDim.x * gridDim.y * gridDim.z;
+}
+__device__ __forceinline__ int coverage_slices(const AttendParams &p, int nthreads) {
+    return (p.total_rows + nthreads - 1) / nthreads;
+}
+
+// Count, for each row of the slice starting at `base`, the segments that
+// cover it: the threads take the segments in turn (one segment table read
+// per thread and pass, whatever the row count) and add one per covered row
+// of the slice in shared memory.  Leaves sCov[t] = 1 (no segment) | 2 (more
+// than one) for row base + t and returns whether any flag is set.  Every
+// thread of the CTA calls it.
+static __device__ __noinline__ int coverage_scan(const AttendParams &p, int *sCov, int base, int nthreads) {
     const int tid = threadIdx.x;
+    sCov[tid] = 0;
+    __syncthreads();
+    const long long hi_row = min((long long)base + nthreads, (long long)p.total_rows);
     #pragma unroll 1
-    for (int base = first_row; base < p.total_rows; base += nthreads) {
-        const int t = base + tid;
-        int cnt = 0;
-        if (t < p.total_rows) {
-            #pragma unroll 1
-            for (int s = 0; s < p.S; ++s) {
-                const Segment g = load_segment(p.seq_info, s);
-                if (g.q0 >= 0 && g.ql > 0 && t >= g.q0 && (long long)t < (long long)g.q0 + g.ql) ++cnt;
-            }
-            if (cnt > 1) atomicOr(p.err, PKV_ERR_OVERLAP);
-        }
-        sFlags[tid] = (t < p.total_rows && cnt == 0);
-        __syncthreads();
-        const int n = min(nthreads, p.total_rows - base);
-        const int per_row = p.Hq * p.D;
+    for (int s = tid; s < p.S; s += nthreads) {
+        const Segment g = load_segment(p.seq_info, s);
+        if (g.q0 < 0 || g.ql <= 0) continue;
+        const long long a = max((long long)g.q0, (long long)base);
+        const long long b = min((long long)g.q0 + g.ql, hi_row);
         #pragma unroll 1
-        for (int r = 0; r < n; ++r) {
-            if (!sFlags[r]) continue;
-            const long long t2 = base + r;
+        for (long long r = a; r < b; ++r) atomicAdd(sCov + (r - base), 1);
+    }
+    __syncthreads();
+    const int cnt = sCov[tid];
+    const int f = (long long)base + tid < hi_row ? ((cnt == 0 ? 1 : 0) | (cnt > 1 ? 2 : 0)) : 0;
+    __syncthreads();
+    sCov[tid] = f;
+    return __syncthreads_or(f != 0);
+}
+
+// After the dependency wait: zero the rows of the slice at `base` that no
+// segment covers (out = 0, lse = -inf) and report rows two segments claim.
+static __device__ __noinline__ void coverage_fix(const AttendParams &p, const int *sCov, int base, int nthreads) {
+    const int tid = threadIdx.x;
+    const int n = min(nthreads, p.total_rows - base), per_row = p.Hq * p.D;
+    if (tid < n && (sCov[tid] & 2)) atomicOr(p.err, PKV_ERR_OVERLAP);
+    #pragma unroll 1
+    for (int r = 0; r < n; ++r) {
+        if (!(sCov[r] & 1)) continue;
+        const long long t = (long long)base + r;
+        #pragma unroll 1
+        for (int e = tid; e < per_row; e += nthreads) p.out[t * per_row + e] = 0.f;
+        if (p.lse)
             #pragma unroll 1
-            for (int e = tid; e < per_row; e += nthreads) p.out[t2 * per_row + e] = 0.f;
-            if (p.lse)
-                #pragma unroll 1
-                for (int e = tid; e < p.Hq; e += nthreads) p.lse[t2 * p.Hq + e] = -CUDART_INF_F;
-        }
-        __syncthreads();
+            for (int e = tid; e < p.Hq; e += nthreads) p.lse[t * p.Hq + e] = -CUDART_INF_F;
+    }
+}
+
+// Before the dependency wait (the segment table is not written by the
+// previous kernel): a CTA that owns a slice scans its first one.  Returns
+// whether that slice needs fixing.
+static __device__ __forceinline__ int coverage_begin(const AttendParams &p, int *sCov, bool cov_cta, int nthreads) {
+    return cov_cta ? coverage_scan(p, sCov, (int)(grid_cta_index() * nthreads), nthreads) : 0;
+}
+
+// After the dependency wait, every thread of a CTA that owns a slice: fix
+// the first slice, then scan and fix any further ones (grids with fewer CTAs
+// than slices).
+static __device__ __noinline__ void apply_coverage(const AttendParams &p, int *sCov, int cov_any, int nthreads) {
+    const long long lin = grid_cta_index(), nct = grid_cta_count();
+    const int slices = coverage_slices(p, nthreads);
+    if (lin >= slices) return;
+    if (cov_any) coverage_fix(p, sCov, (int)(lin * nthreads), nthreads);
+    #pragma unroll 1
+    for (long long k = lin + nct; k < slices; k += nct) {
+        const int base = (int)(k * nthreads);
+        __syncthreads();  // the previous slice's flags are no longer read
+        if (coverage_scan(p, sCov, base, nthreads)) coverage_fix(p, sCov, base, nthreads);
     }
 }
 
@@ -444,28 +492,6 @@ static __device__ __noinline__ void zero_segment_rows(const AttendParams &p, con
 // First CTA, after the dependency wait: zero the rows the pre-wait scan found
 // uncovered among the first `nthreads` rows, flag double coverage, then scan
 // and zero any rows past them.
-static __device__ __noinline__ void apply_coverage(const AttendParams &p, int *sCov, int cov_any, int nthreads) {
-    const int tid = threadIdx.x;
-    if (cov_any) {
-        const int n = min(nthreads, p.total_rows), per_row = p.Hq * p.D;
-        #pragma unroll 1
-        for (int r = 0; r < n; ++r) {
-            const int f = sCov[r];
-            if ((f & 2) && tid == 0) atomicOr(p.err, PKV_ERR_OVERLAP);
-            if (!(f & 1)) continue;
-            #pragma unroll 1
-            for (int e = tid; e < per_row; e += nthreads) p.out[(long long)r * per_row + e] = 0.f;
-            if (p.lse)
-                #pragma unroll 1
-                for (int e = tid; e < p.Hq; e += nthreads) p.lse[(long long)r * p.Hq + e] = -CUDART_INF_F;
-        }
-    }
-    if (p.total_rows > nthreads) {
-        __syncthreads();
-        zero_uncovered(p, sCov, nthreads, nthreads);
-    }
-}
-
 // ---------------------------------------------------------------- the kernel
 
 template <class C>
@@ -507,30 +533,16 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     const int rank = blockIdx.x, ncta = gridDim.x;
     const int g = blockIdx.y / p.row_tiles, rt = blockIdx.y - g * p.row_tiles;
     const int s = blockIdx.z;
-    const bool first_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+    // CTAs that own a slice of output rows for the coverage check.
+    const bool cov_cta = grid_cta_index() < coverage_slices(p, NT);
 
-    // Rows no segment covers: the first CTA scans the first NT rows before the
-    // dependency wait (the segment table is not written by the previous
-    // kernel) and zeroes them after it.
-    int cov_any = 0;
-    if (first_cta) {
-        int f = 0;
-        if (tid < p.total_rows) {
-            int cnt = 0;
-            #pragma unroll 1
-            for (int s2 = 0; s2 < p.S; ++s2) {
-                const Segment o = load_segment(p.seq_info, s2);
-                if (o.q0 >= 0 && o.ql > 0 && tid >= o.q0 && (long long)tid < (long long)o.q0 + o.ql) ++cnt;
-            }
-            f = (cnt == 0 ? 1 : 0) | (cnt > 1 ? 2 : 0);
-        }
-        sCov[tid] = f;
-        cov_any = __syncthreads_or(f != 0);
-    }
+    // Rows no segment covers: counted before the dependency wait (the
+    // segment table is not written by the previous kernel), zeroed after it.
+    const int cov_any = coverage_begin(p, sCov, cov_cta, NT);
     if (p.S == 0) {  // nothing but rows no segment covers
         pdl_wait();
         pdl_trigger();
-        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+        if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
     }
 
@@ -547,7 +559,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
             if (tid == 0) atomicOr(p.err, fault);
             zero_segment_rows(p, sg, g, NT);
         }
-        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+        if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
     }
     if (C::kPush && ncta > 1)  // announce this CTA to the cluster; waited on before any remote store
@@ -734,7 +746,7 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
         }
     }
 
-    if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+    if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
 
     // Query rows of this tile (all loads issued before any store) and their key bounds.
     {

@@ -123,28 +123,15 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     const int rank = blockIdx.x, ncta = gridDim.x;
     const int g = blockIdx.y;  // one CTA row per kv head: the whole group fits the 8 rows
     const int s = blockIdx.z;
-    const bool first_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+    // CTAs that own a slice of output rows for the coverage check.
+    const bool cov_cta = grid_cta_index() < coverage_slices(p, NT);
 
-    // Rows no segment covers: scanned before the dependency wait, zeroed after.
-    int cov_any = 0;
-    if (first_cta) {
-        int f = 0;
-        if (tid < p.total_rows) {
-            int cnt = 0;
-            #pragma unroll 1
-            for (int s2 = 0; s2 < p.S; ++s2) {
-                const Segment o = load_segment(p.seq_info, s2);
-                if (o.q0 >= 0 && o.ql > 0 && tid >= o.q0 && (long long)tid < (long long)o.q0 + o.ql) ++cnt;
-            }
-            f = (cnt == 0 ? 1 : 0) | (cnt > 1 ? 2 : 0);
-        }
-        sCov[tid] = f;
-        cov_any = __syncthreads_or(f != 0);
-    }
+    // Rows no segment covers: counted before the dependency wait, zeroed after.
+    const int cov_any = coverage_begin(p, sCov, cov_cta, NT);
     if (p.S == 0) {
         pdl_wait();
         pdl_trigger();
-        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+        if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
     }
 
@@ -160,7 +147,7 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
             if (tid == 0) atomicOr(p.err, fault);
             zero_segment_rows(p, sg, g, NT);
         }
-        if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+        if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
     }
     const int kend = sg.kend;
@@ -181,8 +168,17 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     const int cb0 = pb_begin + rank * bps;
     const int nb = rank < active ? min(cb0 + bps, pb_end) - cb0 : 0;
     const int n_mine = nb > kw ? (nb - kw + KW - 1) / KW : 0;
-    if (solo && rank > 0 && !first_cta) return;  // nothing to read or write
-    if (gm && rank >= active && !first_cta) return;  // no pages; only the active CTAs take part in the merge
+    // A CTA with nothing to read or write (a solo range's other ranks; with
+    // the global merge, ranks past the active ones) only does its share of
+    // the coverage check.
+    if ((solo && rank > 0) || (gm && rank >= active)) {
+        if (cov_cta) {
+            pdl_wait();
+            pdl_trigger();
+            apply_coverage(p, sCov, cov_any, NT);
+        }
+        return;
+    }
     if (ncl > 1 && !gm)  // announce this CTA to the cluster; waited on before any remote store
         asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
 
@@ -413,7 +409,7 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         if (n < rows_unit)
             row_key_bounds(new_start + n / p.G, kend, p.causal, p.window, first, lo_r[e], hi_r[e]);
     }
-    if (first_cta) apply_coverage(p, sCov, cov_any, NT);
+    if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
     #pragma unroll 1
     for (; issued < NST && issued < n_mine; ++issued) issue(issued);
 

@@ -19,6 +19,7 @@ import torch
 
 from . import _lib
 from .api import PagedKVCache, append, append_attend, attend_varlen, new_err_flags, new_workspace
+from .api import advance as advance_lengths
 
 _SHARED_POOL = None
 
@@ -50,13 +51,19 @@ class DecodeStep:
     table) lives in one device buffer, `inputs`, and every output (per layer
     out, then lse) in another, `outputs`; the per-layer tensors are views of
     them, so a step's host round trip is one copy each way.
+
+    With advance=True the step ends with `kv_end += q_len` for every segment
+    on the device (tiny-llm kv_cache.py, SlotKVCache.end_step), so a replay
+    leaves the segment table ready for the next step and the host writes it
+    only once: per step it copies q, k_new and v_new (`step_inputs`) and
+    keeps its own copy of the lengths in step (advance_host).
     """
 
     def __init__(self, cache: PagedKVCache, num_q_heads: int, rows: int = 1, num_segments: int = 1,
                  max_q_len: int = 1, max_kv: Optional[int] = None, scale: Optional[float] = None,
                  causal: bool = False, window: int = 0, fused: bool = True, pdl: bool = True,
                  flags: int = 0, num_splits: int = 0, with_lse: bool = False, prefetch_next: bool = True,
-                 workspace: bool = False):
+                 workspace: bool = False, advance: bool = False):
         dev = cache.k[0].device
         L, Hkv, D = cache.num_layers, cache.kv_heads, cache.head_dim
         self.cache = cache
@@ -72,6 +79,10 @@ class DecodeStep:
         self.inputs, views = _carve(spec_in, dev)
         self.q, self.k_new, self.v_new = views[:L], views[L:2 * L], views[2 * L:3 * L]
         self.seq_info = views[3 * L]
+        # the per-step part of `inputs` (q, k_new, v_new of every layer): the
+        # segment table sits after it
+        self.step_inputs = self.inputs[:self.seq_info.data_ptr() - self.inputs.data_ptr()]
+        self.advance = advance
         spec_out = [((rows, num_q_heads, D), torch.float32)] * L
         if with_lse:
             spec_out += [((rows, num_q_heads), torch.float32)] * L
@@ -91,10 +102,12 @@ class DecodeStep:
                                     self.max_kv, self.num_splits, self.flags)
 
     def launch_count(self) -> int:
-        return self.cache.num_layers * (1 if self.fused else 2)
+        return self.cache.num_layers * (1 if self.fused else 2) + (1 if self.advance else 0)
 
-    def run(self, stream=None) -> None:
-        """Enqueue every layer's append + attention on the current stream."""
+    def run(self, stream=None, advance: Optional[bool] = None) -> None:
+        """Enqueue every layer's append + attention on the current stream,
+        then (advance=True, by default the step's setting) the on-device
+        length advance."""
         c = self.cache
         for layer in range(c.num_layers):
             flags = self.flags
@@ -113,6 +126,8 @@ class DecodeStep:
                 attend_varlen(c, layer, self.q[layer], self.seq_info, self.out[layer], self.err, self.max_q_len,
                               self.max_kv, self.scale, self.causal, self.window, lse=self.lse[layer],
                               num_splits=self.num_splits, flags=flags, stream=stream, workspace=self.ws)
+        if self.advance if advance is None else advance:
+            advance_lengths(self.seq_info, stream=stream)
 
 
 class DecodeGraphRunner:
@@ -124,15 +139,21 @@ class DecodeGraphRunner:
         self.captures = 0
 
     def _capture(self, key):
+        st = self.step_bufs
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
+            # Warm-up leaves the lengths alone (a warm-up that advanced them
+            # would move the step three tokens on); the advance kernel is
+            # warmed on a scratch row instead.
             for _ in range(3):
-                self.step_bufs.run()
+                st.run(advance=False)
+            if st.advance:
+                advance_lengths(torch.zeros(1, 4, dtype=torch.int32, device=st.seq_info.device))
         torch.cuda.current_stream().wait_stream(side)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, pool=shared_pool()):
-            self.step_bufs.run()
+            st.run()
         self.captures += 1
         self._graphs[key] = graph
         return graph

@@ -54,10 +54,9 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def compact(w, layer: int, segs, k_pool: torch.Tensor, v_pool: torch.Tensor):
-    """Pool, table and segment table holding only the pages `segs` reach, so
-    the oracle runs on a small input.  Block ids are relabelled; the gather
-    through the table (and hence the result) is unchanged."""
+def compact_ids(w, segs, num_blocks: int):
+    """Pool page ids the segments `segs` reach, in order, and per segment its
+    relabelled table row (-1 for a page the table does not list)."""
     bt = w.block_table.cpu().numpy()
     si = w.seq_info.cpu().numpy()
     ids, rows = [], []
@@ -68,12 +67,21 @@ def compact(w, layer: int, segs, k_pool: torch.Tensor, v_pool: torch.Tensor):
         row = []
         for pg in range(npg):
             b = int(bt[col, pg])
-            if 0 <= b < k_pool.shape[0]:
+            if 0 <= b < num_blocks:
                 row.append(len(ids))
                 ids.append(b)
             else:          # a page the table does not list (e.g. a ring not yet grown to it)
                 row.append(-1)
         rows.append(row)
+    return ids, rows
+
+
+def compact(w, layer: int, segs, k_pool: torch.Tensor, v_pool: torch.Tensor):
+    """Pool, table and segment table holding only the pages `segs` reach, so
+    the oracle runs on a small input.  Block ids are relabelled; the gather
+    through the table (and hence the result) is unchanged."""
+    si = w.seq_info.cpu().numpy()
+    ids, rows = compact_ids(w, segs, k_pool.shape[0])
     mb = max(len(r) for r in rows) if rows else 1
     new_bt = np.full((len(segs), max(mb, 1)), -1, np.int32)
     for i, r in enumerate(rows):

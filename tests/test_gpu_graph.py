@@ -203,3 +203,47 @@ def test_batched_left_padding_one_capture(pkv):
         diff = float(np.abs(U.f64(step.out[0]) - ref).max())
         assert diff <= 2e-3, (it, diff)
     assert runner.captures == 1
+
+
+def test_replays_advance_lengths_on_the_device(pkv):
+    """DecodeStep(advance=True): the segment table is written once by the host;
+    each replay appends and attends at the current length and then moves
+    kv_end on by q_len on the device (tiny-llm kv_cache.py, SlotKVCache.end_step).
+    N replays with only q / k_new / v_new copied in match N oracle steps on a
+    host mirror whose lengths the test advances itself, and the table reads
+    back kv_end + N."""
+    from paged_kv_decode_13_gb300.graph import DecodeGraphRunner, DecodeStep
+    layers, bucket, L0, N = 2, 1024, 990, 34    # crosses two page boundaries, ends at the bucket edge
+    gen = torch.Generator().manual_seed(11)
+    cache = pkv.PagedKVCache.allocate(layers, HKV, D, bucket)
+    host = [(torch.randn(t.shape, generator=gen) / math.sqrt(D)).to(torch.bfloat16) for t in cache.k + cache.v]
+    for t, h in zip(cache.k + cache.v, host):
+        t.copy_(h)
+    mirror = Mirror(host[:layers], host[layers:], torch.arange(bucket // 16, dtype=torch.int32)[None])
+    step = DecodeStep(cache, HQ, advance=True)
+    runner = DecodeGraphRunner(step)
+    assert step.launch_count() == layers + 1
+    step.seq_info.copy_(torch.tensor([[0, 1, 0, L0]], dtype=torch.int32))
+    for n in range(N):
+        qs = [torch.randn(1, HQ, D, generator=gen).to(torch.bfloat16) for _ in range(layers)]
+        ks = [(torch.randn(1, HKV, D, generator=gen) / math.sqrt(D)).to(torch.bfloat16) for _ in range(layers)]
+        vs = [(torch.randn(1, HKV, D, generator=gen) / math.sqrt(D)).to(torch.bfloat16) for _ in range(layers)]
+        # one host -> device copy of the step's rows; the segment table is not written
+        host_in = torch.cat([t.view(torch.uint8).reshape(-1) for t in qs + ks + vs])
+        assert host_in.numel() == step.step_inputs.numel()
+        step.step_inputs.copy_(host_in)
+        runner.step()
+        torch.cuda.synchronize()
+        si = np.array([[0, 1, 0, L0 + n]], np.int32)   # the host's own copy of the lengths
+        for layer in range(layers):
+            mirror.append(layer, si, ks[layer], vs[layer])
+            ref, _ = mirror.attend(layer, qs[layer], si, step.scale)
+            diff = float(np.abs(U.f64(step.out[layer]) - ref).max())
+            assert diff <= 2e-3, (n, layer, diff)
+    assert int(step.err.item()) == 0
+    assert step.seq_info.cpu().tolist() == [[0, 1, 0, L0 + N]]
+    assert runner.captures == 1
+    # the pools hold exactly the mirror's appended rows
+    for layer in range(layers):
+        assert U.pool_bytes(cache.k[layer]) == mirror.k[layer].tobytes()
+        assert U.pool_bytes(cache.v[layer]) == mirror.v[layer].tobytes()

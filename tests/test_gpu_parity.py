@@ -483,3 +483,40 @@ def test_load_prefix_and_write_back(pkv):
         assert torch.equal(ko, keys[layer][0]) and torch.equal(vo, vals[layer][0])
         flat = cache.k[layer].view(-1, H, D)
         assert torch.equal(flat[:S], keys[layer][0].transpose(0, 1))
+
+
+@pytest.mark.parametrize("q_heads,q_len", [(32, 1), (64, 2)])
+def test_thousands_of_segments_with_gaps(pkv, q_heads, q_len):
+    """2048 segments (the decode kernel at q_len 1, the general kernel at 2)
+    over an output with a gap row after every 16th segment: the check of rows
+    no segment covers is spread over many CTAs, the gaps come back zero with
+    lse = -inf, every covered row matches the oracle, and making two segments
+    claim one row sets the overlap bit."""
+    S = 2048
+    w = workloads.batched(S=S, max_len=48, seed=q_heads + q_len, q_heads=q_heads, kv_heads=8, min_len=q_len)
+    q0 = [s * q_len + s // 16 for s in range(S)]
+    rows = q0[-1] + q_len + 3
+    gen = torch.Generator().manual_seed(5)
+    w.q[0] = torch.randn(rows, q_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+    w.k_new[0] = (torch.randn(rows, 8, w.head_dim, generator=gen) / math.sqrt(w.head_dim)).to(torch.bfloat16)
+    w.v_new[0] = (torch.randn(rows, 8, w.head_dim, generator=gen) / math.sqrt(w.head_dim)).to(torch.bfloat16)
+    si = w.seq_info.clone()
+    si[:, 0] = torch.tensor(q0, dtype=torch.int32)
+    si[:, 1] = q_len
+    w.seq_info = si
+    w.causal, w.max_q_len = True, q_len
+    w = U.nan_tails(w)
+    out, lse, err, cache = run(pkv, w, max_kv=48)
+    assert err == 0
+    covered = set(U.rows_of(w, range(S)))
+    gaps = [t for t in range(rows) if t not in covered]
+    assert len(gaps) == S // 16 - 1 + 3
+    g = torch.tensor(gaps, device=out.device)
+    assert not out[g].abs().sum().item() and bool(torch.isinf(lse[g]).all())
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+    si2 = si.clone()
+    si2[1000, 0] = si2[999, 0]          # two segments claim the same rows
+    w.seq_info = si2
+    _, _, err, _ = run(pkv, w, max_kv=48)
+    assert err & pkv.ERR_OVERLAP

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import workloads
+from oracle import oracle as O
 from tests import gpu_util as U
 
 
@@ -88,3 +89,53 @@ def test_noalloc_oversize_launches_nothing(pkv):
                                   w.seq_info.to(dev), out, err, 1, 8192, w.scale, num_splits=64)
     torch.cuda.synchronize()
     assert bool((out == 4.0).all()) and int(err.item()) == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_batch_of_32_matches_oracle_over_two_steps(pkv):
+    """32 sequences of different lengths, four splits per (sequence, kv head)
+    range, so the library's scratch holds 256 ranges' partials and arrival
+    counters at once.  Both steps match the fp64 oracle (the second over the
+    pools the first appended to) and, bit for bit, the workspace call."""
+    rng = np.random.default_rng(41)
+    lengths = [int(x) for x in rng.integers(200, 3999, 32)]
+    lengths = [L - 1 if L % 16 == 0 else L for L in lengths]   # the second step stays in the last page
+    w = U.nan_tails(workloads.batched(S=32, max_len=4000, seed=41, lengths=lengths))
+    dev = torch.device("cuda")
+    caches = [U.device_cache(pkv, w), U.device_cache(pkv, w)]
+    splits = 4
+    ws = pkv.new_workspace(caches[0], w.q_heads, 32, 1, 4000, splits)
+    assert ws is not None and ws.numel() <= (8 << 20)
+    kp = w.k[0].view(torch.int16).numpy().copy()
+    vp = w.v[0].view(torch.int16).numpy().copy()
+    bt = w.block_table.numpy()
+    gen = torch.Generator().manual_seed(42)
+    for step in range(2):
+        si = w.seq_info.clone()
+        si[:, 3] += step
+        q = torch.randn(32, w.q_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+        kn = (torch.randn(32, w.kv_heads, w.head_dim, generator=gen) / math.sqrt(w.head_dim)).to(torch.bfloat16)
+        vn = (torch.randn(32, w.kv_heads, w.head_dim, generator=gen) / math.sqrt(w.head_dim)).to(torch.bfloat16)
+        res = []
+        for i, cache in enumerate(caches):
+            out = torch.zeros(32, w.q_heads, w.head_dim, device=dev)
+            lse = torch.zeros(32, w.q_heads, device=dev)
+            err = pkv.new_err_flags()
+            args = (cache, 0, q.to(dev), kn.to(dev), vn.to(dev), si.to(dev), out, err, 1, 4000, w.scale)
+            if i == 0:
+                pkv.append_attend(*args, lse=lse, num_splits=splits, workspace=ws)
+            else:
+                pkv.append_attend_noalloc(*args, lse=lse, num_splits=splits)
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0
+            res.append((out, lse))
+        assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+        sin = si.numpy()
+        assert O.append(kp, vp, bt, sin, kn.view(torch.int16).numpy(), vn.view(torch.int16).numpy()) == 0
+        assert U.pool_bytes(caches[1].k[0]) == kp.tobytes() and U.pool_bytes(caches[1].v[0]) == vp.tobytes()
+        ref, ref_lse, e = O.attend(q.double().numpy(), torch.from_numpy(kp).view(torch.bfloat16).double().numpy(),
+                                   torch.from_numpy(vp).view(torch.bfloat16).double().numpy(), bt, sin, w.scale)
+        assert e == 0
+        diff = float(np.abs(U.f64(res[1][0]) - ref).max())
+        assert diff <= U.TOL[torch.bfloat16], (step, diff)
+        assert float(np.abs(U.f64(res[1][1]) - ref_lse).max()) <= U.TOL[torch.bfloat16]

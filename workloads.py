@@ -132,10 +132,10 @@ def nan_fill_unused(w: Workload) -> None:
             continue
         span = w.ring_rows if w.ring_rows else kend
         span = min(span, bt.shape[1] * BLOCK)
-        for j in range(span):
-            b = int(bt[col, j // BLOCK])
-            if 0 <= b < w.num_blocks:
-                live[b * BLOCK + j % BLOCK] = True
+        j = torch.arange(max(span, 0), dtype=torch.long)
+        b = bt[col, j // BLOCK].long()
+        ok = (b >= 0) & (b < w.num_blocks)
+        live[(b * BLOCK + j % BLOCK)[ok]] = True
     dead = (~live).to(w.k[0].device)
     for t in w.k + w.v:
         flat = t.view(-1, t.shape[2], t.shape[3])
