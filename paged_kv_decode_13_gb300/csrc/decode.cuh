@@ -35,6 +35,9 @@ namespace pkv {
 
 // Key ranges of at most this many pages per compute warp run on one CTA.
 constexpr int kSoloPages = 3;
+// Lazy rescaling threshold of the online softmax (base-2 exponent): weights
+// stay at most 2^8, well inside fp32 and with bf16's relative precision.
+constexpr float kLazyLog2 = 8.f;
 
 template <int DP_, int KW_, int NST_>
 struct DecCfg {
@@ -484,28 +487,36 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         v[1] = (p0 >= lo_r[1] && p0 < hi_r[1]) ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
         v[2] = (p1 >= lo_r[0] && p1 < hi_r[0]) ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
         v[3] = (p1 >= lo_r[1] && p1 < hi_r[1]) ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
+        // Lazy running maximum: a row's reference max moves only when a score
+        // exceeds it by more than kLazyLog2, so the weights stay below
+        // 2^kLazyLog2 and the common page needs no cross-lane reduction and
+        // no rescale.  (m, l, acc) stay consistent with whatever reference
+        // the row holds, which is all the merges need.
         float mx0 = fmaxf(v[0], v[2]), mx1 = fmaxf(v[1], v[3]);
+        if (__any_sync(0xffffffffu, mx0 > m_r[0] + kLazyLog2 || mx1 > m_r[1] + kLazyLog2)) {
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-        }
-        const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
-        const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0, mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-        const float al0 = exp2f(m_r[0] - mu0), al1 = exp2f(m_r[1] - mu1);
-        m_r[0] = mn0;
-        m_r[1] = mn1;
-        const float p00 = exp2f(v[0] - mu0), p01 = exp2f(v[1] - mu1);
-        const float p10 = exp2f(v[2] - mu0), p11 = exp2f(v[3] - mu1);
-        l_r[0] = fmaf(l_r[0], al0, p00 + p10);
-        l_r[1] = fmaf(l_r[1], al1, p01 + p11);
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
+            const float al0 = mn0 == -CUDART_INF_F ? 1.f : exp2f(m_r[0] - mn0);
+            const float al1 = mn1 == -CUDART_INF_F ? 1.f : exp2f(m_r[1] - mn1);
+            m_r[0] = mn0;
+            m_r[1] = mn1;
+            l_r[0] *= al0;
+            l_r[1] *= al1;
 #pragma unroll
             for (int dt = 0; dt < KT; ++dt) {
                 acc[dt][0] *= al0; acc[dt][1] *= al1;
                 acc[dt][2] *= al0; acc[dt][3] *= al1;
             }
         }
+        const float mu0 = m_r[0] == -CUDART_INF_F ? 0.f : m_r[0], mu1 = m_r[1] == -CUDART_INF_F ? 0.f : m_r[1];
+        const float p00 = exp2f(v[0] - mu0), p01 = exp2f(v[1] - mu1);
+        const float p10 = exp2f(v[2] - mu0), p11 = exp2f(v[3] - mu1);
+        l_r[0] += p00 + p10;
+        l_r[1] += p01 + p11;
         // P^T as B fragments: transpose the (key x row) halves in registers.
         const unsigned b0 = movmatrix_trans(pack_bf16x2(p00, p01));
         const unsigned b1 = movmatrix_trans(pack_bf16x2(p10, p11));
