@@ -69,6 +69,7 @@ typedef enum pkv_dtype { PKV_BF16 = 0, PKV_F32 = 1 } pkv_dtype;
 #define PKV_FLAG_SIMT  (1u << 0)  /* bf16: use the CUDA-core kernel instead of the tensor-core one */
 #define PKV_FLAG_PDL   (1u << 1)  /* launch with programmatic dependent launch; see pkv_attend_varlen */
 #define PKV_FLAG_PREFETCH_NEXT (1u << 2)  /* warm L2 with layer + 1's pages; see pkv_attend_varlen */
+#define PKV_FLAG_MMA_SYNC (1u << 3)  /* bf16, head_dim 128, > 8 rows per kv head: mma.sync tile instead of tcgen05 */
 
 /*
  * One paged K/V cache: per layer, a K pool and a V pool, each

@@ -19,7 +19,7 @@ BF16, F32 = 0, 1
 # device error bits
 ERR_SEGMENT, ERR_CAPACITY, ERR_RING, ERR_BLOCK, ERR_QLEN, ERR_OVERLAP, ERR_TIMEOUT = 1, 2, 4, 8, 16, 32, 64
 # attention flags
-FLAG_SIMT, FLAG_PDL, FLAG_PREFETCH_NEXT = 1, 2, 4
+FLAG_SIMT, FLAG_PDL, FLAG_PREFETCH_NEXT, FLAG_MMA_SYNC = 1, 2, 4, 8
 BLOCK_SIZE = 16
 
 

@@ -94,7 +94,7 @@ AttnKernel pick(int variant, int dp, int rc) {
         case 2128: return pick_2_128(rc);
         case 2256: return pick_2_256(rc);
     }
-    return AttnKernel{nullptr, 0, 0, 0, 0, false};
+    return AttnKernel{nullptr, 0, 0, 0, 0, false, false};
 }
 
 // Largest cluster size <= want that the device can schedule for this kernel
@@ -157,11 +157,15 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
     // Groups of at most 8 rows take the decode kernel (rows as the MMA's N side).
     // Long buckets take the decode configuration with more warps (class 5).
     const long long max_pages0 = (max_kv + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE + 1;
+    // Wider bf16 groups with head_dim 128 take the tcgen05 tile (class 6)
+    // unless the caller asks for the mma.sync one.
+    const bool tc = variant == kMmaBf16 && rows_max > 8 && D == 128 && !(flags & PKV_FLAG_MMA_SYNC);
     const int rc = (variant == kMmaBf16 && rows_max <= 8) ? (max_pages0 > 256 ? 5 : 4)
+                   : tc ? 6
                    : rows_max <= 16 ? 0 : rows_max <= 32 ? 1 : rows_max <= 64 ? 2 : 3;
     pl->k = pick(variant, dp, rc);
     if (!pl->k.fn) return PKV_EUNSUPPORTED;
-    pl->gm = want_gm && rc >= 4;
+    pl->gm = want_gm && (rc == 4 || rc == 5);
     if (!pl->gm && num_splits > kMaxCluster) return PKV_EINVAL;
     pl->row_tiles = (int)((rows_max + pl->k.rows - 1) / pl->k.rows);
     if ((long long)c->kv_heads * pl->row_tiles > 65535) return PKV_EINVAL;
@@ -185,7 +189,7 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
         n = 1;
         while (n < want && n < kMaxCluster) n *= 2;
     }
-    if (rc >= 4 && num_splits == 0) {
+    if ((rc == 4 || rc == 5) && num_splits == 0) {
         // decode kernel: no more CTAs than keep each of their warps two pages
         long long cap = 1;
         while (cap * 2 <= max_pages / 8 && cap * 2 <= kMaxCluster) cap *= 2;
@@ -311,7 +315,7 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     AttendParams p;
     // bf16 page tiles come in one box when head_dim fills its padded width
     // exactly (128 or 256); otherwise, and for fp32, the 4-D view.
-    const bool page_box = c->dtype == PKV_BF16 && c->head_dim == pl.k.dp && c->head_dim > 64;
+    const bool page_box = c->dtype == PKV_BF16 && c->head_dim == pl.k.dp && c->head_dim > 64 && !pl.k.tc;
     auto encode = [&](CUtensorMap *m, const void *pool) {
         return page_box ? encode_pool_pages(m, pool, c) : encode_pool(m, pool, c);
     };

@@ -492,6 +492,151 @@ static __device__ __noinline__ void zero_segment_rows(const AttendParams &p, con
 // First CTA, after the dependency wait: zero the rows the pre-wait scan found
 // uncovered among the first `nthreads` rows, flag double coverage, then scan
 // and zero any rows past them.
+// ---------------------------------------------------------------- merge of a CTA's partial rows
+
+// Merge the key groups' partial rows of this CTA (sMo [KW][R][DP] fp32,
+// base-2 (max, sum) in sMm / sMl [KW][R]) and, across the cluster of ncta
+// CTAs that split the key range, the CTAs' partials; write out / lse for the
+// rows_here rows starting at row0 of the (segment, kv head) group.  In push
+// mode each CTA hands every element to the CTA that finishes it (the caller
+// arrived on the cluster barrier at the start); in pull mode each CTA reads
+// its slice from its peers.  A poisoned CTA (flags) zeroes the rows.  Every
+// thread of the CTA calls it.
+template <int DP, int KW, int R, int NT, bool kPush>
+static __device__ __forceinline__ void merge_rows(const AttendParams &p, const Segment &sg, int g, int row0,
+                                                  int rows_here, int flags, int rank, int ncta, float *sMo,
+                                                  float *sMm, float *sMl, float *sPm, float *sPl, float *sLse,
+                                                  float *sAllM, float *sAllL, int *sAllF, int *sFlag,
+                                                  float *sRecv) {
+    namespace cg = cooperative_groups;
+    const int tid = threadIdx.x;
+    constexpr float kLn2 = 0.6931471805599453f;
+    auto out_row = [&](int r) {
+        const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
+        return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
+    };
+    cg::cluster_group cluster = cg::this_cluster();
+    const int E = rows_here * DP;
+    const int per = (E + ncta - 1) / ncta;  // output elements each CTA of the cluster finishes
+    // Row statistics of the key-group merge, one thread per row: the max and
+    // sum, and each key group's weight 2^(m_k - M), left in sMm for the
+    // element pass.  A CTA alone in its cluster also keeps 1/L and the lse.
+    if (tid < rows_here) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) M = fmaxf(M, sMm[k * R + tid]);
+        float L = 0.f;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) {
+            const float w = M == -CUDART_INF_F ? 0.f : exp2f(sMm[k * R + tid] - M);
+            L = fmaf(w, sMl[k * R + tid], L);
+            sMm[k * R + tid] = w;
+        }
+        sPm[tid] = M;
+        if (ncta == 1) {
+            const bool zero = flags || L <= 0.f;
+            sPl[tid] = zero ? 0.f : 1.f / L;
+            sLse[tid] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
+        } else {
+            sPl[tid] = L;
+        }
+    }
+    __syncthreads();
+    // Owner of output element idx in the cluster: idx / per without an
+    // integer division in the loop.
+    const float inv_per = 1.f / (float)per;
+    auto owner = [&](int idx) {
+        int k = __float2int_rz((float)idx * inv_per);
+        k -= k * per > idx;
+        k += (k + 1) * per <= idx;
+        return k;
+    };
+    if (kPush && ncta > 1) {
+        // Every CTA of the cluster has started (the arrive at the top), so
+        // peers' shared memory may be written from here on.
+        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+        if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
+#pragma unroll 1
+        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
+            const int r = idx / ncta, c = idx - r * ncta;
+            *cluster.map_shared_rank(sAllM + r * 16 + rank, c) = sPm[r];
+            *cluster.map_shared_rank(sAllL + r * 16 + rank, c) = sPl[r];
+        }
+    }
+    // Merge the key groups element by element; finish each element here when
+    // the CTA is alone, otherwise hand it to the CTA that finishes it.
+#pragma unroll 4
+    for (int idx = tid; idx < E; idx += NT) {
+        const int r = idx / DP, d = idx - r * DP;
+        float o = 0.f;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) {
+            // a key group with no visible key has weight 0 and a zero accumulator
+            o = fmaf(sMm[k * R + r], sMo[((size_t)k * R + r) * DP + d], o);
+        }
+        if (ncta == 1) {
+            const long long orow = out_row(r);
+            if (d < p.D) p.out[orow * p.D + d] = flags ? 0.f : o * sPl[r];
+            if (d == 0 && p.lse) p.lse[orow] = sLse[r];
+        } else if constexpr (kPush) {
+            const int k = owner(idx);
+            *cluster.map_shared_rank(sRecv + rank * per + (idx - k * per), k) = o;
+        } else {
+            sMo[(size_t)r * DP + d] = o;  // element owned by this thread alone: merged in place
+        }
+    }
+    if (ncta == 1) return;
+
+    // ---- merge the cluster's partials (distributed shared memory)
+    if constexpr (kPush) {
+        cluster.sync();  // publishes every CTA's pushed partials
+    } else {
+        cluster.sync();
+#pragma unroll 1
+        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
+            const int r = idx / ncta, c = idx - r * ncta;
+            sAllM[r * 16 + c] = *cluster.map_shared_rank(sPm + r, c);
+            sAllL[r * 16 + c] = *cluster.map_shared_rank(sPl + r, c);
+        }
+        if (tid < ncta) sAllF[tid] = *cluster.map_shared_rank(sFlag, tid);
+        __syncthreads();
+    }
+    int poison = 0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
+    const int e0 = rank * per, e1 = min(E, e0 + per);
+#pragma unroll 1
+    for (int idx = e0 + tid; idx < e1; idx += NT) {
+        const int r = idx / DP, d = idx - r * DP;
+        float m[16], l[16], v[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            m[c] = c < ncta ? sAllM[r * 16 + c] : -CUDART_INF_F;
+            l[c] = c < ncta ? sAllL[r * 16 + c] : 0.f;
+            if constexpr (kPush)
+                v[c] = c < ncta ? sRecv[c * per + (idx - e0)] : 0.f;
+            else
+                v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
+        }
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) M = fmaxf(M, m[c]);
+        float W = 0.f, o = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            // A zero weight must not touch its partial: a poisoned one may hold NaN.
+            const float w = (M == -CUDART_INF_F || m[c] == -CUDART_INF_F) ? 0.f : exp2f(m[c] - M);
+            W = fmaf(w, l[c], W);
+            o += w != 0.f ? w * v[c] : 0.f;
+        }
+        const bool zero = poison || W <= 0.f;
+        const long long orow = out_row(r);
+        if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / W;
+        if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+    }
+    if constexpr (!kPush) cluster.sync();  // partials stay readable until every CTA has merged its slice
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <class C>
@@ -929,131 +1074,8 @@ __global__ void __launch_bounds__(C::kThreads) attend_kernel(const __grid_consta
     if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
     __syncthreads();
 
-    constexpr float kLn2 = 0.6931471805599453f;
-    auto out_row = [&](int r) {
-        const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
-        return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
-    };
-    cg::cluster_group cluster = cg::this_cluster();
-    const int E = rows_here * DP;
-    const int per = (E + ncta - 1) / ncta;  // output elements each CTA of the cluster finishes
-    // Row statistics of the key-group merge, one thread per row: the max and
-    // sum, and each key group's weight 2^(m_k - M), left in sMm for the
-    // element pass.  A CTA alone in its cluster also keeps 1/L and the lse.
-    if (tid < rows_here) {
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int k = 0; k < KW; ++k) M = fmaxf(M, sMm[k * R + tid]);
-        float L = 0.f;
-#pragma unroll
-        for (int k = 0; k < KW; ++k) {
-            const float w = M == -CUDART_INF_F ? 0.f : exp2f(sMm[k * R + tid] - M);
-            L = fmaf(w, sMl[k * R + tid], L);
-            sMm[k * R + tid] = w;
-        }
-        sPm[tid] = M;
-        if (ncta == 1) {
-            const bool zero = flags || L <= 0.f;
-            sPl[tid] = zero ? 0.f : 1.f / L;
-            sLse[tid] = zero ? -CUDART_INF_F : (M + log2f(L)) * kLn2;
-        } else {
-            sPl[tid] = L;
-        }
-    }
-    __syncthreads();
-    // Owner of output element idx in the cluster: idx / per without an
-    // integer division in the loop.
-    const float inv_per = 1.f / (float)per;
-    auto owner = [&](int idx) {
-        int k = __float2int_rz((float)idx * inv_per);
-        k -= k * per > idx;
-        k += (k + 1) * per <= idx;
-        return k;
-    };
-    if (C::kPush && ncta > 1) {
-        // Every CTA of the cluster has started (the arrive at the top), so
-        // peers' shared memory may be written from here on.
-        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
-        if (tid < ncta) *cluster.map_shared_rank(sAllF + rank, tid) = flags;
-#pragma unroll 1
-        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
-            const int r = idx / ncta, c = idx - r * ncta;
-            *cluster.map_shared_rank(sAllM + r * 16 + rank, c) = sPm[r];
-            *cluster.map_shared_rank(sAllL + r * 16 + rank, c) = sPl[r];
-        }
-    }
-    // Merge the key groups element by element; finish each element here when
-    // the CTA is alone, otherwise hand it to the CTA that finishes it.
-#pragma unroll 4
-    for (int idx = tid; idx < E; idx += NT) {
-        const int r = idx / DP, d = idx - r * DP;
-        float o = 0.f;
-#pragma unroll
-        for (int k = 0; k < KW; ++k) {
-            // a key group with no visible key has weight 0 and a zero accumulator
-            o = fmaf(sMm[k * R + r], sMo[((size_t)k * R + r) * DP + d], o);
-        }
-        if (ncta == 1) {
-            const long long orow = out_row(r);
-            if (d < p.D) p.out[orow * p.D + d] = flags ? 0.f : o * sPl[r];
-            if (d == 0 && p.lse) p.lse[orow] = sLse[r];
-        } else if constexpr (C::kPush) {
-            const int k = owner(idx);
-            *cluster.map_shared_rank(sRecv + rank * per + (idx - k * per), k) = o;
-        } else {
-            sMo[(size_t)r * DP + d] = o;  // element owned by this thread alone: merged in place
-        }
-    }
-    if (ncta == 1) return;
-
-    // ---- merge the cluster's partials (distributed shared memory)
-    if constexpr (C::kPush) {
-        cluster.sync();  // publishes every CTA's pushed partials
-    } else {
-        cluster.sync();
-#pragma unroll 1
-        for (int idx = tid; idx < rows_here * ncta; idx += NT) {
-            const int r = idx / ncta, c = idx - r * ncta;
-            sAllM[r * 16 + c] = *cluster.map_shared_rank(sPm + r, c);
-            sAllL[r * 16 + c] = *cluster.map_shared_rank(sPl + r, c);
-        }
-        if (tid < ncta) sAllF[tid] = *cluster.map_shared_rank(sFlag, tid);
-        __syncthreads();
-    }
-    int poison = 0;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) poison |= c < ncta ? sAllF[c] : 0;
-    const int e0 = rank * per, e1 = min(E, e0 + per);
-#pragma unroll 1
-    for (int idx = e0 + tid; idx < e1; idx += NT) {
-        const int r = idx / DP, d = idx - r * DP;
-        float m[16], l[16], v[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            m[c] = c < ncta ? sAllM[r * 16 + c] : -CUDART_INF_F;
-            l[c] = c < ncta ? sAllL[r * 16 + c] : 0.f;
-            if constexpr (C::kPush)
-                v[c] = c < ncta ? sRecv[c * per + (idx - e0)] : 0.f;
-            else
-                v[c] = c < ncta ? *cluster.map_shared_rank(sMo + (size_t)r * DP + d, c) : 0.f;
-        }
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) M = fmaxf(M, m[c]);
-        float W = 0.f, o = 0.f;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            // A zero weight must not touch its partial: a poisoned one may hold NaN.
-            const float w = (M == -CUDART_INF_F || m[c] == -CUDART_INF_F) ? 0.f : exp2f(m[c] - M);
-            W = fmaf(w, l[c], W);
-            o += w != 0.f ? w * v[c] : 0.f;
-        }
-        const bool zero = poison || W <= 0.f;
-        const long long orow = out_row(r);
-        if (d < p.D) p.out[orow * p.D + d] = zero ? 0.f : o / W;
-        if (d == 0 && p.lse) p.lse[orow] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
-    }
-    if constexpr (!C::kPush) cluster.sync();  // partials stay readable until every CTA has merged its slice
+    merge_rows<DP, KW, R, NT, C::kPush>(p, sg, g, row0, rows_here, flags, rank, ncta, sMo, sMm, sMl, sPm, sPl, sLse,
+                                        sAllM, sAllL, sAllF, sFlag, sRecv);
 }
 
 }  // namespace pkv

@@ -11,6 +11,7 @@
 #include "attend.cuh"
 #include "decode.cuh"
 #include "launch.h"
+#include "verify.cuh"
 
 #ifndef PKV_INST_VARIANT
 #error "PKV_INST_VARIANT not set"
@@ -37,6 +38,14 @@ static AttnKernel dinfo() {
                       C::kRows, C::DP, true};
 }
 
+// tcgen05 tile for wide bf16 groups with head_dim 128 (row class 6).
+template <class C>
+static AttnKernel vinfo() {
+    static_assert(C::kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
+    return AttnKernel{reinterpret_cast<const void *>(&verify_kernel<C>), C::kThreads, C::kSmemBytes,
+                      C::kRows, C::DP, true, true};
+}
+
 using B16 = __nv_bfloat16;
 #define CFG(T, MT, KW, NST, MMA) info<AttnCfg<T, PKV_INST_DP, MT, KW, NST, MMA>>()
 
@@ -55,6 +64,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #elif PKV_INST_DP == 128
     {
+        if (rc == 6) return vinfo<VfyCfg<4>>();
         if (rc == 5) return dinfo<DecCfg<128, 6, 2>>();
         if (rc == 4) return dinfo<DecCfg<128, 4, 3>>();
         if (rc == 0) return CFG(B16, 1, 4, 3, true);

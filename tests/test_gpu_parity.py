@@ -520,3 +520,37 @@ def test_thousands_of_segments_with_gaps(pkv, q_heads, q_len):
     w.seq_info = si2
     _, _, err, _ = run(pkv, w, max_kv=48)
     assert err & pkv.ERR_OVERLAP
+
+
+@pytest.mark.parametrize("q_heads,max_q", [(64, 16), (64, 32), (16, 8), (8, 16)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tcgen05_and_mma_sync_tiles_match_oracle(pkv, q_heads, max_q, causal):
+    """Wide bf16 groups with head_dim 128 (more than 8 rows per kv head) run
+    on the tcgen05 tile by default and on the mma.sync tile with
+    PKV_FLAG_MMA_SYNC; both match the oracle for one CTA per range, a split
+    that does not divide the pages, and the automatic split.  64 heads x 32
+    rows is 256 rows per kv head: two 128-row tiles."""
+    w = U.nan_tails(workloads.spec_verify(S=5, max_q=max_q, len_lo=1, len_hi=2500, causal=causal,
+                                          seed=q_heads * 3 + max_q, q_heads=q_heads))
+    for flags in (0, pkv.FLAG_MMA_SYNC):
+        for splits in (0, 1, 5):
+            out, lse, err, cache = run(pkv, w, flags=flags, num_splits=splits, max_kv=2500)
+            assert err == 0
+            check_append(w, 0, cache)
+            check_against_oracle(w, 0, out, lse, cache)
+
+
+def test_tcgen05_tile_ring_window_and_padding(pkv):
+    """The tcgen05 tile over ring storage with a window, and with left padding."""
+    w = U.nan_tails(workloads.long_context(S=3, kv_len=9000, window=700, ring_rows=720, seed=31, q_heads=64,
+                                           kv_heads=8, head_dim=128))
+    w.max_q_len = 2
+    out, lse, err, cache = run(pkv, w, max_kv=9000, max_q_len=2)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+    w = U.nan_tails(workloads.spec_verify(S=4, max_q=16, len_lo=200, len_hi=1200, seed=32, q_heads=64))
+    first = [150, 0, 1199, 37]
+    out, lse, err, cache = run(pkv, w, max_kv=1200, first_valid=first)
+    assert err == 0
+    check_against_oracle(w, 0, out, lse, cache, first_valid=first)
