@@ -320,7 +320,13 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
         return page_box ? encode_pool_pages(m, pool, c) : encode_pool(m, pool, c);
     };
     p.page_box = page_box ? 1 : 0;
-    if ((st = encode(&p.tmap_k, c->k[layer])) || (st = encode(&p.tmap_v, c->v[layer]))) return st;
+    if (pl.k.tc) {
+        // tcgen05 tile: K in 64-column boxes (one K-major tile per 4 pages), V in page boxes
+        if ((st = encode_pool(&p.tmap_k, c->k[layer], c)) || (st = encode_pool_pages(&p.tmap_v, c->v[layer], c)))
+            return st;
+    } else if ((st = encode(&p.tmap_k, c->k[layer])) || (st = encode(&p.tmap_v, c->v[layer]))) {
+        return st;
+    }
     p.q = q;
     p.k_new = k_new;
     p.v_new = v_new;

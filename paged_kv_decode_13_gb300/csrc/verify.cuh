@@ -4,29 +4,42 @@
 // head) carries G * q_len query rows, up to 128 (GQA 64:8 with 16 draft
 // tokens), so the products Q K^T and P V are real contractions.  They run on
 // the 5th-generation tensor cores: one thread issues tcgen05.mma (bf16 in,
-// fp32 accumulate) with both operands in shared memory, S and O live in
-// tensor memory (TMEM), and the softmax threads move S out of and P into
-// shared memory.  Same launch shape, key split and semantics as attend_kernel
+// fp32 accumulate) with K and V in shared memory and Q, S, P and O in
+// tensor memory (TMEM); the softmax threads read S from TMEM and write P
+// back over it.  Same launch shape, key split and semantics as attend_kernel
 // (grid (C, kv_heads, segments); the C CTAs of a range are one cluster and
-// merge through distributed shared memory with merge_rows).
+// merge through distributed shared memory with merge_rows, pushing into the
+// stage area each CTA has finished with).
 //
-// Per CTA (192 threads):
-//   warps 0-3   softmax: thread t owns query row t (TMEM lane t); after the
-//               loop the epilogue reads O back and hands it to the merge;
-//   warp 4      TMA issue: K and V of 4 pages (64 keys) per stage, each page
-//               as two 64-column boxes so a stage is a K-major tile of 64
-//               keys (128-byte swizzle) for Q K^T and an MN-major tile for
-//               P V;
-//   warp 5      MMA: waits for a stage, fixes its edge pages (stale rows
-//               zeroed, this step's rows taken from k_new / v_new and
-//               appended to the cache), issues S(j) = Q K_j^T (M = 128, N =
-//               64, 8 steps over head_dim) and, once P(j-1) is written,
-//               O += P(j-1) V(j-1) (M = 128, N = 128, 4 steps of 16 keys);
-//               also owns the TMEM allocation.
-// TMEM: S double-buffered in columns 0-63 / 64-127, O in 128-255.
+// Per CTA (352 threads):
+//   warps 0-7   softmax: row t of the tile (TMEM lane t) belongs to warps
+//               t / 32 and t / 32 + 4, each taking 32 of a stage's 64 keys
+//               and 64 of O's 128 columns; the pair agrees on the row's
+//               reference maximum through shared memory.  They also put Q
+//               into TMEM, write P into TMEM over the S columns they have
+//               read, and after the loop write their rows of O out (one CTA
+//               per range) or push them to the CTA of the cluster that
+//               merges those rows;
+//   warp 8      K loads: 4 pages (64 keys) per stage, each page as two
+//               64-column TMA boxes, so a stage is one K-major tile of 64
+//               keys (128-byte swizzle) for Q K^T; a stage is released as
+//               soon as its S product has completed;
+//   warp 10     V loads: 4 pages per stage, one TMA box per page (two
+//               64-column parts), an MN-major tile of 16 keys for each step
+//               of P V; released when its P V has completed;
+//   warp 9      MMA: fixes edge pages (stale V rows zeroed, this step's rows
+//               taken from k_new / v_new and appended to the cache), issues
+//               S(j) = Q K_j^T (M = 128, N = 64, A = Q from TMEM, 8 steps over
+//               head_dim) and, once P(j-1) is in TMEM, O += P(j-1) V(j-1)
+//               (M = 128, N = 128, A = P from TMEM, 4 steps of 16 keys); also
+//               owns the TMEM allocation.
+// TMEM (512 columns): S / P double-buffered in 0-63 / 64-127 (P as bf16
+// pairs in the first 32 columns of its buffer), O in 128-255, Q in 256-319.
+// Shared memory holds only the K and V stages, so 13 stages (208 KB) of
+// loads are in flight.
 //
-// The online softmax keeps one row per thread (no cross-lane reduction) and
-// raises a row's reference maximum lazily: only when a score exceeds it by
+// The online softmax keeps each row in one thread pair (no cross-lane
+// reduction) and raises a row's reference maximum lazily: only when a score exceeds it by
 // more than 2^8, and then O is rescaled in TMEM after the previous P V has
 // landed.  Every wait is bounded; a timeout poisons the CTA's output
 // (PKV_ERR_TIMEOUT), drains what is in flight and frees TMEM.
@@ -40,31 +53,33 @@
 
 namespace pkv {
 
-template <int NS_>
+template <int NK_, int NV_>
 struct VfyCfg {
     using T = __nv_bfloat16;
     static constexpr int DP = 128;                  // head_dim (this tile needs exactly 128)
-    static constexpr int NS = NS_;                  // stages of 4 pages
+    static constexpr int NK = NK_;                  // K stages of 4 pages
+    static constexpr int NV = NV_;                  // V stages of 4 pages
     static constexpr int kRows = 128;               // query rows per CTA = TMEM lanes
-    static constexpr int kThreads = 192;
+    static constexpr int kThreads = 352;            // 8 softmax warps, K loader, MMA, V loader
     static constexpr int kPages = 4;                // pages per stage (N = 64 keys)
-    static constexpr unsigned kQBytes = kRows * DP * 2;            // two 64-column halves
     static constexpr unsigned kHalf = kPages * kPage * 128;        // 64 keys x 128 B
-    static constexpr unsigned kStageBytes = 4 * kHalf;             // K halves, then V halves
-    static constexpr unsigned kPBytes = kRows * 128;               // 128 rows x 64 keys bf16
-    static constexpr size_t kLoopBytes = (size_t)NS * kStageBytes + 2 * kPBytes;
-    // after the loop the stages and P buffers hold the partial rows and their (max, sum)
-    static constexpr size_t kMergeBytes = (size_t)kRows * DP * 4 + 2 * kRows * 4;
-    static constexpr size_t kBodyBytes = kLoopBytes > kMergeBytes ? kLoopBytes : kMergeBytes;
-    // per row: pm, pl, lse, the cluster merge's gathered maxima / sums (16 CTAs each)
-    static constexpr size_t kRowBytes = (size_t)kRows * (3 + 16 + 16) * 4;
-    static constexpr int kBars = 2 * NS + 9;  // full, empty [NS]; s_full, s_free, p_full, pv_done [2]; drain
+    static constexpr unsigned kKStage = 2 * kHalf;                 // K: two 64-column halves
+    static constexpr unsigned kVStage = kPages * 4096;             // V: one 4 KB box per page
+    static constexpr size_t kLoopBytes = (size_t)NK * kKStage + (size_t)NV * kVStage;
+    // After the loop the stage area receives the rows pushed by the cluster:
+    // (max, sum) per source and row, then the rows, 16 sources at most.
+    static constexpr size_t kRecvStat = (size_t)16 * kRows * 8;
+    static constexpr size_t kRecvBytes = kRecvStat + ((size_t)kRows + 16) * DP * 4;
+    static constexpr size_t kBodyBytes = kLoopBytes > kRecvBytes ? kLoopBytes : kRecvBytes;
+    // merge weights [16][rows], cluster flags [16], row max exchange [2][8 warps][32], row sums [2][rows]
+    static constexpr size_t kWnBytes = (size_t)16 * kRows * 4 + 16 * 4 + 2 * 8 * 32 * 4 + 2 * kRows * 4;
+    // K, V full / empty; s_full, p_full, pv_done [2]; drain; row-pair exchange [4 quadrants][2]
+    static constexpr int kBars = 2 * NK + 2 * NV + 7 + 8;
     static constexpr size_t kMiscBytes = (size_t)kBars * 8 + 16 + 32 * 4 + (size_t)kThreads * 4;
-    static constexpr size_t kSmemBytes = 1024 + kQBytes + kBodyBytes + kRowBytes + kMiscBytes;
-    static constexpr int kTmemCols = 256;
+    static constexpr size_t kSmemBytes = 1024 + kBodyBytes + kWnBytes + kMiscBytes;
+    static constexpr int kTmemCols = 512;
     static_assert(kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
-    static_assert(kQBytes % 1024 == 0 && kStageBytes % 1024 == 0 && kPBytes % 1024 == 0,
-                  "operand tiles start on 1024-byte swizzle atoms");
+    static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0, "operand tiles start on 1024-byte swizzle atoms");
 };
 
 // ---------------------------------------------------------------- tcgen05 helpers
@@ -86,6 +101,15 @@ __device__ __forceinline__ void umma_bf16(unsigned d_tmem, uint64_t a, uint64_t 
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// As umma_bf16 with A (M x 16, bf16 pairs per 32-bit column, row = lane) read from TMEM.
+__device__ __forceinline__ void umma_bf16_ts(unsigned d_tmem, unsigned a_tmem, uint64_t b, uint32_t idesc,
+                                             int accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
@@ -151,6 +175,17 @@ __device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, unsigned parity) {
     return true;
 }
 
+// 16 32-bit columns into this thread's TMEM lane (warp-collective; waits for completion).
+__device__ __forceinline__ void tmem_st16(unsigned taddr, const unsigned (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
 // Offset of 16-byte chunk `c` (0..7) of row `r` in a tile of 128-byte rows
 // loaded with 128-byte swizzling (rows grouped in 1024-byte atoms).
 __device__ __forceinline__ unsigned swz_row(int r, int c) { return (unsigned)(r * 128 + ((c ^ (r & 7)) << 4)); }
@@ -160,31 +195,37 @@ __device__ __forceinline__ unsigned swz_row(int r, int c) { return (unsigned)(r 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_constant__ AttendParams p) {
     using T = __nv_bfloat16;
-    constexpr int DP = C::DP, NS = C::NS, R = C::kRows, NT = C::kThreads, PG = C::kPages;
+    namespace cg = cooperative_groups;
+    constexpr int DP = C::DP, NK = C::NK, NV = C::NV, R = C::kRows, NT = C::kThreads, PG = C::kPages;
     constexpr int EPC = 8;  // bf16 per 16-byte chunk
+    constexpr float kLn2 = 0.6931471805599453f;
+    constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+    constexpr unsigned kColO = 128, kColQ = 256;
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sQ = reinterpret_cast<unsigned char *>(
+    unsigned char *body = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *body = sQ + C::kQBytes;                  // stages, then the two P buffers
-    unsigned char *sP = body + (size_t)NS * C::kStageBytes;
-    float *sMo = reinterpret_cast<float *>(body);           // after the loop: [R][DP] partial rows
-    float *sMm = sMo + (size_t)R * DP;                      // [R] base-2 max
-    float *sMl = sMm + R;                                   // [R] sum
-    float *rows = reinterpret_cast<float *>(body + C::kBodyBytes);
-    float *sPm = rows, *sPl = sPm + R, *sLse = sPl + R;
-    float *sAllM = sLse + R, *sAllL = sAllM + R * 16;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sAllL + R * 16);
-    uint64_t *full = bars, *empty = bars + NS;              // [NS] each
-    uint64_t *s_full = bars + 2 * NS, *s_free = s_full + 2, *p_full = s_free + 2, *pv_done = p_full + 2;
+    unsigned char *sK = body;                                      // NK K stages
+    unsigned char *sV = sK + (size_t)NK * C::kKStage;              // NV V stages
+    float *sWn = reinterpret_cast<float *>(body + C::kBodyBytes);  // [16][R] merge weights
+    int *sCf = reinterpret_cast<int *>(sWn + 16 * R);              // [16] flags pushed by the cluster
+    float *sXm = reinterpret_cast<float *>(sCf + 16);              // [2][8][32] row maxima of each warp
+    float *sXl = sXm + 2 * 8 * 32;                                 // [2][R] row sums of each half
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sXl + 2 * R);
+    uint64_t *k_full = bars, *k_empty = bars + NK, *v_full = bars + 2 * NK, *v_empty = v_full + NV;
+    uint64_t *s_full = v_empty + NV, *p_full = s_full + 2, *pv_done = p_full + 2;
     uint64_t *drain = pv_done + 2;
+    uint64_t *pair = drain + 1;                                    // [4][2]: the two warps of a row quadrant
     unsigned *tslot = reinterpret_cast<unsigned *>(bars + C::kBars);
     volatile int *sAbort = reinterpret_cast<volatile int *>(tslot + 1);
-    int *sFlag = reinterpret_cast<int *>(tslot + 4);        // [0] own flags: 1 bad page, 2 timeout
-    int *sAllF = sFlag + 1;                                 // [16] flags of the cluster
-    int *sCov = sFlag + 32;                                 // [NT] coverage flags
+    int *sAppOk = reinterpret_cast<int *>(tslot + 2);
+    int *sFlag = reinterpret_cast<int *>(tslot + 4);            // [0] own flags: 1 bad page, 2 timeout
+    int *sCov = sFlag + 32;                                     // [NT] coverage flags
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool softmax = warp < 8;
+    const int quad = warp & 3, half = (warp >> 2) & 1;          // softmax: TMEM lane quadrant, key / column half
+    const int r = quad * 32 + lane;                             // softmax: this thread's row of the tile
     const int rank = blockIdx.x, ncta = gridDim.x;
     const int g = blockIdx.y / p.row_tiles, rt = blockIdx.y - g * p.row_tiles;
     const int s = blockIdx.z;
@@ -225,7 +266,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     const int active = (nblk + bps - 1) / bps;
     const int cb0 = pb_begin + rank * bps;
     const int nb = rank < active ? min(cb0 + bps, pb_end) - cb0 : 0;
-    const int ngr = (nb + PG - 1) / PG;                     // stages (groups of 4 pages) of this CTA
+    const int ngr = (nb + PG - 1) / PG;                     // groups of 4 pages of this CTA
     const int lo_pos = cb0 * kPage, hi_pos = (cb0 + nb) * kPage;
 
     const T *knew = reinterpret_cast<const T *>(p.k_new);
@@ -237,12 +278,17 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
 
     if (tid == 0) {
         #pragma unroll 1
-        for (int i = 0; i < C::kBars; ++i) mbar_init(bars + i, (i >= 2 * NS + 2 && i < 2 * NS + 6) ? 4 : 1);
+        for (int i = 0; i < C::kBars; ++i) {
+            const bool eight = i >= 2 * NK + 2 * NV + 2 && i < 2 * NK + 2 * NV + 4;  // p_full: every softmax warp
+            const bool two = i >= 2 * NK + 2 * NV + 7;                            // pair: both warps of a quadrant
+            mbar_init(bars + i, eight ? 8 : two ? 2 : 1);
+        }
         fence_barrier_init();
         sFlag[0] = 0;
         *sAbort = 0;
+        *sAppOk = 0;
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tslot)),
                      "r"(C::kTmemCols)
                      : "memory");
@@ -252,21 +298,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const unsigned tmem = *tslot;
-
-    // Append validity, all or nothing over the segment's new rows (the block
-    // table is not written by the previous kernel).
-    bool app_ok = false;
-    if (has_new) {
-        bool ok = true;
-        #pragma unroll 1
-        for (int i = tid; i < sg.ql; i += NT) {
-            const int pos = new_start + i;
-            const int rr = p.ring_rows ? pos % p.ring_rows : pos;
-            const int b = bt_row[rr / kPage];
-            ok &= b >= 0 && (long long)b < p.num_blocks;
-        }
-        app_ok = __syncthreads_and(ok);
-    }
+    const unsigned lane_off = (unsigned)(32 * quad) << 16;
 
     // Bounded wait of a whole warp on one phase (every lane observes it); gives
     // up at once when another role has already timed out.  Warp-uniform:
@@ -286,7 +318,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         return ok;
     };
 
-    // ---- TMA issue (warp 4): group j = pages cb0 + 4j .. cb0 + 4j + 3
+    // ---- TMA loads (warp 8: K, warp 10: V): group j = pages cb0 + 4j .. + 3
+    const bool loader = warp == kWarpK || warp == kWarpV;
+    const bool is_v = warp == kWarpV;
     int id_reg = -1, id_window = -1, issued = 0;
     bool bad = false;
     auto load_ids = [&](int li0) {
@@ -294,41 +328,39 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         const int li = id_window + lane;
         id_reg = li < nb ? bt_row[table_page(cb0 + li, p.ring_rows)] : -1;
     };
+    // K comes in 2 KB TMA boxes (16 keys x 64 columns) into two 64-column
+    // halves of the stage, so the stage is one K-major tile of 64 keys; V in
+    // 4 KB boxes, one per page (16 keys x two 64-column parts).
     auto issue = [&](int j) {
-        const int st = j % NS;
-        unsigned char *stage = body + (size_t)st * C::kStageBytes;
+        uint64_t *bar = (is_v ? v_full + j % NV : k_full + j % NK);
+        unsigned char *stage = is_v ? sV + (size_t)(j % NV) * C::kVStage : sK + (size_t)(j % NK) * C::kKStage;
         int ok_pages = 0;
         unsigned okmask = 0;
+        int bids[PG];
 #pragma unroll
         for (int u = 0; u < PG; ++u) {
             const int li = j * PG + u;
+            bids[u] = -1;
             if (li < nb) {
                 if ((li & ~31) != id_window) load_ids(li);
-                const int bid = __shfl_sync(0xffffffffu, id_reg, li & 31);
-                const bool ok = bid >= 0 && (long long)bid < p.num_blocks;
+                bids[u] = __shfl_sync(0xffffffffu, id_reg, li & 31);
+                const bool ok = bids[u] >= 0 && (long long)bids[u] < p.num_blocks;
                 bad |= !ok;
                 if (ok) { okmask |= 1u << u; ++ok_pages; }
             }
         }
         if (lane == 0) {
-            uint64_t *bar = full + st;
             fence_proxy_async();
-            if (ok_pages) {
-                mbar_expect_tx(bar, (unsigned)ok_pages * 4u * 2048u);
-            } else {
-                mbar_arrive(bar);
-            }
-        }
+            if (ok_pages) mbar_expect_tx(bar, (unsigned)ok_pages * 4096u);
+            else mbar_arrive(bar);
 #pragma unroll
-        for (int u = 0; u < PG; ++u) {
-            const int li = j * PG + u;
-            const int bid = li < nb ? __shfl_sync(0xffffffffu, id_reg, li & 31) : -1;
-            if (lane == 0 && ((okmask >> u) & 1u)) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tma_load_4d(stage + h * C::kHalf + u * 2048, &p.tmap_k, full + st, h * 64, g, 0, bid);
-                    tma_load_4d(stage + 2 * C::kHalf + h * C::kHalf + u * 2048, &p.tmap_v, full + st, h * 64, g, 0,
-                                bid);
+            for (int u = 0; u < PG; ++u) {
+                if (!((okmask >> u) & 1u)) continue;
+                if (is_v) {
+                    tma_load_5d(stage + u * 4096, &p.tmap_v, bar, 0, 0, 0, g, bids[u]);
+                } else {
+                    tma_load_4d(stage + u * 2048, &p.tmap_k, bar, 0, g, 0, bids[u]);
+                    tma_load_4d(stage + C::kHalf + u * 2048, &p.tmap_k, bar, 64, g, 0, bids[u]);
                 }
             }
         }
@@ -336,39 +368,42 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     // Pages wholly below new_start may be fetched before the dependency wait;
     // in the fused call every page may (this step's rows are replaced after it).
     auto early_ok = [&](int j) { return fused || (cb0 + min(j * PG + PG, nb)) * kPage <= new_start; };
+    const int NSt = is_v ? NV : NK;
 
-    if (warp == 4) {
+    if (loader) {
         load_ids(0);
         #pragma unroll 1
-        for (; issued < NS && issued < ngr; ++issued) {
+        for (; issued < NSt && issued < ngr; ++issued) {
             if (!early_ok(issued)) break;
             issue(issued);
         }
-        // The first 32 pages that are not in flight go to L2 now, so their
-        // HBM traffic overlaps the previous kernel's tail: lane l holds the
-        // id of page l.
-        if (id_window == 0 && lane >= issued * PG && lane < nb && id_reg >= 0 && (long long)id_reg < p.num_blocks) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tma_prefetch_l2_4d(&p.tmap_k, h * 64, g, 0, id_reg);
-                tma_prefetch_l2_4d(&p.tmap_v, h * 64, g, 0, id_reg);
-            }
+    }
+    // Append validity, all or nothing over the segment's new rows (the block
+    // table is not written by the previous kernel); kept for the MMA warp.
+    if (has_new && softmax) {
+        bool ok = true;
+        #pragma unroll 1
+        for (int i = tid; i < sg.ql; i += 256) {
+            const int pos = new_start + i;
+            const int rr = p.ring_rows ? pos % p.ring_rows : pos;
+            const int b = bt_row[rr / kPage];
+            ok &= b >= 0 && (long long)b < p.num_blocks;
         }
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0 && !ok) atomicOr(sAppOk, 1);
     }
     // Warm L2 with the rows read right after the wait: this tile's queries
     // and, in the fused call, this step's K/V rows.
-    {
-        const int nq = rows_here * 2;
-        #pragma unroll 1
-        for (int c = tid; c < nq; c += NT) {
-            const int r = c >> 1, ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
+    if (softmax) {
+        if (r < rows_here) {
+            const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
             const T *src = reinterpret_cast<const T *>(p.q) + (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D;
-            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + (c & 1) * 128));
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + half * 128));
         }
         if (has_new) {
             const int a = max(new_start, lo_pos), e = min(kend, hi_pos);
             #pragma unroll 1
-            for (int c = tid; c < (e - a) * 4; c += NT) {
+            for (int c = tid; c < (e - a) * 4; c += 256) {
                 const int row = c >> 2, kv = (c >> 1) & 1;
                 const T *src = (kv ? vnew : knew) + (((long long)sg.q0 + (a + row - new_start)) * p.Hkv + g) * p.D;
                 asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char *>(src) + (c & 1) * 128));
@@ -379,122 +414,143 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     pdl_wait();
     pdl_trigger();
 
-    // ---- queries: 128 rows x 128 columns, K-major, 128-byte swizzle, two
-    // 64-column halves; rows past the group are zero.
-    {
-        constexpr int kIt = (R * 16 + NT - 1) / NT;
-        uint4 qv[kIt];
+    // ---- queries into TMEM (columns 256-319, bf16 pairs): each softmax
+    // thread its row's half; rows past the group are zero.
+    if (softmax) {
+        unsigned qv[32];
+        const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
+        const T *src = reinterpret_cast<const T *>(p.q) + (((long long)sg.q0 + (r < rows_here ? i : 0)) * p.Hq +
+                                                            (long long)g * p.G + (r < rows_here ? jh : 0)) * p.D;
 #pragma unroll
-        for (int it = 0; it < kIt; ++it) {
-            const int c = tid + it * NT, r = c >> 4, ch = c & 15, ur = row0 + r;
-            qv[it] = make_uint4(0u, 0u, 0u, 0u);
-            if (c < R * 16 && r < rows_here && ch < dchunks) {
-                const int i = ur / p.G, jh = ur - i * p.G;
-                qv[it] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) +
-                                                          (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D +
-                                                          ch * EPC);
-            }
+        for (int c = 0; c < 8; ++c) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows_here && half * 8 + c < dchunks) v = *reinterpret_cast<const uint4 *>(src + (half * 8 + c) * EPC);
+            qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
         }
+        unsigned lo16[16], hi16[16];
 #pragma unroll
-        for (int it = 0; it < kIt; ++it) {
-            const int c = tid + it * NT, r = c >> 4, ch = c & 15;
-            if (c < R * 16)
-                *reinterpret_cast<uint4 *>(sQ + (ch >> 3) * (R * 128) + swz_row(r, ch & 7)) = qv[it];
-        }
+        for (int k = 0; k < 16; ++k) { lo16[k] = qv[k]; hi16[k] = qv[16 + k]; }
+        tmem_st16(tmem + lane_off + kColQ + half * 32, lo16);
+        tmem_st16(tmem + lane_off + kColQ + half * 32 + 16, hi16);
     }
-    fence_proxy_async();
     if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
-    if (warp == 4) {
+    if (loader) {
         #pragma unroll 1
-        for (; issued < NS && issued < ngr; ++issued) issue(issued);
+        for (; issued < NSt && issued < ngr; ++issued) issue(issued);
     }
-    __syncthreads();  // queries staged
+    tc_fence_before();
+    __syncthreads();  // queries in TMEM, append validity known
+    tc_fence_after();
+    const bool app_ok = has_new && *sAppOk == 0;
 
     bool timed_out = false;
-    const unsigned lane_off = (unsigned)(32 * (warp & 3)) << 16;
+    float m = -CUDART_INF_F, l = 0.f;  // softmax: this row's reference max and this half's sum
 
-    if (warp == 4) {
-        // ---------------- TMA issue: refill each stage once its P V has completed
+    if (loader) {
+        // ---------------- refill each stage once its product has completed
+        uint64_t *emp = is_v ? v_empty : k_empty;
         #pragma unroll 1
         for (int j = issued; j < ngr; ++j) {
-            if (!wait_bar(empty + (j % NS), ((j / NS) - 1) & 1)) { timed_out = true; break; }
+            if (!wait_bar(emp + (j % NSt), ((j / NSt) - 1) & 1)) { timed_out = true; break; }
             issue(j);
             issued = j + 1;
         }
         // Drain: every issued stage has landed before its memory is reused or freed.
         if (lane == 0) {
+            uint64_t *fb = is_v ? v_full : k_full;
             #pragma unroll 1
-            for (int j = max(0, issued - NS); j < issued; ++j)
-                if (!mbar_wait_ns(full + (j % NS), (j / NS) & 1)) break;
+            for (int j = max(0, issued - NSt); j < issued; ++j)
+                if (!mbar_wait_ns(fb + (j % NSt), (j / NSt) & 1)) break;
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ---------------- edge-page fix-up and MMA issue
         const uint32_t id_s = umma_idesc_bf16(128, 64, 0), id_o = umma_idesc_bf16(128, 128, 1);
-        const unsigned q_addr = smem_u32(sQ);
-        // Stale rows zeroed, this step's rows written into the stage (and the cache).
-        auto fix_group = [&](int j, unsigned char *stage) {
+        // Rows of page u of group j: stale ones [0, zlo) and [zhi, 16) (V
+        // zeroed), this step's ones [na, zhi) (K or V from k_new / v_new, also
+        // appended to the cache).  A page past the range is all stale.
+        auto page_rows = [&](int j, int u, int &zlo, int &zhi, int &na) {
+            const int li = j * PG + u, pos0 = (cb0 + li) * kPage;
+            if (li < nb) {
+                zlo = min(max(lo_u - pos0, 0), kPage);
+                zhi = min(max(kend - pos0, 0), kPage);
+                na = fused ? min(max(new_start - pos0, 0), kPage) : zhi;
+            } else {
+                zlo = kPage; zhi = kPage; na = kPage;
+            }
+        };
+        // this step's rows [na, zhi) of page u into the stage (and the cache)
+        auto put_new = [&](int kv, unsigned char *stage, int j, int u, int na, int zhi) {
+            const int pos0 = (cb0 + j * PG + u) * kPage, nn = (zhi - na) * 16;
+            const long long bpage = app_ok ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
+            const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;
+            #pragma unroll 1
+            for (int c = lane; c < nn; c += 32) {
+                const int o = na + (c >> 4), ch = c & 15;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (ch < dchunks) {
+                    v = *reinterpret_cast<const uint4 *>((kv ? vnew : knew) +
+                                                         (((long long)sg.q0 + (pos0 + o - new_start)) * p.Hkv + g) * p.D +
+                                                         ch * EPC);
+                    if (app_ok) {
+                        const long long slot = bpage * kPage + (ring_base + o) % kPage;
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
+                                                   (slot * p.Hkv + g) * p.D + ch * EPC) = v;
+                    }
+                }
+                const unsigned off = kv ? u * 4096 + (ch >> 3) * 2048 + swz_row(o, ch & 7)
+                                        : (ch >> 3) * C::kHalf + u * 2048 + swz_row(o, ch & 7);
+                *reinterpret_cast<uint4 *>(stage + off) = v;
+            }
+        };
+        // K: only this step's rows (stale keys are masked out of S).
+        auto fix_k = [&](int j, unsigned char *stage) {
             bool any = false;
 #pragma unroll 1
             for (int u = 0; u < PG; ++u) {
-                const int li = j * PG + u;
-                const int pos0 = (cb0 + li) * kPage;
                 int zlo, zhi, na;
-                if (li < nb) {
-                    zlo = min(max(lo_u - pos0, 0), kPage);
-                    zhi = min(max(kend - pos0, 0), kPage);
-                    na = fused ? min(max(new_start - pos0, 0), kPage) : zhi;
-                } else {
-                    zlo = kPage; zhi = kPage; na = kPage;  // no page: all 16 rows zeroed
-                }
-                if (!(zlo > 0 || zhi < kPage || na < zhi)) continue;
-                any = true;
-                const int nz = (zlo + kPage - zhi) * 16;  // (row, chunk) pairs of stale rows, K and V
-                #pragma unroll 1
-                for (int c = lane; c < 2 * nz; c += 32) {
-                    const int kv = c >= nz, rem = c - kv * nz, o0 = rem >> 4, ch = rem & 15;
-                    const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
-                    *reinterpret_cast<uint4 *>(stage + kv * 2 * C::kHalf + (ch >> 3) * C::kHalf + u * 2048 +
-                                               swz_row(o, ch & 7)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                const int nn = (zhi - na) * 16;
-                if (nn > 0) {
-                    const long long bpage = app_ok ? (long long)bt_row[table_page(pos0 / kPage, p.ring_rows)] : 0;
-                    const int ring_base = p.ring_rows ? pos0 % p.ring_rows : pos0;
-                    #pragma unroll 1
-                    for (int c = lane; c < 2 * nn; c += 32) {
-                        const int kv = c >= nn, rem = c - kv * nn, r0 = rem >> 4, ch = rem & 15;
-                        const int o = na + r0;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (ch < dchunks) {
-                            v = *reinterpret_cast<const uint4 *>(
-                                (kv ? vnew : knew) + (((long long)sg.q0 + (pos0 + o - new_start)) * p.Hkv + g) * p.D +
-                                ch * EPC);
-                            if (app_ok) {
-                                const long long slot = bpage * kPage + (ring_base + o) % kPage;
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(kv ? p.v_pool_w : p.k_pool_w) +
-                                                           (slot * p.Hkv + g) * p.D + ch * EPC) = v;
-                            }
-                        }
-                        *reinterpret_cast<uint4 *>(stage + kv * 2 * C::kHalf + (ch >> 3) * C::kHalf + u * 2048 +
-                                                   swz_row(o, ch & 7)) = v;
-                    }
-                }
+                page_rows(j, u, zlo, zhi, na);
+                if (na < zhi) { any = true; put_new(0, stage, j, u, na, zhi); }
             }
             if (any) fence_proxy_async();  // generic writes before the tensor core reads the stage
             __syncwarp();
         };
+        // V: stale rows zeroed (P is zero there, but 0 x NaN is not), this step's rows.
+        auto fix_v = [&](int j, unsigned char *stage) {
+            bool any = false;
+#pragma unroll 1
+            for (int u = 0; u < PG; ++u) {
+                int zlo, zhi, na;
+                page_rows(j, u, zlo, zhi, na);
+                if (zlo > 0 || zhi < kPage) {
+                    any = true;
+                    const int nz = (zlo + kPage - zhi) * 16;
+                    #pragma unroll 1
+                    for (int c = lane; c < nz; c += 32) {
+                        const int o0 = c >> 4, ch = c & 15;
+                        const int o = o0 < zlo ? o0 : zhi + (o0 - zlo);
+                        *reinterpret_cast<uint4 *>(stage + u * 4096 + (ch >> 3) * 2048 + swz_row(o, ch & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                if (na < zhi) { any = true; put_new(1, stage, j, u, na, zhi); }
+            }
+            if (any) fence_proxy_async();
+            __syncwarp();
+        };
         auto issue_pv = [&](int i) {
-            const int b = i & 1, st = i % NS;
+            const int b = i & 1, vs = i % NV;
+            unsigned char *stage = sV + (size_t)vs * C::kVStage;
+            if (!wait_bar(v_full + vs, (i / NV) & 1)) return false;
+            fix_v(i, stage);
             if (!wait_bar(p_full + b, (i >> 1) & 1)) return false;
             tc_fence_after();
             if (lane == 0) {
-                const unsigned p_addr = smem_u32(sP + b * C::kPBytes);
-                const unsigned v_addr = smem_u32(body + (size_t)st * C::kStageBytes + 2 * C::kHalf);
+                const unsigned v_addr = smem_u32(stage);
 #pragma unroll
                 for (int u = 0; u < PG; ++u)
-                    umma_bf16(tmem + 128, umma_desc(p_addr + u * 32, 16, 1024),
-                              umma_desc(v_addr + u * 2048, C::kHalf, 1024), id_o, (i > 0 || u > 0) ? 1 : 0);
-                umma_commit(empty + st);
+                    umma_bf16_ts(tmem + kColO, tmem + b * 64 + u * 8, umma_desc(v_addr + u * 4096, 2048, 1024), id_o,
+                                 (i > 0 || u > 0) ? 1 : 0);
+                umma_commit(v_empty + vs);
                 umma_commit(pv_done + b);
             }
             __syncwarp();
@@ -502,19 +558,21 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         };
         #pragma unroll 1
         for (int j = 0; j < ngr && !timed_out; ++j) {
-            const int st = j % NS, b = j & 1;
-            unsigned char *stage = body + (size_t)st * C::kStageBytes;
-            if (!wait_bar(full + st, (j / NS) & 1)) { timed_out = true; break; }
-            fix_group(j, stage);
-            if (j >= 2 && !wait_bar(s_free + b, ((j - 2) >> 1) & 1)) { timed_out = true; break; }
+            const int ks = j % NK, b = j & 1;
+            unsigned char *stage = sK + (size_t)ks * C::kKStage;
+            if (!wait_bar(k_full + ks, (j / NK) & 1)) { timed_out = true; break; }
+            fix_k(j, stage);
+            // S(j) overwrites buffer b, which P V(j - 2) reads P(j - 2) from.
+            if (j >= 2 && !wait_bar(pv_done + b, ((j - 2) >> 1) & 1)) { timed_out = true; break; }
             tc_fence_after();
             if (lane == 0) {
                 const unsigned k_addr = smem_u32(stage);
 #pragma unroll
                 for (int k = 0; k < DP / 16; ++k)
-                    umma_bf16(tmem + b * 64, umma_desc(q_addr + (k >> 2) * (R * 128) + (k & 3) * 32, 16, 1024),
-                              umma_desc(k_addr + (k >> 2) * C::kHalf + (k & 3) * 32, 16, 1024), id_s, k > 0 ? 1 : 0);
+                    umma_bf16_ts(tmem + b * 64, tmem + kColQ + k * 8,
+                                 umma_desc(k_addr + (k >> 2) * C::kHalf + (k & 3) * 32, 16, 1024), id_s, k > 0 ? 1 : 0);
                 umma_commit(s_full + b);
+                umma_commit(k_empty + ks);
             }
             __syncwarp();
             if (j >= 1 && !issue_pv(j - 1)) { timed_out = true; break; }
@@ -527,37 +585,37 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             mbar_wait_ns(drain, 0);
         }
         __syncwarp();
-    } else {
-        // ---------------- softmax: thread = query row
-        const int r = tid;
+    } else if (softmax) {
+        // ---------------- softmax: this thread = (row r, 32 keys of each stage)
         int lo_r = 0, hi_r = 0;
         if (r < rows_here) row_key_bounds(new_start + (row0 + r) / p.G, kend, p.causal, p.window, first, lo_r, hi_r);
         hi_r = min(hi_r, hi_pos);
-        float m = -CUDART_INF_F, l = 0.f;
         #pragma unroll 1
         for (int j = 0; j < ngr; ++j) {
             const int b = j & 1;
             if (!wait_bar(s_full + b, (j >> 1) & 1)) { timed_out = true; break; }
             tc_fence_after();
-            float x[64];
-            {
-                float t0[32], t1[32];
-                tmem_ld32(tmem + lane_off + b * 64, t0);
-                tmem_ld32(tmem + lane_off + b * 64 + 32, t1);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) { x[k] = t0[k]; x[32 + k] = t1[k]; }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free + b);
-            const int pos0 = lo_pos + j * PG * kPage;
+            float x[32];
+            tmem_ld32(tmem + lane_off + b * 64 + half * 32, x);
+            const int pos0 = lo_pos + j * PG * kPage + half * 32;
             float mx = -CUDART_INF_F;
 #pragma unroll
-            for (int k = 0; k < 64; ++k) {
+            for (int k = 0; k < 32; ++k) {
                 const int pos = pos0 + k;
                 x[k] = (pos >= lo_r && pos < hi_r) ? x[k] * p.scale_log2 : -CUDART_INF_F;
                 mx = fmaxf(mx, x[k]);
             }
+            // The row's two halves agree on its maximum (double-buffered
+            // exchange: a buffer is rewritten only after the partner has
+            // passed the next exchange).  The pair's barrier also orders this
+            // half's read of S before the other half writes P over it.
+            sXm[(b * 8 + warp) * 32 + lane] = mx;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair + quad * 2 + b);
+            if (!wait_bar(pair + quad * 2 + b, (j >> 1) & 1)) { timed_out = true; break; }
+            tc_fence_after();
+            mx = fmaxf(mx, sXm[(b * 8 + (warp ^ 4)) * 32 + lane]);
             // Lazy reference maximum: raised only when a score passes it by 2^8.
             const bool grow = mx > m + 8.f;
             if (__any_sync(0xffffffffu, grow)) {
@@ -565,87 +623,165 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
                 const float alpha = (!grow || m == -CUDART_INF_F) ? (grow ? 0.f : 1.f) : exp2f(m - m_new);
                 if (j > 0 && __any_sync(0xffffffffu, grow && m != -CUDART_INF_F)) {
                     // O holds P V up to group j - 1 against the old reference:
-                    // wait for that product, then rescale in TMEM.
+                    // wait for that product, then rescale this half's columns.
                     if (!wait_bar(pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1)) { timed_out = true; break; }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c0 = 0; c0 < DP; c0 += 32) {
+                    for (int c0 = 0; c0 < 64; c0 += 32) {
                         float o[32];
-                        tmem_ld32(tmem + lane_off + 128 + c0, o);
+                        tmem_ld32(tmem + lane_off + kColO + half * 64 + c0, o);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) o[k] *= alpha;
-                        tmem_st32(tmem + lane_off + 128 + c0, o);
+                        tmem_st32(tmem + lane_off + kColO + half * 64 + c0, o);
                     }
-                    tc_fence_before();
                 }
                 l *= alpha;
                 m = m_new;
             }
             const float mu = m == -CUDART_INF_F ? 0.f : m;
-            // P(j) goes to buffer b once P V(j - 2) has read it.
-            if (j >= 2 && !wait_bar(pv_done + b, ((j - 2) >> 1) & 1)) { timed_out = true; break; }
-            unsigned char *prow = sP + b * C::kPBytes;
+            unsigned pk[16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float e[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    e[k] = exp2f(x[c * 8 + k] - mu);
-                    l += e[k];
-                }
-                uint4 v;
-                v.x = pack_bf16x2(e[0], e[1]);
-                v.y = pack_bf16x2(e[2], e[3]);
-                v.z = pack_bf16x2(e[4], e[5]);
-                v.w = pack_bf16x2(e[6], e[7]);
-                *reinterpret_cast<uint4 *>(prow + swz_row(r, c)) = v;
+            for (int k = 0; k < 16; ++k) {
+                const float e0 = exp2f(x[2 * k] - mu), e1 = exp2f(x[2 * k + 1] - mu);
+                l += e0 + e1;
+                pk[k] = pack_bf16x2(e0, e1);
             }
-            fence_proxy_async();
+            // P(j) as bf16 pairs over the first 32 columns of buffer b
+            tmem_st16(tmem + lane_off + b * 64 + half * 16, pk);
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + b);
         }
-        // ---------------- epilogue: this row's partial O, base-2 max and sum
+        // the last product has landed before O is read back
         if (!timed_out && ngr > 0 && !wait_bar(pv_done + ((ngr - 1) & 1), ((ngr - 1) >> 1) & 1)) timed_out = true;
         timed_out = __any_sync(0xffffffffu, timed_out);
-        if (!timed_out && ngr > 0) {
-            tc_fence_after();
-            // The stages are idle once the last product has landed; the
-            // partial rows overwrite them (after the barrier below).
-            float o[4][32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + 128 + q * 32, o[q]);
-            tc_fence_before();
-            named_barrier(1, 128);  // every softmax warp has read its O rows: stages may be overwritten
-            float *dst = sMo + (size_t)r * DP;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int k = 0; k < 32; k += 4)
-                    *reinterpret_cast<float4 *>(dst + q * 32 + k) = make_float4(o[q][k], o[q][k + 1], o[q][k + 2], o[q][k + 3]);
-        } else {
-            named_barrier(1, 128);
-            float *dst = sMo + (size_t)r * DP;
-#pragma unroll 4
-            for (int k = 0; k < DP; k += 4) *reinterpret_cast<float4 *>(dst + k) = make_float4(0.f, 0.f, 0.f, 0.f);
-            m = -CUDART_INF_F;
-            l = 0.f;
-        }
-        sMm[r] = m;
-        sMl[r] = l;
+        sXl[half * R + r] = timed_out ? 0.f : l;
     }
     if (timed_out && lane == 0) atomicOr(sFlag, 2);
     if (bad && lane == 0) atomicOr(sFlag, 1);
     tc_fence_before();
-    __syncthreads();  // partial rows written, every tcgen05 access done
-    if (warp == 5) {
+    __syncthreads();  // every role is done; the stage area is idle
+    tc_fence_after();
+    const int flags = sFlag[0];
+    if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
+    const bool has_o = ngr > 0 && !(flags & 2);  // O in TMEM holds this CTA's product
+    if (softmax) {
+        l = sXl[r] + sXl[R + r];                  // the row's sum over both halves
+        if (!has_o) { m = -CUDART_INF_F; l = 0.f; }
+    }
+
+    // ---- epilogue: rows of O straight from TMEM
+    auto out_row = [&](int rr) {
+        const int ur = row0 + rr, i = ur / p.G, jh = ur - i * p.G;
+        return ((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh;
+    };
+    // out is only required to be 4-byte aligned: vector stores when it is 16.
+    const bool out16 = (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0;
+    auto store4 = [&](float *dst, float4 v) {
+        if (out16) {
+            *reinterpret_cast<float4 *>(dst) = v;
+        } else {
+            dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+        }
+    };
+    if (ncta == 1) {
+        if (softmax) {
+            const bool zero = flags || !(l > 0.f);
+            const float inv = zero ? 0.f : 1.f / l;
+            float *dst = p.out + out_row(min(r, rows_here - 1)) * p.D + half * 64;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                float o[32];
+                if (has_o) tmem_ld32(tmem + lane_off + kColO + half * 64 + c0, o);
+                if (r < rows_here) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        store4(dst + c0 + k, zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                  : make_float4(o[k] * inv, o[k + 1] * inv, o[k + 2] * inv,
+                                                                o[k + 3] * inv));
+                }
+            }
+            if (half == 0 && r < rows_here && p.lse)
+                p.lse[out_row(r)] = zero ? -CUDART_INF_F : (m + log2f(l)) * kLn2;
+        }
+    } else {
+        // Rows are merged by owner: CTA k of the cluster finishes rows
+        // [k * per, (k + 1) * per).  Every CTA pushes each row's (max, sum)
+        // and partial O into the owner's (idle) stage area.
+        cg::cluster_group cluster = cg::this_cluster();
+        const int per = (rows_here + ncta - 1) / ncta;
+        float2 *rStat = reinterpret_cast<float2 *>(body);                       // [16][per]
+        float *rRows = reinterpret_cast<float *>(body + C::kRecvStat);         // [16][per][DP]
+        cluster.sync();  // every CTA is past its loop: its stage area may be written
+        if (tid < ncta) *cluster.map_shared_rank(sCf + rank, tid) = flags;
+        if (softmax) {
+            const int k = min(r / per, ncta - 1), rr = r - k * per;
+            if (half == 0 && r < rows_here) *cluster.map_shared_rank(rStat + rank * per + rr, k) = make_float2(m, l);
+            float *dst = r < rows_here ? cluster.map_shared_rank(rRows + ((size_t)rank * per + rr) * DP + half * 64, k)
+                                       : nullptr;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                float o[32];
+                if (has_o) {
+                    tmem_ld32(tmem + lane_off + kColO + half * 64 + c0, o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+                }
+                if (r < rows_here)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+            }
+        }
+        cluster.sync();  // publishes the pushed rows
+        int poison = 0;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) poison |= c < ncta ? sCf[c] : 0;
+        const int r0 = rank * per, nr = max(0, min(per, rows_here - r0));
+        // per owned row: normalised weight of each source, and the lse
+        if (tid < nr) {
+            float M = -CUDART_INF_F;
+#pragma unroll 1
+            for (int c = 0; c < ncta; ++c) M = fmaxf(M, rStat[c * per + tid].x);
+            float W = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < ncta; ++c) {
+                const float2 st = rStat[c * per + tid];
+                // a zero weight must not touch its partial: a poisoned one may hold NaN
+                const float w = (M == -CUDART_INF_F || st.x == -CUDART_INF_F) ? 0.f : exp2f(st.x - M);
+                sWn[c * R + tid] = w;
+                W = fmaf(w, st.y, W);
+            }
+            const bool zero = poison || !(W > 0.f);
+            const float inv = zero ? 0.f : 1.f / W;
+#pragma unroll 1
+            for (int c = 0; c < ncta; ++c) sWn[c * R + tid] = zero ? 0.f : sWn[c * R + tid] * inv;
+            if (p.lse) p.lse[out_row(r0 + tid)] = zero ? -CUDART_INF_F : (M + log2f(W)) * kLn2;
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int e = tid * 4; e < nr * DP; e += NT * 4) {
+            const int rr = e / DP, d = e - rr * DP;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+            for (int c = 0; c < ncta; ++c) {
+                const float w = sWn[c * R + rr];
+                if (w != 0.f) {
+                    const float4 v = *reinterpret_cast<const float4 *>(rRows + ((size_t)c * per + rr) * DP + d);
+                    o.x = fmaf(w, v.x, o.x); o.y = fmaf(w, v.y, o.y); o.z = fmaf(w, v.z, o.z); o.w = fmaf(w, v.w, o.w);
+                }
+            }
+            store4(p.out + out_row(r0 + rr) * p.D + d, o);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();  // every TMEM read is done
+    if (warp == kWarpMma) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::kTmemCols)
                      : "memory");
     }
-    const int flags = sFlag[0];
-    if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
-    merge_rows<DP, 1, R, NT, false>(p, sg, g, row0, rows_here, flags, rank, ncta, sMo, sMm, sMl, sPm, sPl, sLse,
-                                    sAllM, sAllL, sAllF, sFlag, nullptr);
 }
 
 }  // namespace pkv
