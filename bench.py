@@ -141,7 +141,7 @@ def bench_config(world: int) -> dict:
 
 # ---------------------------------------------------------------- GPU arm
 
-def make_runner(pkv, L: int, seed: int, device, advance: bool = False, bucket: int = 0):
+def make_runner(pkv, L: int, seed: int, device, advance: bool = False, bucket: int = 0, flags: int = 0):
     import torch
 
     import workloads
@@ -149,7 +149,7 @@ def make_runner(pkv, L: int, seed: int, device, advance: bool = False, bucket: i
     bucket = bucket or pkv.bucket_for(L)
     w = workloads.sensenova(L, bucket, num_layers=LAYERS, seed=seed, device=device)
     cache = pkv.PagedKVCache(w.k, w.v, w.block_table, bucket=bucket)
-    step = DecodeStep(cache, HQ, advance=advance)
+    step = DecodeStep(cache, HQ, advance=advance, flags=flags)
     for layer in range(LAYERS):
         step.q[layer].copy_(w.q[layer])
         step.k_new[layer].copy_(w.k_new[layer])
@@ -248,7 +248,8 @@ CONFIGS = (
 )
 
 
-def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int = 50, warmup: int = 5, only=None):
+def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int = 50, warmup: int = 5, only=None,
+                 flags: int = 0):
     """The other workloads of the scope table, one fused append + attention
     call each (one launch), L2 flushed before every timed call: median µs,
     algorithmic GB/s and its fraction of the copy peak."""
@@ -268,7 +269,7 @@ def time_configs(pkv, device, flush, stream, peak: float, seed: int, reps: int =
 
         def call():
             pkv.append_attend(cache, 0, q, kn, vn, si, out, err, w.max_q_len, max_kv, w.scale, w.causal,
-                              w.window, stream=stream)
+                              w.window, stream=stream, flags=flags)
 
         for _ in range(warmup):
             flush()
@@ -433,7 +434,7 @@ def gpu_arm(args):
     peak, peak_kind = load_peaks()
 
     # Headline: KV length 8192.
-    runner, w = make_runner(pkv, HEADLINE_LEN, seed=rank, device=device)
+    runner, w = make_runner(pkv, HEADLINE_LEN, seed=rank, device=device, flags=args.flags)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -479,7 +480,7 @@ def gpu_arm(args):
     by_len = {}
     if not args.no_sweep:
         for L in SWEEP:
-            r, _ = make_runner(pkv, L, seed=rank, device=device)
+            r, _ = make_runner(pkv, L, seed=rank, device=device, flags=args.flags)
             t = time_steps(r, max(args.steps // 4, 20), args.warmup, flush, stream)
             m = reduce_max(statistics.median(t), world, device)
             gbs = algorithmic_bytes_per_layer(L) * LAYERS / (m * 1e-3) / 1e9
@@ -500,7 +501,7 @@ def gpu_arm(args):
 
     by_config = None
     if not args.no_sweep:
-        by_config = time_configs(pkv, device, flush, stream, peak, seed=rank)
+        by_config = time_configs(pkv, device, flush, stream, peak, seed=rank, flags=args.flags)
 
     traffic = None
     if os.path.exists(PROFILE):
@@ -545,12 +546,14 @@ def gpu_arm(args):
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
         }
+        if args.flags:
+            line["config"]["attention_flags"] = args.flags
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def config_only(key: str):
+def config_only(key: str, flags: int = 0):
     """One workload of the scope table, 3 + 3 calls, one JSON line (no
     headline): the command the profiler summaries capture."""
     import torch
@@ -562,8 +565,48 @@ def config_only(key: str):
     scratch = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     peak, _ = load_peaks()
     res = time_configs(pkv, device, lambda: scratch.fill_(1), torch.cuda.current_stream(), peak, seed=0, reps=3,
-                       warmup=3, only=key)
+                       warmup=3, only=key, flags=flags)
+    res[0]["flags"] = flags
     print(json.dumps(res[0]), flush=True)
+
+
+def decode_layer_only(L: int, flags: int = 0):
+    """One layer of the headline step (fused append + attention of one token,
+    GQA 32:8, D 128) at KV length L, 3 + 3 launches with L2 flushed before
+    each, one JSON line: the command the decode profiler summaries capture."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_decode_13_gb300 as pkv
+
+    import workloads
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    peak, _ = load_peaks()
+    bucket = pkv.bucket_for(L)
+    w = workloads.sensenova(L, bucket, num_layers=1, seed=0, device=device)
+    cache = pkv.PagedKVCache(w.k, w.v, w.block_table, bucket=bucket)
+    out = torch.empty(w.total_rows, w.q_heads, w.head_dim, device=device)
+    err = pkv.new_err_flags(device)
+    stream = torch.cuda.current_stream()
+    evs = []
+    for i in range(6):
+        scratch.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pkv.append_attend(cache, 0, w.q[0], w.k_new[0], w.v_new[0], w.seq_info, out, err, 1, L, w.scale, w.causal,
+                          w.window, stream=stream, flags=flags)
+        b.record(stream)
+        if i >= 3:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError(f"device error flags {int(err.item()):#x}")
+    ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+    gbs = algorithmic_bytes_per_layer(L) / (ms * 1e-3) / 1e9
+    print(json.dumps({"decode_layer": L, "flags": flags, "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                      "frac_of_peak": round(gbs / peak, 4)}), flush=True)
 
 
 # ---------------------------------------------------------------- reference arm (CPU oracle)
@@ -647,13 +690,19 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--config-only", choices=[c[0] for c in CONFIGS],
                     help="time only this workload's call (3 warm-up + 3 timed calls; for profiler runs)")
+    ap.add_argument("--decode-layer", type=int, default=0, metavar="L",
+                    help="time only one headline layer at KV length L (3 warm-up + 3 timed launches; for profiler runs)")
+    ap.add_argument("--flags", type=int, default=0,
+                    help="attention flags of every timed call (1: CUDA-core kernels, 8: mma.sync tile for wide groups)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         reference_arm(args)
     elif args.config_only:
-        config_only(args.config_only)
+        config_only(args.config_only, args.flags)
+    elif args.decode_layer:
+        decode_layer_only(args.decode_layer, args.flags)
     else:
         gpu_arm(args)
 

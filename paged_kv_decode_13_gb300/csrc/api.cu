@@ -97,13 +97,15 @@ AttnKernel pick(int variant, int dp, int rc) {
     return AttnKernel{nullptr, 0, 0, 0, 0, false, false};
 }
 
-// Largest cluster size <= want that the device can schedule for this kernel
-// (1 when no device answers the query).
-int schedulable_cluster(const AttnKernel &k, int want) {
+// Clusters of c CTAs of this kernel that the device holds at once (c = 1:
+// resident CTAs); cached per kernel and size, 0 when none fits or no device
+// answers the query.
+int active_clusters(const AttnKernel &k, int c) {
     static std::mutex mu;
     static const void *fns[64];
-    static int best[64][kMaxCluster + 1];
+    static int count[64][kMaxCluster + 1];
     static int n = 0;
+    if (c < 1 || c > kMaxCluster) return 0;
     std::lock_guard<std::mutex> lock(mu);
     int slot = -1;
     for (int i = 0; i < n; ++i)
@@ -111,13 +113,18 @@ int schedulable_cluster(const AttnKernel &k, int want) {
     if (slot < 0 && n < 64) {
         slot = n++;
         fns[slot] = k.fn;
-        for (int c = 0; c <= kMaxCluster; ++c) best[slot][c] = -1;
+        for (int i = 0; i <= kMaxCluster; ++i) count[slot][i] = -1;
     }
-    for (int c = want; c > 1; --c) {
-        if (slot >= 0 && best[slot][c] >= 0) {
-            if (best[slot][c] > 0) return c;
-            continue;
+    if (slot >= 0 && count[slot][c] >= 0) return count[slot][c];
+    int clusters = 0;
+    if (c == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, k.threads, k.smem) != cudaSuccess) {
+            cudaGetLastError();
+            per_sm = 0;
         }
+        clusters = per_sm * device_sms();
+    } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)c, 1, 1);
         cfg.blockDim = dim3((unsigned)k.threads);
@@ -129,15 +136,52 @@ int schedulable_cluster(const AttnKernel &k, int want) {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, k.fn, &cfg) != cudaSuccess) {
             cudaGetLastError();
             clusters = 0;
         }
-        if (slot >= 0) best[slot][c] = clusters > 0 ? 1 : 0;
-        if (clusters > 0) return c;
     }
+    clusters = std::max(clusters, 0);
+    if (slot >= 0) count[slot][c] = clusters;
+    return clusters;
+}
+
+// Largest cluster size <= want that the device can schedule for this kernel
+// (1 when no device answers the query).
+int schedulable_cluster(const AttnKernel &k, int want) {
+    for (int c = want; c > 1; --c)
+        if (active_clusters(k, c) > 0) return c;
     return 1;
+}
+
+// Automatic split count of a kernel that fits once per SM.  A key range's
+// CTAs form one cluster, and clusters only start where a GPC has that many
+// free SMs, so a large cluster size can leave part of the units for a second
+// or third wave (16-CTA clusters: seven at a time on GB300's 152 SMs).  The
+// time of a launch goes about as waves / cluster size, waves = units over the
+// clusters held at once; take the size at or below `want` that minimises it,
+// and of equal ones the size with fewer waves (each wave repeats the ramp-up
+// and the merge).  Kernels that fit twice per SM keep `want`: there the
+// second slot holds the next layer's CTAs (programmatic launch), which the
+// wave count does not see.
+int wave_cluster(const AttnKernel &k, long long units, int want) {
+    if (want <= 1 || units <= 0 || active_clusters(k, 1) > device_sms()) return want;
+    auto waves = [&](int c) {
+        const long long a = active_clusters(k, c);
+        return a > 0 ? (units + a - 1) / a : (long long)1 << 40;
+    };
+    int best = want;
+    long long best_w = waves(want);
+    for (int c = want - 1; c >= 1; --c) {
+        const long long w = waves(c);
+        // w / c against best_w / best, exactly
+        const long long lhs = w * best, rhs = best_w * c;
+        if (lhs < rhs || (lhs == rhs && w < best_w)) {
+            best = c;
+            best_w = w;
+        }
+    }
+    return best;
 }
 
 int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv, int num_splits,
@@ -154,13 +198,14 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
     const long long rows_max = (long long)pl->G * max_q_len;
     if (rows_max > (1 << 20)) return PKV_EINVAL;
     pl->rows_max = (int)rows_max;
-    // Groups of at most 8 rows take the decode kernel (rows as the MMA's N side).
-    // Long buckets take the decode configuration with more warps (class 5).
+    // bf16 groups of at most 8 rows take the decode kernel (rows as the MMA's
+    // N side; with PKV_FLAG_SIMT its CUDA-core variant).  Long buckets take
+    // the decode configuration with more warps (class 5).
     const long long max_pages0 = (max_kv + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE + 1;
     // Wider bf16 groups with head_dim 128 take the tcgen05 tile (class 6)
     // unless the caller asks for the mma.sync one.
     const bool tc = variant == kMmaBf16 && rows_max > 8 && D == 128 && !(flags & PKV_FLAG_MMA_SYNC);
-    const int rc = (variant == kMmaBf16 && rows_max <= 8) ? (max_pages0 > 256 ? 5 : 4)
+    const int rc = (variant != kSimtF32 && rows_max <= 8) ? (max_pages0 > 256 ? 5 : 4)
                    : tc ? 6
                    : rows_max <= 16 ? 0 : rows_max <= 32 ? 1 : rows_max <= 64 ? 2 : 3;
     pl->k = pick(variant, dp, rc);
@@ -310,7 +355,8 @@ int attend_common(const pkv_cache *c, int layer, const void *q, const void *k_ne
     const WsLayout wl = ws_layout((long long)S * c->kv_heads * pl.row_tiles, pl.ncta, pl.k.dp);
     if (gm && workspace_bytes < (long long)wl.total) return PKV_EINVAL;
     if ((st = prepare_kernel(pl.k))) return st;
-    const int ncta = S == 0 ? 1 : pl.gm ? pl.ncta : schedulable_cluster(pl.k, pl.ncta);
+    int ncta = S == 0 ? 1 : pl.gm ? pl.ncta : schedulable_cluster(pl.k, pl.ncta);
+    if (S > 0 && !pl.gm && num_splits == 0) ncta = wave_cluster(pl.k, pl.units, ncta);
 
     AttendParams p;
     // bf16 page tiles come in one box when head_dim fills its padded width

@@ -30,12 +30,13 @@ static AttnKernel info() {
 }
 
 // Decode kernel for groups of at most 8 query rows (row class 4; class 5 for
-// long buckets, with more warps where head_dim 128 allows).
+// long buckets, with more warps where head_dim 128 allows).  The CUDA-core
+// variant keeps the tensor-core one's warps and stages.
 template <class C>
 static AttnKernel dinfo() {
     static_assert(C::kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
     return AttnKernel{reinterpret_cast<const void *>(&decode_kernel<C>), C::kThreads, C::kSmemBytes,
-                      C::kRows, C::DP, true};
+                      C::kRows, C::DP, !C::SIMT};
 }
 
 // tcgen05 tile for wide bf16 groups with head_dim 128 (row class 6).
@@ -84,6 +85,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
 #elif PKV_INST_VARIANT == 1
 #if PKV_INST_DP == 64
     {
+        if (rc >= 4) return dinfo<DecCfg<64, 4, 6, true>>();
         if (rc == 0) return CFG(B16, 1, 4, 4, false);
         if (rc == 1) return CFG(B16, 2, 2, 4, false);
         if (rc == 2) return CFG(B16, 4, 1, 4, false);
@@ -91,6 +93,8 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #elif PKV_INST_DP == 128
     {
+        if (rc == 5) return dinfo<DecCfg<128, 6, 2, true>>();
+        if (rc == 4) return dinfo<DecCfg<128, 4, 3, true>>();
         if (rc == 0) return CFG(B16, 1, 4, 3, false);
         if (rc == 1) return CFG(B16, 2, 2, 4, false);
         if (rc == 2) return CFG(B16, 4, 1, 4, false);
@@ -98,6 +102,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #else
     {
+        if (rc >= 4) return dinfo<DecCfg<256, 4, 2, true>>();
         if (rc == 0) return CFG(B16, 1, 4, 2, false);
         if (rc == 1) return CFG(B16, 2, 2, 3, false);
         return CFG(B16, 4, 1, 4, false);

@@ -39,10 +39,11 @@ constexpr int kSoloPages = 3;
 // stay at most 2^8, well inside fp32 and with bf16's relative precision.
 constexpr float kLazyLog2 = 8.f;
 
-template <int DP_, int KW_, int NST_>
+template <int DP_, int KW_, int NST_, bool SIMT_ = false>
 struct DecCfg {
     using T = __nv_bfloat16;
     static constexpr int DP = DP_;      // head_dim rounded up to 64 / 128 / 256
+    static constexpr bool SIMT = SIMT_; // dot products on the CUDA cores (fp32 FMA) instead of mma.sync
     static constexpr int KW = KW_;      // warps = key groups
     static constexpr int NST = NST_;    // page stages per warp
     static constexpr int kThreads = KW * 32;
@@ -66,8 +67,14 @@ struct DecCfg {
     static constexpr size_t kBarBytes = (size_t)KW * NST * 8;
     static constexpr size_t kFlagBytes = 32 * 4;
     static constexpr size_t kCovBytes = (size_t)kThreads * 4;
+    // CUDA-core variant: each lane owns kE consecutive head_dim columns; a
+    // warp's page weights P go through shared memory, [row][token] with rows
+    // padded to kPLd floats (conflict-free stores, 16-byte aligned rows).
+    static constexpr int kE = DP / 32;
+    static constexpr int kPLd = kPage + 4;
+    static constexpr size_t kPBytes = SIMT ? 16 + (size_t)KW * kRows * kPLd * 4 : 0;
     static constexpr size_t kSmemBytes =
-        1024 + kPipeBytes + kRecvBytes + kStatBytes + kBarBytes + kFlagBytes + kCovBytes + kWnBytes;
+        1024 + kPipeBytes + kRecvBytes + kStatBytes + kBarBytes + kFlagBytes + kCovBytes + kWnBytes + kPBytes;
     // L2 warm-up before the dependency wait: each warp prefetches up to
     // kL2Pages pages past its stages, about 512 KB per SM over the CTAs that
     // fit on one (at most 32 pages: the page-id window of a warp).
@@ -120,6 +127,10 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     int *sAllF = sFlag + 1;                                 // [16] flags of the cluster
     int *sCov = sFlag + 32;                                 // [NT] coverage flags of the first rows
     float *sWn = reinterpret_cast<float *>(sCov + NT);      // [8][16] normalised cluster merge weights
+    // CUDA-core variant: this warp's page weights, [8 rows][kPLd]
+    float *sP = reinterpret_cast<float *>(
+                    (reinterpret_cast<uintptr_t>(sWn + C::kRows * 16 + C::kRows) + 15) & ~uintptr_t(15)) +
+                (threadIdx.x >> 5) * C::kRows * C::kPLd;
 
     const int tid = threadIdx.x, kw = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
@@ -372,9 +383,23 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     pdl_wait();
     pdl_trigger();
 
-    // ---- after the wait: Q^T fragments, this step's new rows, row bounds
+    // ---- after the wait: Q^T fragments (CUDA-core variant: this lane's
+    // columns of every row in fp32), this step's new rows, row bounds
+    constexpr bool SIMT = C::SIMT;
+    constexpr int E = C::kE;
     unsigned qb[KT][2];
-    {
+    float qs[SIMT ? C::kRows : 1][E];
+    if constexpr (SIMT) {
+#pragma unroll
+        for (int n = 0; n < C::kRows; ++n) {
+            const int i = n / p.G, jh = n - i * p.G, col = lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) qs[n][e] = 0.f;
+            if (n < rows_unit && col < p.D)
+                load_f32<T, E>(qs[n], reinterpret_cast<const T *>(p.q) +
+                                          (((long long)sg.q0 + i) * p.Hq + (long long)g * p.G + jh) * p.D + col);
+        }
+    } else {
         const bool real = gq < rows_unit;
         const int i = gq / p.G, jh = gq - i * p.G;
         const T *qrow = reinterpret_cast<const T *>(p.q) +
@@ -412,6 +437,10 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         if (n < rows_unit)
             row_key_bounds(new_start + n / p.G, kend, p.causal, p.window, first, lo_r[e], hi_r[e]);
     }
+    // CUDA-core variant: a lane's scores are those of row lane / 4.
+    const int rs = lane >> 2;
+    int lo_s = 0, hi_s = 0;
+    if (SIMT && rs < rows_unit) row_key_bounds(new_start + rs / p.G, kend, p.causal, p.window, first, lo_s, hi_s);
     if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
     #pragma unroll 1
     for (; issued < NST && issued < n_mine; ++issued) issue(issued);
@@ -421,6 +450,13 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
 #pragma unroll
     for (int dt = 0; dt < KT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
     float m_r[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_r[2] = {0.f, 0.f};
+    // CUDA-core variant: O rows x this lane's columns; (max, sum) of row rs
+    float acs[SIMT ? C::kRows : 1][E];
+#pragma unroll
+    for (int n = 0; n < (SIMT ? C::kRows : 1); ++n)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acs[n][e] = 0.f;
+    float m_s = -CUDART_INF_F, l_s = 0.f;
     const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), kchk = lane >> 4;
     const int vrow = (lane & 7) + ((lane >> 4) << 3), vchk = (lane >> 3) & 1;
 
@@ -471,62 +507,140 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
         const int pos0 = (cb0 + kw + j * KW) * kPage;
         wait_page(j);
         fix_page(j, st, pos0);
-        // S^T = K . Q^T, two accumulation chains over head_dim.
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (SIMT) {
+            // Scores of 4 keys at a time: each lane sums its columns for
+            // every (row, key) slot, then a reduce-scatter across the warp
+            // leaves slot `lane` = (row lane / 4, key lane % 4) with lane.
+            float sc[4];
 #pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-            unsigned a[4];
-            ldmatrix_x4(a, st + swz(krow, 2 * kk + kchk));
-            if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
-            else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
-        }
-        // This thread holds keys gq, gq + 8 of rows 2tq, 2tq + 1: mask, online softmax (base 2).
-        const int p0 = pos0 + gq, p1 = p0 + 8;
-        float v[4];
-        v[0] = (p0 >= lo_r[0] && p0 < hi_r[0]) ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
-        v[1] = (p0 >= lo_r[1] && p0 < hi_r[1]) ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
-        v[2] = (p1 >= lo_r[0] && p1 < hi_r[0]) ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
-        v[3] = (p1 >= lo_r[1] && p1 < hi_r[1]) ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
-        // Lazy running maximum: a row's reference max moves only when a score
-        // exceeds it by more than kLazyLog2, so the weights stay below
-        // 2^kLazyLog2 and the common page needs no cross-lane reduction and
-        // no rescale.  (m, l, acc) stay consistent with whatever reference
-        // the row holds, which is all the merges need.
-        float mx0 = fmaxf(v[0], v[2]), mx1 = fmaxf(v[1], v[3]);
-        if (__any_sync(0xffffffffu, mx0 > m_r[0] + kLazyLog2 || mx1 > m_r[1] + kLazyLog2)) {
+            for (int tg = 0; tg < 4; ++tg) {
+                float x[32];
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                for (int i = 0; i < 32; ++i) x[i] = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float kf[E];
+                    tile_load<T, E>(kf, st, tg * 4 + u, lane * E);
+#pragma unroll
+                    for (int n = 0; n < C::kRows; ++n)
+#pragma unroll
+                        for (int e = 0; e < E; ++e) x[n * 4 + u] = fmaf(qs[n][e], kf[e], x[n * 4 + u]);
+                }
+#pragma unroll
+                for (int h = 16; h >= 1; h >>= 1) {
+                    const bool upper = (lane & h) != 0;
+#pragma unroll
+                    for (int e = 0; e < h; ++e) {
+                        const float send = upper ? x[e] : x[e + h];
+                        const float keep = upper ? x[e + h] : x[e];
+                        x[e] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+                    }
+                }
+                const int pos = pos0 + tg * 4 + (lane & 3);
+                sc[tg] = (pos >= lo_s && pos < hi_s) ? x[0] * p.scale_log2 : -CUDART_INF_F;
             }
-            const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
-            const float al0 = mn0 == -CUDART_INF_F ? 1.f : exp2f(m_r[0] - mn0);
-            const float al1 = mn1 == -CUDART_INF_F ? 1.f : exp2f(m_r[1] - mn1);
-            m_r[0] = mn0;
-            m_r[1] = mn1;
-            l_r[0] *= al0;
-            l_r[1] *= al1;
+            // Lazy running maximum of row rs (its 4 lanes), as in the tensor-core path.
+            float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            if (__any_sync(0xffffffffu, mx > m_s + kLazyLog2)) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float mn = fmaxf(m_s, mx);
+                const float al = mn == -CUDART_INF_F ? 1.f : exp2f(m_s - mn);
+                m_s = mn;
+                l_s *= al;
 #pragma unroll
+                for (int n = 0; n < C::kRows; ++n) {
+                    const float a = __shfl_sync(0xffffffffu, al, n * 4);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acs[n][e] *= a;
+                }
+            }
+            const float mu = m_s == -CUDART_INF_F ? 0.f : m_s;
+#pragma unroll
+            for (int tg = 0; tg < 4; ++tg) {
+                const float pw = exp2f(sc[tg] - mu);
+                l_s += pw;
+                sP[rs * C::kPLd + tg * 4 + (lane & 3)] = pw;
+            }
+            __syncwarp();
+            // O += P V over this lane's columns.
+            const unsigned char *sv = st + C::kTileBytes;
+#pragma unroll
+            for (int tg = 0; tg < 4; ++tg) {
+                float4 pr[C::kRows];
+#pragma unroll
+                for (int n = 0; n < C::kRows; ++n)
+                    pr[n] = *reinterpret_cast<const float4 *>(sP + n * C::kPLd + tg * 4);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float vf[E];
+                    tile_load<T, E>(vf, sv, tg * 4 + u, lane * E);
+#pragma unroll
+                    for (int n = 0; n < C::kRows; ++n) {
+                        const float pw = u == 0 ? pr[n].x : u == 1 ? pr[n].y : u == 2 ? pr[n].z : pr[n].w;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acs[n][e] = fmaf(pw, vf[e], acs[n][e]);
+                    }
+                }
+            }
+        } else {
+            // S^T = K . Q^T, two accumulation chains over head_dim.
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                unsigned a[4];
+                ldmatrix_x4(a, st + swz(krow, 2 * kk + kchk));
+                if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
+                else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
+            }
+            // This thread holds keys gq, gq + 8 of rows 2tq, 2tq + 1: mask, online softmax (base 2).
+            const int p0 = pos0 + gq, p1 = p0 + 8;
+            float v[4];
+            v[0] = (p0 >= lo_r[0] && p0 < hi_r[0]) ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
+            v[1] = (p0 >= lo_r[1] && p0 < hi_r[1]) ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
+            v[2] = (p1 >= lo_r[0] && p1 < hi_r[0]) ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
+            v[3] = (p1 >= lo_r[1] && p1 < hi_r[1]) ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
+            // Lazy running maximum: a row's reference max moves only when a score
+            // exceeds it by more than kLazyLog2, so the weights stay below
+            // 2^kLazyLog2 and the common page needs no cross-lane reduction and
+            // no rescale.  (m, l, acc) stay consistent with whatever reference
+            // the row holds, which is all the merges need.
+            float mx0 = fmaxf(v[0], v[2]), mx1 = fmaxf(v[1], v[3]);
+            if (__any_sync(0xffffffffu, mx0 > m_r[0] + kLazyLog2 || mx1 > m_r[1] + kLazyLog2)) {
+    #pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
+                const float al0 = mn0 == -CUDART_INF_F ? 1.f : exp2f(m_r[0] - mn0);
+                const float al1 = mn1 == -CUDART_INF_F ? 1.f : exp2f(m_r[1] - mn1);
+                m_r[0] = mn0;
+                m_r[1] = mn1;
+                l_r[0] *= al0;
+                l_r[1] *= al1;
+    #pragma unroll
+                for (int dt = 0; dt < KT; ++dt) {
+                    acc[dt][0] *= al0; acc[dt][1] *= al1;
+                    acc[dt][2] *= al0; acc[dt][3] *= al1;
+                }
+            }
+            const float mu0 = m_r[0] == -CUDART_INF_F ? 0.f : m_r[0], mu1 = m_r[1] == -CUDART_INF_F ? 0.f : m_r[1];
+            const float p00 = exp2f(v[0] - mu0), p01 = exp2f(v[1] - mu1);
+            const float p10 = exp2f(v[2] - mu0), p11 = exp2f(v[3] - mu1);
+            l_r[0] += p00 + p10;
+            l_r[1] += p01 + p11;
+            // P^T as B fragments: transpose the (key x row) halves in registers.
+            const unsigned b0 = movmatrix_trans(pack_bf16x2(p00, p01));
+            const unsigned b1 = movmatrix_trans(pack_bf16x2(p10, p11));
+            // O^T += V^T . P^T, one independent MMA per 16 columns of head_dim.
+            const unsigned char *sv = st + C::kTileBytes;
+    #pragma unroll
             for (int dt = 0; dt < KT; ++dt) {
-                acc[dt][0] *= al0; acc[dt][1] *= al1;
-                acc[dt][2] *= al0; acc[dt][3] *= al1;
+                unsigned a[4];
+                ldmatrix_x4_trans(a, sv + swz(vrow, 2 * dt + vchk));
+                mma_bf16_16816(acc[dt], a, b0, b1);
             }
-        }
-        const float mu0 = m_r[0] == -CUDART_INF_F ? 0.f : m_r[0], mu1 = m_r[1] == -CUDART_INF_F ? 0.f : m_r[1];
-        const float p00 = exp2f(v[0] - mu0), p01 = exp2f(v[1] - mu1);
-        const float p10 = exp2f(v[2] - mu0), p11 = exp2f(v[3] - mu1);
-        l_r[0] += p00 + p10;
-        l_r[1] += p01 + p11;
-        // P^T as B fragments: transpose the (key x row) halves in registers.
-        const unsigned b0 = movmatrix_trans(pack_bf16x2(p00, p01));
-        const unsigned b1 = movmatrix_trans(pack_bf16x2(p10, p11));
-        // O^T += V^T . P^T, one independent MMA per 16 columns of head_dim.
-        const unsigned char *sv = st + C::kTileBytes;
-#pragma unroll
-        for (int dt = 0; dt < KT; ++dt) {
-            unsigned a[4];
-            ldmatrix_x4_trans(a, sv + swz(vrow, 2 * dt + vchk));
-            mma_bf16_16816(acc[dt], a, b0, b1);
         }
         __syncwarp();  // every lane is done with the stage
         if (j + NST < n_mine) issue(j + NST);
@@ -543,12 +657,25 @@ __global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_con
     if ((bad || timed_out) && lane == 0) atomicOr(sFlag, (bad ? 1 : 0) | (timed_out ? 2 : 0));
 
     // ---- the warp's partial, written over its own stages: O^T as [row][col], max and sum per row
+    if constexpr (SIMT) {
+        l_s += __shfl_xor_sync(0xffffffffu, l_s, 1);
+        l_s += __shfl_xor_sync(0xffffffffu, l_s, 2);
+        float *part = reinterpret_cast<float *>(wstage);
+        float *pm = part + C::kRows * LD, *pl = pm + C::kRows;
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], o);
-        l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], o);
-    }
-    {
+        for (int n = 0; n < C::kRows; ++n)
+#pragma unroll
+            for (int e = 0; e < E; ++e) part[n * LD + lane * E + e] = acs[n][e];
+        if ((lane & 3) == 0) {
+            pm[rs] = m_s;
+            pl[rs] = l_s;
+        }
+    } else {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], o);
+            l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], o);
+        }
         float *part = reinterpret_cast<float *>(wstage);
         float *pm = part + C::kRows * LD, *pl = pm + C::kRows;
 #pragma unroll

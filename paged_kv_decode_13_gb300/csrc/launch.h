@@ -21,8 +21,8 @@ enum Variant { kMmaBf16 = 0, kSimtBf16 = 1, kSimtF32 = 2 };
 
 // Row class: 0 for <= 16 query rows per (segment, kv head), 1 for <= 32,
 // 2 for <= 64, 3 for more (128 per CTA, extra CTAs along the rows beyond);
-// 4 for <= 8 rows on the tensor-core path (decode_kernel), 5 the same for
-// buckets over 256 pages; 6 for more than 8 rows on the tcgen05 tile
+// 4 for <= 8 bf16 rows (decode_kernel, tensor-core or CUDA-core variant), 5
+// the same for buckets over 256 pages; 6 for more than 8 rows on the tcgen05 tile
 // (verify_kernel, bf16 with head_dim 128: 128 rows per CTA).
 #define PKV_DECLARE_PICK(V, DP) AttnKernel pick_##V##_##DP(int row_class);
 PKV_DECLARE_PICK(0, 64)

@@ -33,8 +33,9 @@
 //               head_dim) and, once P(j-1) is in TMEM, O += P(j-1) V(j-1)
 //               (M = 128, N = 128, A = P from TMEM, 4 steps of 16 keys); also
 //               owns the TMEM allocation.
-// TMEM (512 columns): S / P double-buffered in 0-63 / 64-127 (P as bf16
-// pairs in the first 32 columns of its buffer), O in 128-255, Q in 256-319.
+// TMEM (512 columns): S / P in NB = 2 buffers of 64 columns from column 0
+// (P as bf16 pairs in the first 32 columns of its buffer), then O (128
+// columns) and Q (64).  A third buffer measured no faster: the loads bound.
 // Shared memory holds only the K and V stages, so 13 stages (208 KB) of
 // loads are in flight.
 //
@@ -73,8 +74,9 @@ struct VfyCfg {
     static constexpr size_t kBodyBytes = kLoopBytes > kRecvBytes ? kLoopBytes : kRecvBytes;
     // merge weights [16][rows], cluster flags [16], row max exchange [2][8 warps][32], row sums [2][rows]
     static constexpr size_t kWnBytes = (size_t)16 * kRows * 4 + 16 * 4 + 2 * 8 * 32 * 4 + 2 * kRows * 4;
-    // K, V full / empty; s_full, p_full, pv_done [2]; drain; row-pair exchange [4 quadrants][2]
-    static constexpr int kBars = 2 * NK + 2 * NV + 7 + 8;
+    static constexpr int NB = 2;                    // S / P buffers in TMEM
+    // K, V full / empty; s_full, p_full, pv_done [NB]; drain; row-pair exchange [4 quadrants][2]
+    static constexpr int kBars = 2 * NK + 2 * NV + 3 * NB + 1 + 8;
     static constexpr size_t kMiscBytes = (size_t)kBars * 8 + 16 + 32 * 4 + (size_t)kThreads * 4;
     static constexpr size_t kSmemBytes = 1024 + kBodyBytes + kWnBytes + kMiscBytes;
     static constexpr int kTmemCols = 512;
@@ -200,7 +202,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     constexpr int EPC = 8;  // bf16 per 16-byte chunk
     constexpr float kLn2 = 0.6931471805599453f;
     constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
-    constexpr unsigned kColO = 128, kColQ = 256;
+    constexpr int NB = C::NB;
+    constexpr unsigned kColO = 64 * NB, kColQ = kColO + 128;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *body = reinterpret_cast<unsigned char *>(
@@ -213,8 +216,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     float *sXl = sXm + 2 * 8 * 32;                                 // [2][R] row sums of each half
     uint64_t *bars = reinterpret_cast<uint64_t *>(sXl + 2 * R);
     uint64_t *k_full = bars, *k_empty = bars + NK, *v_full = bars + 2 * NK, *v_empty = v_full + NV;
-    uint64_t *s_full = v_empty + NV, *p_full = s_full + 2, *pv_done = p_full + 2;
-    uint64_t *drain = pv_done + 2;
+    uint64_t *s_full = v_empty + NV, *p_full = s_full + NB, *pv_done = p_full + NB;
+    uint64_t *drain = pv_done + NB;
     uint64_t *pair = drain + 1;                                    // [4][2]: the two warps of a row quadrant
     unsigned *tslot = reinterpret_cast<unsigned *>(bars + C::kBars);
     volatile int *sAbort = reinterpret_cast<volatile int *>(tslot + 1);
@@ -279,8 +282,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     if (tid == 0) {
         #pragma unroll 1
         for (int i = 0; i < C::kBars; ++i) {
-            const bool eight = i >= 2 * NK + 2 * NV + 2 && i < 2 * NK + 2 * NV + 4;  // p_full: every softmax warp
-            const bool two = i >= 2 * NK + 2 * NV + 7;                            // pair: both warps of a quadrant
+            const bool eight = i >= 2 * NK + 2 * NV + NB && i < 2 * NK + 2 * NV + 2 * NB;  // p_full: every softmax warp
+            const bool two = i >= 2 * NK + 2 * NV + 3 * NB + 1;                         // pair: both warps of a quadrant
             mbar_init(bars + i, eight ? 8 : two ? 2 : 1);
         }
         fence_barrier_init();
@@ -538,11 +541,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             __syncwarp();
         };
         auto issue_pv = [&](int i) {
-            const int b = i & 1, vs = i % NV;
+            const int b = i % NB, vs = i % NV;
             unsigned char *stage = sV + (size_t)vs * C::kVStage;
             if (!wait_bar(v_full + vs, (i / NV) & 1)) return false;
             fix_v(i, stage);
-            if (!wait_bar(p_full + b, (i >> 1) & 1)) return false;
+            if (!wait_bar(p_full + b, (i / NB) & 1)) return false;
             tc_fence_after();
             if (lane == 0) {
                 const unsigned v_addr = smem_u32(stage);
@@ -558,12 +561,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         };
         #pragma unroll 1
         for (int j = 0; j < ngr && !timed_out; ++j) {
-            const int ks = j % NK, b = j & 1;
+            const int ks = j % NK, b = j % NB;
             unsigned char *stage = sK + (size_t)ks * C::kKStage;
             if (!wait_bar(k_full + ks, (j / NK) & 1)) { timed_out = true; break; }
             fix_k(j, stage);
-            // S(j) overwrites buffer b, which P V(j - 2) reads P(j - 2) from.
-            if (j >= 2 && !wait_bar(pv_done + b, ((j - 2) >> 1) & 1)) { timed_out = true; break; }
+            // S(j) overwrites buffer b, which P V(j - NB) reads P(j - NB) from.
+            if (j >= NB && !wait_bar(pv_done + b, ((j - NB) / NB) & 1)) { timed_out = true; break; }
             tc_fence_after();
             if (lane == 0) {
                 const unsigned k_addr = smem_u32(stage);
@@ -592,8 +595,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         hi_r = min(hi_r, hi_pos);
         #pragma unroll 1
         for (int j = 0; j < ngr; ++j) {
-            const int b = j & 1;
-            if (!wait_bar(s_full + b, (j >> 1) & 1)) { timed_out = true; break; }
+            const int b = j % NB, xb = j & 1;  // S / P buffer, row-pair exchange buffer
+            if (!wait_bar(s_full + b, (j / NB) & 1)) { timed_out = true; break; }
             tc_fence_after();
             float x[32];
             tmem_ld32(tmem + lane_off + b * 64 + half * 32, x);
@@ -609,13 +612,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             // exchange: a buffer is rewritten only after the partner has
             // passed the next exchange).  The pair's barrier also orders this
             // half's read of S before the other half writes P over it.
-            sXm[(b * 8 + warp) * 32 + lane] = mx;
+            sXm[(xb * 8 + warp) * 32 + lane] = mx;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pair + quad * 2 + b);
-            if (!wait_bar(pair + quad * 2 + b, (j >> 1) & 1)) { timed_out = true; break; }
+            if (lane == 0) mbar_arrive(pair + quad * 2 + xb);
+            if (!wait_bar(pair + quad * 2 + xb, (j >> 1) & 1)) { timed_out = true; break; }
             tc_fence_after();
-            mx = fmaxf(mx, sXm[(b * 8 + (warp ^ 4)) * 32 + lane]);
+            mx = fmaxf(mx, sXm[(xb * 8 + (warp ^ 4)) * 32 + lane]);
             // Lazy reference maximum: raised only when a score passes it by 2^8.
             const bool grow = mx > m + 8.f;
             if (__any_sync(0xffffffffu, grow)) {
@@ -624,7 +627,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
                 if (j > 0 && __any_sync(0xffffffffu, grow && m != -CUDART_INF_F)) {
                     // O holds P V up to group j - 1 against the old reference:
                     // wait for that product, then rescale this half's columns.
-                    if (!wait_bar(pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1)) { timed_out = true; break; }
+                    if (!wait_bar(pv_done + ((j - 1) % NB), ((j - 1) / NB) & 1)) { timed_out = true; break; }
                     tc_fence_after();
 #pragma unroll 1
                     for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -653,7 +656,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             if (lane == 0) mbar_arrive(p_full + b);
         }
         // the last product has landed before O is read back
-        if (!timed_out && ngr > 0 && !wait_bar(pv_done + ((ngr - 1) & 1), ((ngr - 1) >> 1) & 1)) timed_out = true;
+        if (!timed_out && ngr > 0 && !wait_bar(pv_done + ((ngr - 1) % NB), ((ngr - 1) / NB) & 1)) timed_out = true;
         timed_out = __any_sync(0xffffffffu, timed_out);
         sXl[half * R + r] = timed_out ? 0.f : l;
     }

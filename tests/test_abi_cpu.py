@@ -160,8 +160,11 @@ def test_workspace_size_query(lib):
     assert L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 1, 0) == 0
     # 16 query rows per kv head: the wide kernel, which merges in the cluster
     assert L.pkv_attend_workspace_bytes(ref, 8, 1, 4, 512, 0, 0) == 0
-    # the CUDA-core path never uses one
-    assert L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 0, 1) == 0
+    # the CUDA-core variant of the decode kernel merges the same way
+    assert L.pkv_attend_workspace_bytes(ref, 8, 1, 1, 512, 0, 1) == n
+    # the fp32 tile never uses one
+    f, keep32 = _desc(lib, dtype=lib.F32)
+    assert L.pkv_attend_workspace_bytes(ctypes.byref(f), 8, 1, 1, 512, 0, 0) == 0
     assert L.pkv_attend_workspace_bytes(ref, 3, 1, 1, 512, 0, 0) == -1
 
 

@@ -309,6 +309,41 @@ def test_long_ranges_per_cta(pkv, q_heads, max_q, flags, num_splits):
     check_against_oracle(w, 0, out, lse, cache)
 
 
+def _simt_workload(kind):
+    if kind == "single_1000":
+        return U.nan_tails(workloads.sensenova(1000, 1024, num_layers=1, seed=81))
+    if kind == "single_4099":
+        return U.nan_tails(workloads.sensenova(4099, 8192, num_layers=1, seed=82))
+    if kind == "batched_d64":
+        return U.nan_tails(workloads.batched(S=8, max_len=2000, seed=83, q_heads=16, kv_heads=2, head_dim=64))
+    if kind == "batched_d96":  # head_dim below its padded width: zero-filled columns
+        return U.nan_tails(workloads.batched(S=5, max_len=1500, seed=84, q_heads=8, kv_heads=1, head_dim=96))
+    if kind == "window_d128":
+        w = U.nan_tails(workloads.batched(S=6, max_len=3000, seed=85, kv_heads=8, q_heads=32, min_len=100))
+        w.causal, w.window = True, 180
+        return w
+    if kind == "two_rows":  # q_len 2 x 4 heads: 8 rows per kv head, causal inside the step
+        return U.nan_tails(workloads.spec_verify(S=6, max_q=2, len_lo=1, len_hi=3000, causal=True, seed=86,
+                                                 q_heads=32))
+    return U.nan_tails(workloads.long_context(S=3, kv_len=20000, window=1000, ring_rows=1024, seed=87, num_layers=1,
+                                              q_heads=32, kv_heads=4, head_dim=256))
+
+
+@pytest.mark.parametrize("kind", ["single_1000", "single_4099", "batched_d64", "batched_d96", "window_d128",
+                                  "two_rows", "ring_d256"])
+@pytest.mark.parametrize("workspace", [False, True])
+def test_cuda_core_decode_variant(pkv, kind, workspace):
+    # PKV_FLAG_SIMT with at most 8 rows per kv head: the decode kernel with
+    # fp32 FMA dot products, merging its splits in the cluster or through the
+    # workspace, at head_dim 64 / 96 / 128 / 256
+    w = _simt_workload(kind)
+    mk = int(w.seq_info[:, 3].max())
+    out, lse, err, cache = run(pkv, w, max_kv=mk, flags=pkv.FLAG_SIMT, workspace=workspace)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
 def test_fused_equals_two_calls_bitwise(pkv):
     w = U.nan_tails(workloads.spec_verify(S=5, max_q=8, len_lo=100, len_hi=900, seed=11, q_heads=16))
     a, la, ea, ca = run(pkv, w, fused=True, max_kv=900)
