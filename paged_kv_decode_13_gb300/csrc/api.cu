@@ -161,11 +161,15 @@ int schedulable_cluster(const AttnKernel &k, int want) {
 // time of a launch goes about as waves / cluster size, waves = units over the
 // clusters held at once; take the size at or below `want` that minimises it,
 // and of equal ones the size with fewer waves (each wave repeats the ramp-up
-// and the merge).  Kernels that fit twice per SM keep `want`: there the
-// second slot holds the next layer's CTAs (programmatic launch), which the
-// wave count does not see.
+// and the merge).  The waves run in lock step only when there are few units
+// (at most half the resident CTAs), each split across many CTAs; with more
+// units of uneven length the split balances the long ranges instead, so
+// those launches keep `want`.  Kernels that fit twice per SM keep it too:
+// there the second slot holds the next layer's CTAs (programmatic launch),
+// which the wave count does not see.
 int wave_cluster(const AttnKernel &k, long long units, int want) {
-    if (want <= 1 || units <= 0 || active_clusters(k, 1) > device_sms()) return want;
+    const int resident = active_clusters(k, 1);
+    if (want <= 1 || units <= 0 || resident > device_sms() || 2 * units > resident) return want;
     auto waves = [&](int c) {
         const long long a = active_clusters(k, c);
         return a > 0 ? (units + a - 1) / a : (long long)1 << 40;
