@@ -66,7 +66,7 @@ typedef enum pkv_dtype { PKV_BF16 = 0, PKV_F32 = 1 } pkv_dtype;
 #define PKV_ERR_TIMEOUT  (1u << 6)  /* a bounded wait for a K/V copy inside the kernel gave up; output zeroed */
 
 /* Flags for the attention calls. */
-#define PKV_FLAG_SIMT  (1u << 0)  /* bf16: use the CUDA-core kernel instead of the tensor-core one */
+#define PKV_FLAG_SIMT  (1u << 0)  /* bf16: use the CUDA-core kernels instead of the tensor-core ones */
 #define PKV_FLAG_PDL   (1u << 1)  /* launch with programmatic dependent launch; see pkv_attend_varlen */
 #define PKV_FLAG_PREFETCH_NEXT (1u << 2)  /* warm L2 with layer + 1's pages; see pkv_attend_varlen */
 #define PKV_FLAG_MMA_SYNC (1u << 3)  /* bf16, head_dim 128, > 8 rows per kv head: mma.sync tile instead of tcgen05 */
@@ -186,12 +186,17 @@ int pkv_append(const pkv_cache *cache, int32_t layer,
  * softmax results are merged by log-sum-exp through distributed shared
  * memory in the same launch, so no workspace is needed (workspace NULL,
  * workspace_bytes 0; see pkv_attend_workspace_bytes for the other mode).  0 picks the count
- * from the launch shape (and a smaller one if the device cannot co-schedule
- * the cluster); a larger count than the segment has 16-token pages leaves
- * CTAs idle.
+ * from the launch shape: a power of two aiming at about three waves of
+ * resident CTAs, the largest cluster the device can co-schedule below it,
+ * and, for kernels that fit once per SM with few (segment, kv head) ranges,
+ * the cluster size that needs the fewest waves of clusters resident at once.
+ * A larger count than the segment has 16-token pages leaves CTAs idle.
  *
- * flags: PKV_FLAG_SIMT selects the CUDA-core kernel for bf16 (fp32 always
- * uses it).  PKV_FLAG_PDL launches with programmatic dependent launch: the
+ * flags: PKV_FLAG_SIMT selects the CUDA-core kernels for bf16 (fp32 always
+ * uses them): at most 8 query rows per kv head take the decode kernel's
+ * variant with fp32 FMA products, wider groups the general CUDA-core tile.
+ * PKV_FLAG_MMA_SYNC keeps wide bf16 groups at head_dim 128 (more than 8
+ * rows per kv head) on the mma.sync tile instead of the tcgen05 one.  PKV_FLAG_PDL launches with programmatic dependent launch: the
  * kernel may start reading cache slots of positions below kv_end - q_len,
  * the block table and seq_info while the previous kernel on the stream is
  * still running, so set it only when that previous kernel writes none of
