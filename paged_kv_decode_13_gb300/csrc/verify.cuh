@@ -11,7 +11,7 @@
 // merge through distributed shared memory with merge_rows, pushing into the
 // stage area each CTA has finished with).
 //
-// Per CTA (352 threads):
+// Per CTA (448 threads):
 //   warps 0-7   softmax: row t of the tile (TMEM lane t) belongs to warps
 //               t / 32 and t / 32 + 4, each taking 32 of a stage's 64 keys
 //               and 64 of O's 128 columns; the pair agrees on the row's
@@ -20,19 +20,25 @@
 //               read, and after the loop write their rows of O out (one CTA
 //               per range) or push them to the CTA of the cluster that
 //               merges those rows;
-//   warp 8      K loads: 4 pages (64 keys) per stage, each page as two
-//               64-column TMA boxes, so a stage is one K-major tile of 64
-//               keys (128-byte swizzle) for Q K^T; a stage is released as
-//               soon as its S product has completed;
-//   warp 10     V loads: 4 pages per stage, one TMA box per page (two
-//               64-column parts), an MN-major tile of 16 keys for each step
-//               of P V; released when its P V has completed;
-//   warp 9      MMA: fixes edge pages (stale V rows zeroed, this step's rows
-//               taken from k_new / v_new and appended to the cache), issues
-//               S(j) = Q K_j^T (M = 128, N = 64, A = Q from TMEM, 8 steps over
-//               head_dim) and, once P(j-1) is in TMEM, O += P(j-1) V(j-1)
-//               (M = 128, N = 128, A = P from TMEM, 4 steps of 16 keys); also
-//               owns the TMEM allocation.
+//   warps 8, 11 K loads, alternate stages: 4 pages (64 keys) per stage,
+//               each page as two 64-column TMA boxes, so a stage is one
+//               K-major tile of 64 keys (128-byte swizzle) for Q K^T; a stage
+//               is released as soon as its S product has completed;
+//   warps 10, 12 V loads, alternate stages: 4 pages per stage, one TMA box
+//               per page (two 64-column parts), an MN-major tile of 16 keys
+//               for each step of P V; released when its P V has completed;
+//   warp 9      S products: fixes this step's K rows into the stage (taken
+//               from k_new, appended to the cache), issues S(j) = Q K_j^T
+//               (M = 128, N = 64, A = Q from TMEM, 8 steps over head_dim)
+//               once P V(j - NB) has freed its TMEM buffer; also owns the
+//               TMEM allocation;
+//   warp 13     P V products: fixes edge V pages (stale rows zeroed, this
+//               step's rows from v_new, appended), and once P(j) is in TMEM
+//               issues O += P(j) V(j) (M = 128, N = 128, A = P from TMEM, 4
+//               steps of 16 keys).
+// One thread issuing every copy, or every product, was the limit: a warp's
+// later instructions wait behind its tensor-core and TMA issues, so two
+// loaders per stream and separate S and P V issuers keep each queue short.
 // TMEM (512 columns): S / P in NB = 2 buffers of 64 columns from column 0
 // (P as bf16 pairs in the first 32 columns of its buffer), then O (128
 // columns) and Q (64).  A third buffer measured no faster: the loads bound.
@@ -61,7 +67,8 @@ struct VfyCfg {
     static constexpr int NK = NK_;                  // K stages of 4 pages
     static constexpr int NV = NV_;                  // V stages of 4 pages
     static constexpr int kRows = 128;               // query rows per CTA = TMEM lanes
-    static constexpr int kThreads = 352;            // 8 softmax warps, K loader, MMA, V loader
+    static constexpr int kThreads = 448;            // 8 softmax warps, 2 K loaders, 2 V loaders, S and P V issuers
+    static constexpr int kLoaders = 2;              // loader warps per stream (alternate stages)
     static constexpr int kPages = 4;                // pages per stage (N = 64 keys)
     static constexpr unsigned kHalf = kPages * kPage * 128;        // 64 keys x 128 B
     static constexpr unsigned kKStage = 2 * kHalf;                 // K: two 64-column halves
@@ -82,6 +89,9 @@ struct VfyCfg {
     static constexpr int kTmemCols = 512;
     static_assert(kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
     static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0, "operand tiles start on 1024-byte swizzle atoms");
+    // A loader waits on the release of its stage's previous use; with at
+    // least as many stages as loaders that use is never two phases back.
+    static_assert(NK >= kLoaders && NV >= kLoaders, "ring shorter than its loaders");
 };
 
 // ---------------------------------------------------------------- tcgen05 helpers
@@ -201,7 +211,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     constexpr int DP = C::DP, NK = C::NK, NV = C::NV, R = C::kRows, NT = C::kThreads, PG = C::kPages;
     constexpr int EPC = 8;  // bf16 per 16-byte chunk
     constexpr float kLn2 = 0.6931471805599453f;
-    constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+    constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpK2 = 11, kWarpV2 = 12, kWarpPv = 13;
+    constexpr int NL = C::kLoaders;
     constexpr int NB = C::NB;
     constexpr unsigned kColO = 64 * NB, kColQ = kColO + 128;
 
@@ -321,10 +332,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         return ok;
     };
 
-    // ---- TMA loads (warp 8: K, warp 10: V): group j = pages cb0 + 4j .. + 3
-    const bool loader = warp == kWarpK || warp == kWarpV;
-    const bool is_v = warp == kWarpV;
-    int id_reg = -1, id_window = -1, issued = 0;
+    // ---- TMA loads (warps 8, 11: K; 10, 12: V): group j = pages cb0 + 4j .. + 3,
+    // loader lidx of a stream issuing the groups j = lidx (mod 2)
+    const bool loader = warp == kWarpK || warp == kWarpV || warp == kWarpK2 || warp == kWarpV2;
+    const bool is_v = warp == kWarpV || warp == kWarpV2;
+    const int lidx = (warp == kWarpK2 || warp == kWarpV2) ? 1 : 0;
+    int id_reg = -1, id_window = -1, issued = lidx;
     bool bad = false;
     auto load_ids = [&](int li0) {
         id_window = li0 & ~31;
@@ -376,7 +389,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     if (loader) {
         load_ids(0);
         #pragma unroll 1
-        for (; issued < NSt && issued < ngr; ++issued) {
+        for (; issued < NSt && issued < ngr; issued += NL) {
             if (!early_ok(issued)) break;
             issue(issued);
         }
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
     if (loader) {
         #pragma unroll 1
-        for (; issued < NSt && issued < ngr; ++issued) issue(issued);
+        for (; issued < NSt && issued < ngr; issued += NL) issue(issued);
     }
     tc_fence_before();
     __syncthreads();  // queries in TMEM, append validity known
@@ -453,20 +466,23 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         // ---------------- refill each stage once its product has completed
         uint64_t *emp = is_v ? v_empty : k_empty;
         #pragma unroll 1
-        for (int j = issued; j < ngr; ++j) {
+        for (int j = issued; j < ngr; j += NL) {
             if (!wait_bar(emp + (j % NSt), ((j / NSt) - 1) & 1)) { timed_out = true; break; }
             issue(j);
-            issued = j + 1;
+            issued = j + NL;
         }
-        // Drain: every issued stage has landed before its memory is reused or freed.
-        if (lane == 0) {
+        // Drain: every issued stage has landed before its memory is reused or
+        // freed.  The first loader of the stream waits on each stage's last
+        // use, whichever loader issued it (an earlier use's phase may have
+        // been overtaken).
+        if (lane == 0 && lidx == 0) {
             uint64_t *fb = is_v ? v_full : k_full;
             #pragma unroll 1
-            for (int j = max(0, issued - NSt); j < issued; ++j)
+            for (int j = max(0, ngr - NSt); j < ngr; ++j)
                 if (!mbar_wait_ns(fb + (j % NSt), (j / NSt) & 1)) break;
         }
-    } else if (warp == kWarpMma) {
-        // ---------------- edge-page fix-up and MMA issue
+    } else if (warp == kWarpMma || warp == kWarpPv) {
+        // ---------------- edge-page fix-up and MMA issue (S: warp 9, P V: warp 13)
         const uint32_t id_s = umma_idesc_bf16(128, 64, 0), id_o = umma_idesc_bf16(128, 128, 1);
         // Rows of page u of group j: stale ones [0, zlo) and [zhi, 16) (V
         // zeroed), this step's ones [na, zhi) (K or V from k_new / v_new, also
@@ -559,6 +575,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             __syncwarp();
             return true;
         };
+        if (warp == kWarpMma) {
         #pragma unroll 1
         for (int j = 0; j < ngr && !timed_out; ++j) {
             const int ks = j % NK, b = j % NB;
@@ -578,9 +595,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
                 umma_commit(k_empty + ks);
             }
             __syncwarp();
-            if (j >= 1 && !issue_pv(j - 1)) { timed_out = true; break; }
         }
-        if (!timed_out && ngr > 0 && !issue_pv(ngr - 1)) timed_out = true;
         // Drain: every MMA this thread issued has completed before TMEM or the
         // stages are released.
         if (lane == 0) {
@@ -588,6 +603,17 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             mbar_wait_ns(drain, 0);
         }
         __syncwarp();
+        } else {
+        int last = -1;
+        #pragma unroll 1
+        for (int i = 0; i < ngr && !timed_out; ++i) {
+            if (!issue_pv(i)) { timed_out = true; break; }
+            last = i;
+        }
+        // Drain: the last commit completes after every product this thread issued.
+        if (lane == 0 && last >= 0) mbar_wait_ns(pv_done + (last % NB), (last / NB) & 1);
+        __syncwarp();
+        }
     } else if (softmax) {
         // ---------------- softmax: this thread = (row r, 32 keys of each stage)
         int lo_r = 0, hi_r = 0;
