@@ -521,8 +521,18 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
                 *reinterpret_cast<uint4 *>(stage + off) = v;
             }
         };
+        // A group wholly inside the CTA's range and below this step's rows
+        // (and, for V, at or above the first visible key) needs no fix-up;
+        // deciding that up front keeps the per-page checks off the issuing
+        // warps' critical path (they measured 0.6 us per group).
+        const int clean_hi = fused ? new_start : kend;
+        auto interior = [&](int j, bool v) {
+            const int g0 = (cb0 + j * PG) * kPage, g1 = g0 + PG * kPage;
+            return j * PG + PG <= nb && g1 <= clean_hi && (!v || g0 >= lo_u);
+        };
         // K: only this step's rows (stale keys are masked out of S).
         auto fix_k = [&](int j, unsigned char *stage) {
+            if (interior(j, false)) return;
             bool any = false;
 #pragma unroll 1
             for (int u = 0; u < PG; ++u) {
@@ -535,6 +545,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         };
         // V: stale rows zeroed (P is zero there, but 0 x NaN is not), this step's rows.
         auto fix_v = [&](int j, unsigned char *stage) {
+            if (interior(j, true)) return;
             bool any = false;
 #pragma unroll 1
             for (int u = 0; u < PG; ++u) {
