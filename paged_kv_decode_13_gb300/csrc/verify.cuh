@@ -14,12 +14,14 @@
 // Per CTA (448 threads):
 //   warps 0-7   softmax: row t of the tile (TMEM lane t) belongs to warps
 //               t / 32 and t / 32 + 4, each taking 32 of a stage's 64 keys
-//               and 64 of O's 128 columns; the pair agrees on the row's
-//               reference maximum through shared memory.  They also put Q
-//               into TMEM, write P into TMEM over the S columns they have
-//               read, and after the loop write their rows of O out (one CTA
-//               per range) or push them to the CTA of the cluster that
-//               merges those rows;
+//               with a running maximum and sum of its own and its own O
+//               accumulator (O_0 for keys 0-31 of every stage, O_1 for
+//               32-63), so the halves never wait for each other inside the
+//               loop; they are combined once, in the epilogue.  The warps
+//               also put Q into TMEM, write P over the S columns they have
+//               read, and after the loop write their rows out (one CTA per
+//               range) or push them to the CTA of the cluster that merges
+//               those rows;
 //   warps 8, 11 K loads, alternate stages: 4 pages (64 keys) per stage,
 //               each page as two 64-column TMA boxes, so a stage is one
 //               K-major tile of 64 keys (128-byte swizzle) for Q K^T; a stage
@@ -34,21 +36,22 @@
 //               TMEM allocation;
 //   warp 13     P V products: fixes edge V pages (stale rows zeroed, this
 //               step's rows from v_new, appended), and once P(j) is in TMEM
-//               issues O += P(j) V(j) (M = 128, N = 128, A = P from TMEM, 4
-//               steps of 16 keys).
+//               issues O_0 += P(j) V(j) over keys 0-31 and O_1 += ... over
+//               keys 32-63 (M = 128, N = 128, A = P from TMEM, 2 steps of 16
+//               keys each).
 // One thread issuing every copy, or every product, was the limit: a warp's
 // later instructions wait behind its tensor-core and TMA issues, so two
 // loaders per stream and separate S and P V issuers keep each queue short.
 // TMEM (512 columns): S / P in NB = 2 buffers of 64 columns from column 0
-// (P as bf16 pairs in the first 32 columns of its buffer), then O (128
-// columns) and Q (64).  A third buffer measured no faster: the loads bound.
+// (each half's P as bf16 pairs in the first 16 of its own 32 S columns),
+// then O_0 and O_1 (128 columns each) and Q (64).
 // Shared memory holds only the K and V stages, so 13 stages (208 KB) of
 // loads are in flight.
 //
-// The online softmax keeps each row in one thread pair (no cross-lane
-// reduction) and raises a row's reference maximum lazily: only when a score exceeds it by
-// more than 2^8, and then O is rescaled in TMEM after the previous P V has
-// landed.  Every wait is bounded; a timeout poisons the CTA's output
+// The online softmax keeps each half row in one thread (no cross-lane
+// reduction) and raises its reference maximum lazily: only when a score
+// exceeds it by more than 2^8, and then its O is rescaled in TMEM after the
+// previous P V has landed.  Every wait is bounded; a timeout poisons the CTA's output
 // (PKV_ERR_TIMEOUT), drains what is in flight and frees TMEM.
 //
 // Semantics follow the segment-table attention of ExecuTorch PR #24072
@@ -79,11 +82,11 @@ struct VfyCfg {
     static constexpr size_t kRecvStat = (size_t)16 * kRows * 8;
     static constexpr size_t kRecvBytes = kRecvStat + ((size_t)kRows + 16) * DP * 4;
     static constexpr size_t kBodyBytes = kLoopBytes > kRecvBytes ? kLoopBytes : kRecvBytes;
-    // merge weights [16][rows], cluster flags [16], row max exchange [2][8 warps][32], row sums [2][rows]
-    static constexpr size_t kWnBytes = (size_t)16 * kRows * 4 + 16 * 4 + 2 * 8 * 32 * 4 + 2 * kRows * 4;
+    // merge weights [16][rows], cluster flags [16], per-half row maxima and sums [2][rows] each
+    static constexpr size_t kWnBytes = (size_t)16 * kRows * 4 + 16 * 4 + 2 * kRows * 4 + 2 * kRows * 4;
     static constexpr int NB = 2;                    // S / P buffers in TMEM
-    // K, V full / empty; s_full, p_full, pv_done [NB]; drain; row-pair exchange [4 quadrants][2]
-    static constexpr int kBars = 2 * NK + 2 * NV + 3 * NB + 1 + 8;
+    // K, V full / empty; s_full, p_full, pv_done [NB]; drain
+    static constexpr int kBars = 2 * NK + 2 * NV + 3 * NB + 1;
     static constexpr size_t kMiscBytes = (size_t)kBars * 8 + 16 + 32 * 4 + (size_t)kThreads * 4;
     static constexpr size_t kSmemBytes = 1024 + kBodyBytes + kWnBytes + kMiscBytes;
     static constexpr int kTmemCols = 512;
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpK2 = 11, kWarpV2 = 12, kWarpPv = 13;
     constexpr int NL = C::kLoaders;
     constexpr int NB = C::NB;
-    constexpr unsigned kColO = 64 * NB, kColQ = kColO + 128;
+    constexpr unsigned kColO = 64 * NB, kColQ = kColO + 256;  // O_h at kColO + 128 h
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *body = reinterpret_cast<unsigned char *>(
@@ -223,13 +226,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     unsigned char *sV = sK + (size_t)NK * C::kKStage;              // NV V stages
     float *sWn = reinterpret_cast<float *>(body + C::kBodyBytes);  // [16][R] merge weights
     int *sCf = reinterpret_cast<int *>(sWn + 16 * R);              // [16] flags pushed by the cluster
-    float *sXm = reinterpret_cast<float *>(sCf + 16);              // [2][8][32] row maxima of each warp
-    float *sXl = sXm + 2 * 8 * 32;                                 // [2][R] row sums of each half
+    float *sXm = reinterpret_cast<float *>(sCf + 16);              // [2][R] row maxima of each half
+    float *sXl = sXm + 2 * R;                                      // [2][R] row sums of each half
     uint64_t *bars = reinterpret_cast<uint64_t *>(sXl + 2 * R);
     uint64_t *k_full = bars, *k_empty = bars + NK, *v_full = bars + 2 * NK, *v_empty = v_full + NV;
     uint64_t *s_full = v_empty + NV, *p_full = s_full + NB, *pv_done = p_full + NB;
     uint64_t *drain = pv_done + NB;
-    uint64_t *pair = drain + 1;                                    // [4][2]: the two warps of a row quadrant
     unsigned *tslot = reinterpret_cast<unsigned *>(bars + C::kBars);
     volatile int *sAbort = reinterpret_cast<volatile int *>(tslot + 1);
     int *sAppOk = reinterpret_cast<int *>(tslot + 2);
@@ -294,8 +296,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         #pragma unroll 1
         for (int i = 0; i < C::kBars; ++i) {
             const bool eight = i >= 2 * NK + 2 * NV + NB && i < 2 * NK + 2 * NV + 2 * NB;  // p_full: every softmax warp
-            const bool two = i >= 2 * NK + 2 * NV + 3 * NB + 1;                         // pair: both warps of a quadrant
-            mbar_init(bars + i, eight ? 8 : two ? 2 : 1);
+            mbar_init(bars + i, eight ? 8 : 1);
         }
         fence_barrier_init();
         sFlag[0] = 0;
@@ -577,9 +578,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             if (lane == 0) {
                 const unsigned v_addr = smem_u32(stage);
 #pragma unroll
-                for (int u = 0; u < PG; ++u)
-                    umma_bf16_ts(tmem + kColO, tmem + b * 64 + u * 8, umma_desc(v_addr + u * 4096, 2048, 1024), id_o,
-                                 (i > 0 || u > 0) ? 1 : 0);
+                for (int u = 0; u < PG; ++u) {
+                    const int h = u >> 1;  // keys 0-31 -> O_0 (P of half 0), 32-63 -> O_1 (P of half 1)
+                    umma_bf16_ts(tmem + kColO + h * 128, tmem + b * 64 + h * 32 + (u & 1) * 8,
+                                 umma_desc(v_addr + u * 4096, 2048, 1024), id_o, (i > 0 || (u & 1)) ? 1 : 0);
+                }
                 umma_commit(v_empty + vs);
                 umma_commit(pv_done + b);
             }
@@ -632,47 +635,52 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         hi_r = min(hi_r, hi_pos);
         #pragma unroll 1
         for (int j = 0; j < ngr; ++j) {
-            const int b = j % NB, xb = j & 1;  // S / P buffer, row-pair exchange buffer
+            const int b = j % NB;  // S / P buffer
             if (!wait_bar(s_full + b, (j / NB) & 1)) { timed_out = true; break; }
             tc_fence_after();
             float x[32];
             tmem_ld32(tmem + lane_off + b * 64 + half * 32, x);
             const int pos0 = lo_pos + j * PG * kPage + half * 32;
-            float mx = -CUDART_INF_F;
+            // Key bounds per score only where some real row of the warp
+            // does not see all 32 keys (padding rows are never written out).
+            if (__all_sync(0xffffffffu, r >= rows_here || (pos0 >= lo_r && pos0 + 32 <= hi_r))) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int pos = pos0 + k;
-                x[k] = (pos >= lo_r && pos < hi_r) ? x[k] * p.scale_log2 : -CUDART_INF_F;
-                mx = fmaxf(mx, x[k]);
+                for (int k = 0; k < 32; ++k) x[k] *= p.scale_log2;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int pos = pos0 + k;
+                    x[k] = (pos >= lo_r && pos < hi_r) ? x[k] * p.scale_log2 : -CUDART_INF_F;
+                }
             }
-            // The row's two halves agree on its maximum (double-buffered
-            // exchange: a buffer is rewritten only after the partner has
-            // passed the next exchange).  The pair's barrier also orders this
-            // half's read of S before the other half writes P over it.
-            sXm[(xb * 8 + warp) * 32 + lane] = mx;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pair + quad * 2 + xb);
-            if (!wait_bar(pair + quad * 2 + xb, (j >> 1) & 1)) { timed_out = true; break; }
-            tc_fence_after();
-            mx = fmaxf(mx, sXm[(xb * 8 + (warp ^ 4)) * 32 + lane]);
+            float mx;
+            {   // row maximum of the 32 scores as a tree (depth 5, not a 32-long chain)
+                float t[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) t[k] = fmaxf(x[k], x[k + 16]);
+#pragma unroll
+                for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+                mx = t[0];
+            }
             // Lazy reference maximum: raised only when a score passes it by 2^8.
             const bool grow = mx > m + 8.f;
             if (__any_sync(0xffffffffu, grow)) {
                 const float m_new = grow ? mx : m;
                 const float alpha = (!grow || m == -CUDART_INF_F) ? (grow ? 0.f : 1.f) : exp2f(m - m_new);
                 if (j > 0 && __any_sync(0xffffffffu, grow && m != -CUDART_INF_F)) {
-                    // O holds P V up to group j - 1 against the old reference:
-                    // wait for that product, then rescale this half's columns.
+                    // O_half holds P V up to group j - 1 against the old
+                    // reference: wait for that product, then rescale it.
                     if (!wait_bar(pv_done + ((j - 1) % NB), ((j - 1) / NB) & 1)) { timed_out = true; break; }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 64; c0 += 32) {
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
                         float o[32];
-                        tmem_ld32(tmem + lane_off + kColO + half * 64 + c0, o);
+                        tmem_ld32(tmem + lane_off + kColO + half * 128 + c0, o);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) o[k] *= alpha;
-                        tmem_st32(tmem + lane_off + kColO + half * 64 + c0, o);
+                        tmem_st32(tmem + lane_off + kColO + half * 128 + c0, o);
                     }
                 }
                 l *= alpha;
@@ -686,8 +694,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
                 l += e0 + e1;
                 pk[k] = pack_bf16x2(e0, e1);
             }
-            // P(j) as bf16 pairs over the first 32 columns of buffer b
-            tmem_st16(tmem + lane_off + b * 64 + half * 16, pk);
+            // P(j) as bf16 pairs over the first 16 of this half's S columns (read above)
+            tmem_st16(tmem + lane_off + b * 64 + half * 32, pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + b);
@@ -695,6 +703,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         // the last product has landed before O is read back
         if (!timed_out && ngr > 0 && !wait_bar(pv_done + ((ngr - 1) % NB), ((ngr - 1) / NB) & 1)) timed_out = true;
         timed_out = __any_sync(0xffffffffu, timed_out);
+        sXm[half * R + r] = m;
         sXl[half * R + r] = timed_out ? 0.f : l;
     }
     if (timed_out && lane == 0) atomicOr(sFlag, 2);
@@ -704,11 +713,31 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     tc_fence_after();
     const int flags = sFlag[0];
     if (tid == 0 && flags) atomicOr(p.err, ((flags & 1) ? PKV_ERR_BLOCK : 0u) | ((flags & 2) ? PKV_ERR_TIMEOUT : 0u));
-    const bool has_o = ngr > 0 && !(flags & 2);  // O in TMEM holds this CTA's product
+    const bool has_o = ngr > 0 && !(flags & 2);  // O_0, O_1 in TMEM hold this CTA's product
+    // The row's two halves against one reference: weights w_h = 2^(m_h - m)
+    // (a half that saw no key has weight 0 and is never multiplied in).
+    float w0 = 0.f, w1 = 0.f;
     if (softmax) {
-        l = sXl[r] + sXl[R + r];                  // the row's sum over both halves
+        const float m0 = sXm[r], m1 = sXm[R + r];
+        m = fmaxf(m0, m1);
+        w0 = (m == -CUDART_INF_F || m0 == -CUDART_INF_F) ? 0.f : exp2f(m0 - m);
+        w1 = (m == -CUDART_INF_F || m1 == -CUDART_INF_F) ? 0.f : exp2f(m1 - m);
+        l = w0 * sXl[r] + w1 * sXl[R + r];
         if (!has_o) { m = -CUDART_INF_F; l = 0.f; }
     }
+    // This thread's 32 columns c0.. of the row's combined (unnormalised) O.
+    auto o_cols = [&](int c0, float (&o)[32]) {
+        if (!has_o) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0.f;
+            return;
+        }
+        float o1[32];
+        tmem_ld32(tmem + lane_off + kColO + half * 64 + c0, o);
+        tmem_ld32(tmem + lane_off + kColO + 128 + half * 64 + c0, o1);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = (w0 != 0.f ? w0 * o[e] : 0.f) + (w1 != 0.f ? w1 * o1[e] : 0.f);
+    };
 
     // ---- epilogue: rows of O straight from TMEM
     auto out_row = [&](int rr) {
@@ -732,7 +761,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 float o[32];
-                if (has_o) tmem_ld32(tmem + lane_off + kColO + half * 64 + c0, o);
+                o_cols(c0, o);
                 if (r < rows_here) {
 #pragma unroll
                     for (int k = 0; k < 32; k += 4)
@@ -762,12 +791,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 float o[32];
-                if (has_o) {
-                    tmem_ld32(tmem + lane_off + kColO + half * 64 + c0, o);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
-                }
+                o_cols(c0, o);
                 if (r < rows_here)
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
