@@ -231,9 +231,12 @@ int make_plan(const pkv_cache *c, int Hq, int S, int max_q_len, long long max_kv
         return PKV_OK;
     }
     if (n == 0) {
-        // CTAs of this kernel that fit on one SM by shared memory
+        // CTAs of this kernel that fit on one SM by shared memory.  The
+        // tcgen05 tile aims at one wave: its fixed cost per CTA (first page
+        // loads, cluster merge) is worth about 15 groups of 64 keys, and it
+        // orders ranges longest first and runs short ones alone instead.
         const long long per_sm = std::max<long long>(1, 232448 / ((long long)pl->k.smem + 1024));
-        const long long target = (long long)kTargetWaves * device_sms() * per_sm;
+        const long long target = (long long)(pl->k.tc ? 1 : kTargetWaves) * device_sms() * per_sm;
         const long long want = (target + units - 1) / units;
         n = 1;
         while (n < want && n < kMaxCluster) n *= 2;

@@ -65,7 +65,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #elif PKV_INST_DP == 128
     {
-        if (rc == 6) return vinfo<VfyCfg<6, 7>>();
+        if (rc == 6) return vinfo<VfyCfg<5, 6>>();
         if (rc == 5) return dinfo<DecCfg<128, 6, 2>>();
         if (rc == 4) return dinfo<DecCfg<128, 4, 3>>();
         if (rc == 0) return CFG(B16, 1, 4, 3, true);

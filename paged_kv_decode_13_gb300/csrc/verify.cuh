@@ -31,7 +31,8 @@
 //               for each step of P V; released when its P V has completed;
 //   warp 9      S products: fixes this step's K rows into the stage (taken
 //               from k_new, appended to the cache), issues S(j) = Q K_j^T
-//               (M = 128, N = 64, A = Q from TMEM, 8 steps over head_dim)
+//               (M = 128, N = 64, A = Q from shared memory, 8 steps over
+//               head_dim)
 //               once P V(j - NB) has freed its TMEM buffer; also owns the
 //               TMEM allocation;
 //   warp 13     P V products: fixes edge V pages (stale rows zeroed, this
@@ -42,11 +43,14 @@
 // One thread issuing every copy, or every product, was the limit: a warp's
 // later instructions wait behind its tensor-core and TMA issues, so two
 // loaders per stream and separate S and P V issuers keep each queue short.
-// TMEM (512 columns): S / P in NB = 2 buffers of 64 columns from column 0
-// (each half's P as bf16 pairs in the first 16 of its own 32 S columns),
-// then O_0 and O_1 (128 columns each) and Q (64).
-// Shared memory holds only the K and V stages, so 13 stages (208 KB) of
-// loads are in flight.
+// TMEM (512 columns allocated): S / P in NB = 2 buffers of 64 columns from
+// column 0 (each half's P as bf16 pairs in the first 16 of its own 32 S
+// columns), then O_0 and O_1 (128 columns each).  Q sits in shared memory
+// (K-major, 128-byte swizzle): a product whose A operand comes from TMEM
+// issues at 117 cycles against 67 from shared memory (N <= 128), and the
+// S products were the tile's pacing work.
+// Shared memory holds Q (32 KB) and the K and V stages: 11 stages (176 KB)
+// of loads in flight.
 //
 // The online softmax keeps each half row in one thread (no cross-lane
 // reduction) and raises its reference maximum lazily: only when a score
@@ -82,16 +86,22 @@ struct VfyCfg {
     static constexpr size_t kRecvStat = (size_t)16 * kRows * 8;
     static constexpr size_t kRecvBytes = kRecvStat + ((size_t)kRows + 16) * DP * 4;
     static constexpr size_t kBodyBytes = kLoopBytes > kRecvBytes ? kLoopBytes : kRecvBytes;
+    // Q: two K-major halves of 128 rows x 64 columns, 128-byte swizzle
+    static constexpr size_t kQHalf = (size_t)kRows * 128;
+    static constexpr size_t kQBytes = 2 * kQHalf;
     // merge weights [16][rows], cluster flags [16], per-half row maxima and sums [2][rows] each
     static constexpr size_t kWnBytes = (size_t)16 * kRows * 4 + 16 * 4 + 2 * kRows * 4 + 2 * kRows * 4;
-    static constexpr int NB = 2;                    // S / P buffers in TMEM
+    static constexpr int NB = 3;                    // S / P buffers in TMEM
     // K, V full / empty; s_full, p_full, pv_done [NB]; drain
     static constexpr int kBars = 2 * NK + 2 * NV + 3 * NB + 1;
     static constexpr size_t kMiscBytes = (size_t)kBars * 8 + 16 + 32 * 4 + (size_t)kThreads * 4;
-    static constexpr size_t kSmemBytes = 1024 + kBodyBytes + kWnBytes + kMiscBytes;
+    static constexpr size_t kSmemBytes = 1024 + kBodyBytes + kQBytes + kWnBytes + kMiscBytes;
     static constexpr int kTmemCols = 512;
+    static constexpr int kSoloGroups = 24;          // a range of at most this many groups runs on one CTA
+    static constexpr int kRankSegs = 64;            // up to this many segments launch longest range first
     static_assert(kSmemBytes <= 232448, "exceeds the per-CTA shared memory limit");
-    static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0, "operand tiles start on 1024-byte swizzle atoms");
+    static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0 && kBodyBytes % 1024 == 0,
+                  "operand tiles start on 1024-byte swizzle atoms");
     // A loader waits on the release of its stage's previous use; with at
     // least as many stages as loaders that use is never two phases back.
     static_assert(NK >= kLoaders && NV >= kLoaders, "ring shorter than its loaders");
@@ -217,14 +227,15 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpK2 = 11, kWarpV2 = 12, kWarpPv = 13;
     constexpr int NL = C::kLoaders;
     constexpr int NB = C::NB;
-    constexpr unsigned kColO = 64 * NB, kColQ = kColO + 256;  // O_h at kColO + 128 h
+    constexpr unsigned kColO = 64 * NB;  // O_h at kColO + 128 h
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *body = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *sK = body;                                      // NK K stages
     unsigned char *sV = sK + (size_t)NK * C::kKStage;              // NV V stages
-    float *sWn = reinterpret_cast<float *>(body + C::kBodyBytes);  // [16][R] merge weights
+    unsigned char *sQ = body + C::kBodyBytes;                      // Q, two K-major halves
+    float *sWn = reinterpret_cast<float *>(sQ + C::kQBytes);       // [16][R] merge weights
     int *sCf = reinterpret_cast<int *>(sWn + 16 * R);              // [16] flags pushed by the cluster
     float *sXm = reinterpret_cast<float *>(sCf + 16);              // [2][R] row maxima of each half
     float *sXl = sXm + 2 * R;                                      // [2][R] row sums of each half
@@ -244,7 +255,6 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     const int r = quad * 32 + lane;                             // softmax: this thread's row of the tile
     const int rank = blockIdx.x, ncta = gridDim.x;
     const int g = blockIdx.y / p.row_tiles, rt = blockIdx.y - g * p.row_tiles;
-    const int s = blockIdx.z;
     const bool cov_cta = grid_cta_index() < coverage_slices(p, NT);
     const int cov_any = coverage_begin(p, sCov, cov_cta, NT);
     if (p.S == 0) {
@@ -252,6 +262,28 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         pdl_trigger();
         if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
         return;
+    }
+    // Longest ranges first: with few segments every CTA ranks them by their
+    // key count (ties by index) and takes the blockIdx.z-th, so the longest
+    // ranges start in the first wave and the short ones fill the tail.  Any
+    // order is correct; this only schedules.  (The merge weights' space is
+    // idle until the epilogue.)
+    int s = blockIdx.z;
+    if (p.S <= C::kRankSegs) {
+        int *sLen = reinterpret_cast<int *>(sWn), *sPick = sLen + C::kRankSegs;
+        if (tid < p.S) {
+            const Segment t = load_segment(p.seq_info, tid);
+            const int lo = p.window > 0 ? max(0, t.kend - t.ql - p.window + 1) : 0;
+            sLen[tid] = max(0, t.kend - lo);
+        }
+        __syncthreads();
+        if (tid < p.S) {
+            int k = 0;
+            for (int u = 0; u < p.S; ++u) k += (sLen[u] > sLen[tid]) || (sLen[u] == sLen[tid] && u < tid);
+            if (k == (int)blockIdx.z) *sPick = tid;
+        }
+        __syncthreads();
+        s = *sPick;
     }
 
     // ---- segment and its key range (reads allowed before the dependency wait)
@@ -278,7 +310,20 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     const int pb_begin = lo_u / kPage;
     const int pb_end = (kend + kPage - 1) / kPage;
     const int nblk = pb_end - pb_begin;
-    const int bps = (nblk + ncta - 1) / ncta;
+    // A short range runs on the cluster's first CTA alone, without a merge;
+    // the others leave at once (uniform: every CTA of the cluster sees the
+    // same range, so no cluster barrier is ever half attended).
+    const bool solo = ncta > 1 && (nblk + PG - 1) / PG <= C::kSoloGroups;
+    const int ncl = solo ? 1 : ncta;  // CTAs sharing the range
+    if (solo && rank > 0) {
+        if (cov_cta) {
+            pdl_wait();
+            pdl_trigger();
+            apply_coverage(p, sCov, cov_any, NT);
+        }
+        return;
+    }
+    const int bps = (nblk + ncl - 1) / ncl;
     const int active = (nblk + bps - 1) / bps;
     const int cb0 = pb_begin + rank * bps;
     const int nb = rank < active ? min(cb0 + bps, pb_end) - cb0 : 0;
@@ -431,24 +476,22 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
     pdl_wait();
     pdl_trigger();
 
-    // ---- queries into TMEM (columns 256-319, bf16 pairs): each softmax
-    // thread its row's half; rows past the group are zero.
+    // ---- queries into shared memory: each softmax thread its row's half
+    // (64 columns = one swizzled 128-byte row of that half's tile); rows
+    // past the group are zero.
     if (softmax) {
-        unsigned qv[32];
+        uint4 qv[8];
         const int ur = row0 + r, i = ur / p.G, jh = ur - i * p.G;
         const T *src = reinterpret_cast<const T *>(p.q) + (((long long)sg.q0 + (r < rows_here ? i : 0)) * p.Hq +
                                                             (long long)g * p.G + (r < rows_here ? jh : 0)) * p.D;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < rows_here && half * 8 + c < dchunks) v = *reinterpret_cast<const uint4 *>(src + (half * 8 + c) * EPC);
-            qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
+            qv[c] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows_here && half * 8 + c < dchunks) qv[c] = *reinterpret_cast<const uint4 *>(src + (half * 8 + c) * EPC);
         }
-        unsigned lo16[16], hi16[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) { lo16[k] = qv[k]; hi16[k] = qv[16 + k]; }
-        tmem_st16(tmem + lane_off + kColQ + half * 32, lo16);
-        tmem_st16(tmem + lane_off + kColQ + half * 32 + 16, hi16);
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(sQ + half * C::kQHalf + swz_row(r, c)) = qv[c];
+        fence_proxy_async();  // the tensor core reads Q through the async proxy
     }
     if (cov_cta) apply_coverage(p, sCov, cov_any, NT);
     if (loader) {
@@ -456,7 +499,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
         for (; issued < NSt && issued < ngr; issued += NL) issue(issued);
     }
     tc_fence_before();
-    __syncthreads();  // queries in TMEM, append validity known
+    __syncthreads();  // queries in shared memory, append validity known
     tc_fence_after();
     const bool app_ok = has_new && *sAppOk == 0;
 
@@ -600,11 +643,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             if (j >= NB && !wait_bar(pv_done + b, ((j - NB) / NB) & 1)) { timed_out = true; break; }
             tc_fence_after();
             if (lane == 0) {
-                const unsigned k_addr = smem_u32(stage);
+                const unsigned k_addr = smem_u32(stage), q_addr = smem_u32(sQ);
 #pragma unroll
                 for (int k = 0; k < DP / 16; ++k)
-                    umma_bf16_ts(tmem + b * 64, tmem + kColQ + k * 8,
-                                 umma_desc(k_addr + (k >> 2) * C::kHalf + (k & 3) * 32, 16, 1024), id_s, k > 0 ? 1 : 0);
+                    umma_bf16(tmem + b * 64, umma_desc(q_addr + (k >> 2) * (unsigned)C::kQHalf + (k & 3) * 32, 16, 1024),
+                              umma_desc(k_addr + (k >> 2) * C::kHalf + (k & 3) * 32, 16, 1024), id_s, k > 0 ? 1 : 0);
                 umma_commit(s_full + b);
                 umma_commit(k_empty + ks);
             }
@@ -753,7 +796,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) verify_kernel(const __grid_con
             dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
         }
     };
-    if (ncta == 1) {
+    if (ncl == 1) {
         if (softmax) {
             const bool zero = flags || !(l > 0.f);
             const float inv = zero ? 0.f : 1.f / l;
