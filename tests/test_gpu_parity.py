@@ -575,6 +575,35 @@ def test_tcgen05_and_mma_sync_tiles_match_oracle(pkv, q_heads, max_q, causal):
             check_against_oracle(w, 0, out, lse, cache)
 
 
+@pytest.mark.parametrize("kv_len", [1472, 1536, 1537, 1600])
+@pytest.mark.parametrize("num_splits", [0, 2, 4])
+def test_tcgen05_solo_threshold(pkv, kv_len, num_splits):
+    """Ranges of at most 24 groups of 64 keys (1536 keys) run on the
+    cluster's first CTA alone, the other CTAs leaving before any cluster
+    barrier; one page more splits the range.  Equal lengths also exercise
+    the longest-first ranking's tie order."""
+    w = U.nan_tails(workloads.spec_verify(S=3, max_q=16, len_lo=kv_len, len_hi=kv_len, causal=True,
+                                          seed=kv_len + num_splits, q_heads=64))
+    out, lse, err, cache = run(pkv, w, num_splits=num_splits, max_kv=kv_len)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
+@pytest.mark.parametrize("S", [2, 64, 65])
+def test_tcgen05_longest_first_order(pkv, S):
+    """Up to 64 segments the CTAs take the ranges longest first (a
+    permutation of blockIdx.z computed on the device); beyond, in segment
+    order.  Either way every row matches the oracle."""
+    # kv_end >= q_len (= at most 8), so every segment is valid
+    w = U.nan_tails(workloads.spec_verify(S=S, max_q=8, len_lo=8, len_hi=2200, causal=S % 2 == 0, seed=90 + S,
+                                          q_heads=16))
+    out, lse, err, cache = run(pkv, w, max_kv=2200)
+    assert err == 0
+    check_append(w, 0, cache)
+    check_against_oracle(w, 0, out, lse, cache)
+
+
 def test_tcgen05_tile_ring_window_and_padding(pkv):
     """The tcgen05 tile over ring storage with a window, and with left padding."""
     w = U.nan_tails(workloads.long_context(S=3, kv_len=9000, window=700, ring_rows=720, seed=31, q_heads=64,
