@@ -3,13 +3,13 @@
 // The row class of speculative verify and chunked steps: one (segment, kv
 // head) carries G * q_len query rows, up to 128 (GQA 64:8 with 16 draft
 // tokens), so the products Q K^T and P V are real contractions.  They run on
-// the 5th-generation tensor cores: one thread issues tcgen05.mma (bf16 in,
-// fp32 accumulate) with K and V in shared memory and Q, S, P and O in
-// tensor memory (TMEM); the softmax threads read S from TMEM and write P
-// back over it.  Same launch shape, key split and semantics as attend_kernel
-// (grid (C, kv_heads, segments); the C CTAs of a range are one cluster and
-// merge through distributed shared memory with merge_rows, pushing into the
-// stage area each CTA has finished with).
+// the 5th-generation tensor cores: two issuing threads (one for S, one for
+// P V) run tcgen05.mma (bf16 in, fp32 accumulate) with Q, K and V in shared
+// memory and S, P and O in tensor memory (TMEM); the softmax threads read S
+// from TMEM and write P back over it.  Same semantics and key split as
+// attend_kernel (grid (C, kv_heads, segments); the C CTAs of a range are one
+// cluster and merge through distributed shared memory, each CTA pushing rows
+// into the stage area of the CTA that finishes them).
 //
 // Per CTA (448 threads):
 //   warps 0-7   softmax: row t of the tile (TMEM lane t) belongs to warps
@@ -18,10 +18,10 @@
 //               accumulator (O_0 for keys 0-31 of every stage, O_1 for
 //               32-63), so the halves never wait for each other inside the
 //               loop; they are combined once, in the epilogue.  The warps
-//               also put Q into TMEM, write P over the S columns they have
-//               read, and after the loop write their rows out (one CTA per
-//               range) or push them to the CTA of the cluster that merges
-//               those rows;
+//               also stage Q in shared memory, write P over the S columns
+//               they have read, and after the loop write their rows out (one
+//               CTA per range) or push them to the CTA of the cluster that
+//               merges those rows;
 //   warps 8, 11 K loads, alternate stages: 4 pages (64 keys) per stage,
 //               each page as two 64-column TMA boxes, so a stage is one
 //               K-major tile of 64 keys (128-byte swizzle) for Q K^T; a stage
@@ -32,9 +32,8 @@
 //   warp 9      S products: fixes this step's K rows into the stage (taken
 //               from k_new, appended to the cache), issues S(j) = Q K_j^T
 //               (M = 128, N = 64, A = Q from shared memory, 8 steps over
-//               head_dim)
-//               once P V(j - NB) has freed its TMEM buffer; also owns the
-//               TMEM allocation;
+//               head_dim) once P V(j - NB) has freed its TMEM buffer; also
+//               owns the TMEM allocation;
 //   warp 13     P V products: fixes edge V pages (stale rows zeroed, this
 //               step's rows from v_new, appended), and once P(j) is in TMEM
 //               issues O_0 += P(j) V(j) over keys 0-31 and O_1 += ... over
@@ -43,20 +42,24 @@
 // One thread issuing every copy, or every product, was the limit: a warp's
 // later instructions wait behind its tensor-core and TMA issues, so two
 // loaders per stream and separate S and P V issuers keep each queue short.
-// TMEM (512 columns allocated): S / P in NB = 2 buffers of 64 columns from
+// TMEM (512 columns allocated): S / P in NB = 3 buffers of 64 columns from
 // column 0 (each half's P as bf16 pairs in the first 16 of its own 32 S
 // columns), then O_0 and O_1 (128 columns each).  Q sits in shared memory
 // (K-major, 128-byte swizzle): a product whose A operand comes from TMEM
-// issues at 117 cycles against 67 from shared memory (N <= 128), and the
-// S products were the tile's pacing work.
-// Shared memory holds Q (32 KB) and the K and V stages: 11 stages (176 KB)
-// of loads in flight.
+// issues at 117 cycles against 67 from shared memory (N <= 128).  Shared
+// memory holds Q (32 KB) and the K and V stages: 11 stages (176 KB) of loads
+// in flight.
+//
+// Scheduling: a CTA's fixed cost (first page loads, cluster merge) is worth
+// about 15 groups of 64 keys, so with few segments the CTAs take ranges
+// longest first, a range of at most kSoloGroups groups runs on one CTA
+// without a merge, and the planner aims at one wave of CTAs.
 //
 // The online softmax keeps each half row in one thread (no cross-lane
 // reduction) and raises its reference maximum lazily: only when a score
 // exceeds it by more than 2^8, and then its O is rescaled in TMEM after the
-// previous P V has landed.  Every wait is bounded; a timeout poisons the CTA's output
-// (PKV_ERR_TIMEOUT), drains what is in flight and frees TMEM.
+// previous P V has landed.  Every wait is bounded; a timeout poisons the
+// CTA's output (PKV_ERR_TIMEOUT), drains what is in flight and frees TMEM.
 //
 // Semantics follow the segment-table attention of ExecuTorch PR #24072
 // (triton::sdpa_varlen) over the paged layout of vLLM-Omni's SenseNova-U1
