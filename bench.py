@@ -70,33 +70,63 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons every 10 ms, each sample stamped
+    on arrival; the summary keeps the samples that arrived inside the marked
+    timed region (or, when that region is shorter than the sampling
+    interval, the one nearest to it)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.proc = None
+    def __init__(self, gpu_index: int, interval_ms: int = 10):
+        import threading
+        self.proc, self.samples, self.t0, self.t1 = None, [], None, None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                          "-lms", str(interval_ms), "-i", str(gpu_index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
+            return
+        first = threading.Event()
+
+        def read():
+            for line in self.proc.stdout:
+                self.samples.append((time.perf_counter(), line))
+                first.set()
+
+        self.reader = threading.Thread(target=read, daemon=True)
+        self.reader.start()
+        first.wait(timeout=5.0)  # sampling is running before the region starts
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_stop(self):
+        self.t1 = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
             return None
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            self.proc.wait()
+        self.reader.join(timeout=5)
+        t0 = self.t0 if self.t0 is not None else -math.inf
+        t1 = self.t1 if self.t1 is not None else math.inf
+        inside = [line for t, line in self.samples if t0 <= t <= t1]
+        where = "inside the timed region"
+        if not inside and self.samples:  # region shorter than the interval: the nearest sample
+            mid = (t0 + t1) / 2 if math.isfinite(t0) and math.isfinite(t1) else 0.0
+            inside = [min(self.samples, key=lambda x: abs(x[0] - mid))[1]]
+            where = "nearest to the timed region (shorter than the sampling interval)"
         sms, maxes, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in inside:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -111,7 +141,7 @@ class ClockSampler:
         if not sms:
             return None
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
-                "samples": len(sms)}
+                "samples": len(sms), "samples_taken": where}
 
 
 def dist_env():
@@ -161,7 +191,7 @@ def make_runner(pkv, L: int, seed: int, device, advance: bool = False, bucket: i
     return runner, w
 
 
-def time_steps(runner, steps: int, warmup: int, flush, stream):
+def time_steps(runner, steps: int, warmup: int, flush, stream, sampler=None):
     import torch
     graph = runner.graph_for()
     for _ in range(warmup):
@@ -169,12 +199,16 @@ def time_steps(runner, steps: int, warmup: int, flush, stream):
         graph.replay()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if sampler is not None:
+        sampler.mark_start()
     for a, b in evs:
         flush()
         a.record(stream)
         graph.replay()
         b.record(stream)
     torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.mark_stop()
     return [a.elapsed_time(b) for a, b in evs]
 
 
@@ -439,7 +473,7 @@ def gpu_arm(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(device.index or 0)
-    times = time_steps(runner, args.steps, args.warmup, flush, stream)
+    times = time_steps(runner, args.steps, args.warmup, flush, stream, sampler=sampler)
     clocks = sampler.stop()
     torch.cuda.synchronize()
     if world > 1:
