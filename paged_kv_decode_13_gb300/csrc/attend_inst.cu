@@ -75,9 +75,10 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #else
     {
-        // one CTA per SM at this width whatever the stage count: three
-        // stages per warp keep more pages in flight (long ranges gain 4 %)
-        if (rc >= 4) return dinfo<DecCfg<256, 4, 3>>();
+        // one CTA per SM at this width whatever the split: six warps of two
+        // stages (192 KB in flight) spread the per-page MMA latency over
+        // more warps than four of three (long ranges: 327 against 332 us)
+        if (rc >= 4) return dinfo<DecCfg<256, 6, 2>>();
         if (rc == 0) return CFG(B16, 1, 4, 2, true);
         if (rc == 1) return CFG(B16, 2, 2, 3, true);
         if (rc == 2) return CFG(B16, 4, 1, 4, true);
@@ -104,7 +105,7 @@ AttnKernel PICK_NAME(PKV_INST_VARIANT, PKV_INST_DP)(int rc) {
     }
 #else
     {
-        if (rc >= 4) return dinfo<DecCfg<256, 4, 3, true>>();
+        if (rc >= 4) return dinfo<DecCfg<256, 6, 2, true>>();
         if (rc == 0) return CFG(B16, 1, 4, 2, false);
         if (rc == 1) return CFG(B16, 2, 2, 3, false);
         return CFG(B16, 4, 1, 4, false);

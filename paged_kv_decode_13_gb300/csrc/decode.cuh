@@ -109,8 +109,10 @@ __device__ __forceinline__ int rs_halve(float (&x)[16], int lane_bits, int m) {
     return upper ? HALF : 0;
 }
 
+// Register budget for the CTAs that fit on one SM by shared memory (two at
+// head_dim 64 / 128, one at 256).
 template <class C>
-__global__ void __launch_bounds__(C::kThreads, 2) decode_kernel(const __grid_constant__ AttendParams p) {
+__global__ void __launch_bounds__(C::kThreads, C::kCtasPerSm) decode_kernel(const __grid_constant__ AttendParams p) {
     using T = __nv_bfloat16;
     namespace cg = cooperative_groups;
     constexpr int DP = C::DP, KW = C::KW, NST = C::NST, NT = C::kThreads, KT = C::kKT, LD = C::kPartLd;
