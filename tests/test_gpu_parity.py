@@ -604,6 +604,25 @@ def test_tcgen05_longest_first_order(pkv, S):
     check_against_oracle(w, 0, out, lse, cache)
 
 
+@pytest.mark.parametrize("kv_len,page", [(2000, 40), (2000, 100), (1000, 30)])
+def test_tcgen05_bad_block_poisons_only_its_segment(pkv, kv_len, page):
+    """A block id out of range inside one segment's key range (in one CTA of
+    a range split over a cluster, or in a range run by one CTA alone):
+    that segment's rows are zero with lse -inf and PKV_ERR_BLOCK is set; the
+    other segments still match the oracle."""
+    w = U.nan_tails(workloads.spec_verify(S=3, max_q=16, len_lo=kv_len, len_hi=kv_len, causal=True, seed=page,
+                                          q_heads=64))
+    bt = w.block_table.clone()
+    bt[1, page] = 1 << 20
+    w.block_table = bt
+    out, lse, err, cache = run(pkv, w, max_kv=kv_len)
+    assert err & pkv.ERR_BLOCK
+    rows = U.rows_of(w, [1])
+    assert not out[rows].abs().sum().item()
+    assert bool(torch.isinf(lse[rows]).all())
+    check_against_oracle(w, 0, out, lse, cache, segs=[0, 2])
+
+
 def test_tcgen05_tile_ring_window_and_padding(pkv):
     """The tcgen05 tile over ring storage with a window, and with left padding."""
     w = U.nan_tails(workloads.long_context(S=3, kv_len=9000, window=700, ring_rows=720, seed=31, q_heads=64,
