@@ -187,10 +187,14 @@ int pkv_append(const pkv_cache *cache, int32_t layer,
  * memory in the same launch, so no workspace is needed (workspace NULL,
  * workspace_bytes 0; see pkv_attend_workspace_bytes for the other mode).  0 picks the count
  * from the launch shape: a power of two aiming at about three waves of
- * resident CTAs, the largest cluster the device can co-schedule below it,
- * and, for kernels that fit once per SM with few (segment, kv head) ranges,
- * the cluster size that needs the fewest waves of clusters resident at once.
- * A larger count than the segment has 16-token pages leaves CTAs idle.
+ * resident CTAs (one wave for the tcgen05 tile of wide bf16 groups), the
+ * largest cluster the device can co-schedule below it, and, for kernels
+ * that fit once per SM with few (segment, kv head) ranges, the cluster size
+ * that needs the fewest waves of clusters resident at once.  The tcgen05
+ * tile also runs a range of at most 24 groups of 64 keys on one CTA of its
+ * cluster, and with up to 64 segments takes the ranges longest first; the
+ * results do not depend on either.  A larger count than the segment has
+ * 16-token pages leaves CTAs idle.
  *
  * flags: PKV_FLAG_SIMT selects the CUDA-core kernels for bf16 (fp32 always
  * uses them): at most 8 query rows per kv head take the decode kernel's
