@@ -75,8 +75,15 @@ def _touched(w) -> tuple:
     return ids, small
 
 
-@pytest.mark.parametrize("key", [c[0] for c in bench.CONFIGS])
-def test_benched_workload_matches_oracle(pkv, key):
+# Every workload with the default kernels, and the other kernels a caller can
+# pick by flag at the same sizes: the CUDA-core decode variant (PKV_FLAG_SIMT,
+# head_dim 128 and 256) and the mma.sync tile for wide groups
+# (PKV_FLAG_MMA_SYNC).
+CASES = [(c[0], 0) for c in bench.CONFIGS] + [("batched", 1), ("long_context_ring", 1), ("verify_causal", 8)]
+
+
+@pytest.mark.parametrize("key,flags", CASES)
+def test_benched_workload_matches_oracle(pkv, key, flags):
     _, name, gen, kw = next(c for c in bench.CONFIGS if c[0] == key)
     dev = torch.device("cuda")
     w = getattr(workloads, gen)(seed=0, device=dev, **kw)
@@ -89,7 +96,7 @@ def test_benched_workload_matches_oracle(pkv, key):
     err = pkv.new_err_flags(dev)
     max_kv = int(w.seq_info[:, 3].max().item())
     pkv.append_attend(cache, 0, w.q[0], w.k_new[0], w.v_new[0], w.seq_info, out, err, w.max_q_len, max_kv, w.scale,
-                      w.causal, w.window, lse=lse)
+                      w.causal, w.window, lse=lse, flags=flags)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"{name}: device error flags {int(err.item()):#x}"
     assert bool(torch.isfinite(out).all())
