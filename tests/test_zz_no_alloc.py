@@ -139,3 +139,33 @@ def test_noalloc_batch_of_32_matches_oracle_over_two_steps(pkv):
         diff = float(np.abs(U.f64(res[1][0]) - ref).max())
         assert diff <= U.TOL[torch.bfloat16], (step, diff)
         assert float(np.abs(U.f64(res[1][1]) - ref_lse).max()) <= U.TOL[torch.bfloat16]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [True, False])
+def test_noalloc_wide_groups_match_append_attend(pkv, causal):
+    """More than 8 rows per kv head (speculative verify: the tcgen05 tile,
+    merged in the cluster): the call needs none of the library's scratch,
+    and it equals pkv_append_attend bit for bit and the oracle."""
+    w = U.nan_tails(workloads.spec_verify(S=6, max_q=16, len_lo=16, len_hi=2500, causal=causal, seed=57,
+                                          q_heads=64))
+    dev = torch.device("cuda")
+    caches = [U.device_cache(pkv, w), U.device_cache(pkv, w)]
+    res = []
+    for i, cache in enumerate(caches):
+        out = torch.zeros(w.total_rows, w.q_heads, w.head_dim, device=dev)
+        lse = torch.zeros(w.total_rows, w.q_heads, device=dev)
+        err = pkv.new_err_flags()
+        args = (cache, 0, w.q[0].to(dev), w.k_new[0].to(dev), w.v_new[0].to(dev), w.seq_info.to(dev), out, err,
+                w.max_q_len, 2500, w.scale, causal)
+        if i == 0:
+            pkv.append_attend(*args, lse=lse)
+        else:
+            pkv.append_attend_noalloc(*args, lse=lse)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        res.append((out, lse))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+    assert U.pool_bytes(caches[0].k[0]) == U.pool_bytes(caches[1].k[0])
+    ref, ref_lse = U.oracle_attend(w, 0)
+    assert float(np.abs(U.f64(res[1][0]) - ref).max()) <= U.TOL[torch.bfloat16]
